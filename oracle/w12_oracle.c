@@ -1,0 +1,327 @@
+/*
+ * W12 CPU oracle — TEST INFRASTRUCTURE ONLY.
+ *
+ * A plain, slow, scalar restatement of the W12 lossless 12-bit weight format and of the GEMM,
+ * argmax and Q-view computations built on it, in fp64 where floating point is involved. It is
+ * used by the test-suite, by the smoke check and by the benchmark's CPU baseline only; the
+ * product path (the CUDA library) never calls it, and it shares no code with that path.
+ *
+ * Sources (cited by page title and section):
+ *   [SP]    "SpecPilot: Autonomous Algorithm Discovery and Systems Optimization for Speculative
+ *           Decoding" (arXiv 2611.02501).
+ *   [SP-R]  the jaehun.me review of the same paper.
+ *
+ *   - format (planes A/E/B, per-channel 16-binade window, escapes, 12 KB 128x64 records with the
+ *     8-bit view first): [SP] §4.1 "W12: A Lossless 12-bit Weight Format", Fig. 5a; [SP-R] §4.1.
+ *   - load-time bit-for-bit check:  [SP] §4.1; Table A2 caption.
+ *   - GEMM over exactly decoded weights: [SP] §4.1, Fig. 5b.
+ *   - greedy argmax: [SP] §2.1 "Speculative Decoding".
+ *   - Q view (A+E only, dropped mantissa bits at their midpoint): [SP] §4.3 "Zero-copy Q pass",
+ *     Fig. 7.
+ *
+ * Physical details the pages leave open (window tie rule, placeholders, byte and nibble order,
+ * per-record escape index) follow the build's written W12 specification; every function states
+ * the rule it implements. Parity status: every function here is pinned by a CPU test
+ * (round trip over all 65,536 bf16 patterns, brute-force window search, exact rational GEMM,
+ * brute-force argmax, hand-derived byte fixtures); none is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define W12O_TILE_N 128
+#define W12O_TILE_K 64
+#define W12O_RECORD_BYTES 12288
+#define W12O_VIEW_BYTES 8192
+
+/* ---- bf16 field helpers ------------------------------------------------------------------ */
+
+static int bf_sign(uint16_t u) { return u >> 15; }
+static int bf_exp(uint16_t u) { return (u >> 7) & 0xFF; }
+static int bf_mhi(uint16_t u) { return (u >> 4) & 0x7; }
+static int bf_mlo(uint16_t u) { return u & 0xF; }
+static int bf_is_normal(uint16_t u) { int e = bf_exp(u); return e >= 1 && e <= 254; }
+
+/* exact value of a bf16 pattern as a double (a bf16 is the top half of an fp32) */
+double w12o_bf16_to_double(uint16_t u) {
+    uint32_t bits = (uint32_t)u << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* ---- window choice: [SP] §4.1 ("for each channel n, W12 selects the 16-binade window
+ *      [E_n-15, E_n] that covers the most weights"); ties -> smallest E_n ---------------- */
+
+int w12o_window(const uint16_t *row, int K) {
+    long hist[256];
+    for (int e = 0; e < 256; ++e) hist[e] = 0;
+    for (int k = 0; k < K; ++k)
+        if (bf_is_normal(row[k])) hist[bf_exp(row[k])] += 1;
+    int best_E = 16;
+    long best_cover = -1;
+    for (int E = 16; E <= 254; ++E) {
+        long cover = 0;
+        for (int e = E - 15; e <= E; ++e) cover += hist[e];
+        if (cover > best_cover) { /* strict: the first (smallest) maximiser wins */
+            best_cover = cover;
+            best_E = E;
+        }
+    }
+    return best_E;
+}
+
+/* Is weight u stored in-window for base E_n? ([SP] §4.1: outside-window weights, zeros and
+ * denormals become escapes; Inf/NaN have e = 255 and are outside every window.) */
+static int in_window(uint16_t u, int En) {
+    int e = bf_exp(u);
+    return bf_is_normal(u) && e >= En - 15 && e <= En;
+}
+
+/* Planes of one real weight: E offset, m_hi, low nibble, sign. Escapes get the placeholder. */
+static void planes_of(uint16_t u, int En, int *E, int *mhi, int *b, int *s) {
+    *s = bf_sign(u);
+    if (in_window(u, En)) {
+        *E = bf_exp(u) - (En - 15);
+        *mhi = bf_mhi(u);
+        *b = bf_mlo(u);
+    } else if (bf_exp(u) == 255 || (bf_is_normal(u) && bf_exp(u) > En)) {
+        *E = 15; *mhi = 7; *b = 15;          /* above the window: clamp to its top */
+    } else {
+        *E = 0; *mhi = 0; *b = 0;            /* zero, subnormal or below: clamp to its bottom */
+    }
+}
+
+/* ---- record byte placement (the build's specification of the 12 KB record) --------------- */
+
+static size_t view_offset(int nl, int kl) { return (size_t)2048 * (kl >> 4) + 16 * nl + (kl & 15); }
+static size_t b_word_offset(int nl, int kl) {
+    return W12O_VIEW_BYTES + (size_t)2048 * (kl >> 5) + 16 * nl + 4 * ((kl >> 3) & 3);
+}
+static int b_nibble_pos(int kl) { int i = kl & 7; return (i >> 1) + 4 * (i & 1); }
+
+static uint32_t load_u32le(const uint8_t *p) {
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+static void store_u32le(uint8_t *p, uint32_t v) {
+    p[0] = v & 0xFF; p[1] = (v >> 8) & 0xFF; p[2] = (v >> 16) & 0xFF; p[3] = (v >> 24) & 0xFF;
+}
+
+/* ---- sizes ------------------------------------------------------------------------------- */
+
+/* Counts of the canonical escape list and of the padded per-record index. */
+void w12o_count(const uint16_t *w, int N, int K, int64_t *n_esc, int64_t *n_rec_esc) {
+    int n_tiles = (N + W12O_TILE_N - 1) / W12O_TILE_N;
+    int k_tiles = (K + W12O_TILE_K - 1) / W12O_TILE_K;
+    int *En = (int *)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+    for (int n = 0; n < N; ++n) En[n] = w12o_window(w + (size_t)n * K, K);
+    int64_t total = 0, total_rec = 0;
+    for (int nt = 0; nt < n_tiles; ++nt)
+        for (int kt = 0; kt < k_tiles; ++kt) {
+            int64_t c = 0;
+            for (int nl = 0; nl < W12O_TILE_N; ++nl) {
+                int n = nt * W12O_TILE_N + nl;
+                if (n >= N) break;
+                for (int kl = 0; kl < W12O_TILE_K; ++kl) {
+                    int k = kt * W12O_TILE_K + kl;
+                    if (k >= K) break;
+                    if (!in_window(w[(size_t)n * K + k], En[n])) c += 1;
+                }
+            }
+            total += c;
+            total_rec += (c + 3) / 4 * 4;
+        }
+    free(En);
+    *n_esc = total;
+    *n_rec_esc = total_rec;
+}
+
+/* ---- encoder: [SP] §4.1 and Fig. 5a ------------------------------------------------------- */
+
+void w12o_encode(const uint16_t *w, int N, int K,
+                 uint8_t *records, uint8_t *base_exp,
+                 uint32_t *esc_off, uint32_t *esc_k, uint16_t *esc_bits,
+                 uint32_t *rec_esc_off, uint32_t *rec_esc) {
+    int n_tiles = (N + W12O_TILE_N - 1) / W12O_TILE_N;
+    int k_tiles = (K + W12O_TILE_K - 1) / W12O_TILE_K;
+
+    /* step 1: window base per channel */
+    for (int n = 0; n < n_tiles * W12O_TILE_N; ++n)
+        base_exp[n] = (uint8_t)(n < N ? w12o_window(w + (size_t)n * K, K) : 16);
+
+    /* step 2: canonical per-channel escape list, k ascending */
+    uint32_t pos = 0;
+    for (int n = 0; n < N; ++n) {
+        esc_off[n] = pos;
+        for (int k = 0; k < K; ++k) {
+            uint16_t u = w[(size_t)n * K + k];
+            if (!in_window(u, base_exp[n])) {
+                esc_k[pos] = (uint32_t)k;
+                esc_bits[pos] = u;
+                pos += 1;
+            }
+        }
+    }
+    esc_off[N] = pos;
+
+    /* step 3: records (planes) and the per-record escape index */
+    memset(records, 0, (size_t)n_tiles * k_tiles * W12O_RECORD_BYTES);
+    uint32_t rpos = 0;
+    for (int nt = 0; nt < n_tiles; ++nt)
+        for (int kt = 0; kt < k_tiles; ++kt) {
+            size_t r = (size_t)nt * k_tiles + kt;
+            uint8_t *rec = records + r * W12O_RECORD_BYTES;
+            rec_esc_off[r] = rpos;
+            for (int nl = 0; nl < W12O_TILE_N; ++nl)
+                for (int kl = 0; kl < W12O_TILE_K; ++kl) {
+                    int n = nt * W12O_TILE_N + nl, k = kt * W12O_TILE_K + kl;
+                    if (n >= N || k >= K) continue; /* padding: byte 0, nibble 0 */
+                    uint16_t u = w[(size_t)n * K + k];
+                    int E, mhi, b, s;
+                    planes_of(u, base_exp[n], &E, &mhi, &b, &s);
+                    rec[view_offset(nl, kl)] = (uint8_t)((E << 4) | (mhi << 1) | s);
+                    uint8_t *bw = rec + b_word_offset(nl, kl);
+                    uint32_t word = load_u32le(bw);
+                    word |= (uint32_t)b << (4 * b_nibble_pos(kl));
+                    store_u32le(bw, word);
+                    if (!in_window(u, base_exp[n])) {
+                        rec_esc[rpos] = (uint32_t)(nl * W12O_TILE_K + kl) | ((uint32_t)u << 16);
+                        rpos += 1;
+                    }
+                }
+            while (rpos % 4 != 0) rec_esc[rpos++] = 0xFFFFFFFFu;
+        }
+    rec_esc_off[(size_t)n_tiles * k_tiles] = rpos;
+}
+
+/* ---- decoder (from records + the per-record index): [SP] §4.1 ----------------------------- */
+
+void w12o_decode(const uint8_t *records, const uint8_t *base_exp,
+                 const uint32_t *rec_esc_off, const uint32_t *rec_esc,
+                 int N, int K, uint16_t *w_out) {
+    int n_tiles = (N + W12O_TILE_N - 1) / W12O_TILE_N;
+    int k_tiles = (K + W12O_TILE_K - 1) / W12O_TILE_K;
+    for (int nt = 0; nt < n_tiles; ++nt)
+        for (int kt = 0; kt < k_tiles; ++kt) {
+            size_t r = (size_t)nt * k_tiles + kt;
+            const uint8_t *rec = records + r * W12O_RECORD_BYTES;
+            for (int nl = 0; nl < W12O_TILE_N; ++nl)
+                for (int kl = 0; kl < W12O_TILE_K; ++kl) {
+                    int n = nt * W12O_TILE_N + nl, k = kt * W12O_TILE_K + kl;
+                    if (n >= N || k >= K) continue;
+                    int V = rec[view_offset(nl, kl)];
+                    int E = V >> 4, mhi = (V >> 1) & 7, s = V & 1;
+                    int b = (load_u32le(rec + b_word_offset(nl, kl)) >> (4 * b_nibble_pos(kl))) & 0xF;
+                    int e = E + base_exp[n] - 15;
+                    w_out[(size_t)n * K + k] = (uint16_t)((s << 15) | (e << 7) | (mhi << 4) | b);
+                }
+            for (uint32_t i = rec_esc_off[r]; i < rec_esc_off[r + 1]; ++i) {
+                uint32_t ent = rec_esc[i];
+                uint32_t p = ent & 0xFFFF;
+                if (p >= (uint32_t)(W12O_TILE_N * W12O_TILE_K)) continue; /* padding entry */
+                int n = nt * W12O_TILE_N + (int)(p / W12O_TILE_K);
+                int k = kt * W12O_TILE_K + (int)(p % W12O_TILE_K);
+                w_out[(size_t)n * K + k] = (uint16_t)(ent >> 16);
+            }
+        }
+}
+
+/* decoder variant that restores escapes from the canonical per-channel list */
+void w12o_decode_csr(const uint8_t *records, const uint8_t *base_exp,
+                     const uint32_t *esc_off, const uint32_t *esc_k, const uint16_t *esc_bits,
+                     int N, int K, uint16_t *w_out) {
+    int k_tiles = (K + W12O_TILE_K - 1) / W12O_TILE_K;
+    for (int n = 0; n < N; ++n)
+        for (int k = 0; k < K; ++k) {
+            int nt = n / W12O_TILE_N, nl = n % W12O_TILE_N, kt = k / W12O_TILE_K, kl = k % W12O_TILE_K;
+            const uint8_t *rec = records + ((size_t)nt * k_tiles + kt) * W12O_RECORD_BYTES;
+            int V = rec[view_offset(nl, kl)];
+            int b = (load_u32le(rec + b_word_offset(nl, kl)) >> (4 * b_nibble_pos(kl))) & 0xF;
+            int e = (V >> 4) + base_exp[n] - 15;
+            w_out[(size_t)n * K + k] = (uint16_t)(((V & 1) << 15) | (e << 7) | (((V >> 1) & 7) << 4) | b);
+        }
+    for (int n = 0; n < N; ++n)
+        for (uint32_t i = esc_off[n]; i < esc_off[n + 1]; ++i)
+            w_out[(size_t)n * K + esc_k[i]] = esc_bits[i];
+}
+
+/* ---- Q view, by definition from W: [SP] §4.3 "Zero-copy Q pass" ----------------------------
+ * sign, exponent offset and top three mantissa bits of the stored planes, low four mantissa
+ * bits set to their midpoint 1000b; escapes keep their placeholder planes. */
+
+void w12o_qview_weights(const uint16_t *w, int N, int K, uint16_t *wq) {
+    for (int n = 0; n < N; ++n) {
+        int En = w12o_window(w + (size_t)n * K, K);
+        for (int k = 0; k < K; ++k) {
+            int E, mhi, b, s;
+            planes_of(w[(size_t)n * K + k], En, &E, &mhi, &b, &s);
+            (void)b;
+            wq[(size_t)n * K + k] = (uint16_t)((s << 15) | ((E + En - 15) << 7) | (mhi << 4) | 8);
+        }
+    }
+}
+
+/* ---- GEMM in fp64: y[m,n] = sum_k x[m,k] w[n,k]  ([SP] §4.1, Fig. 5b) ----------------------
+ * Also returns sum_k |x[m,k] w[n,k]|, the scale of the stated error bound. */
+
+void w12o_gemm(const uint16_t *x, int M, const uint16_t *w, int N, int K,
+               double *y, double *absdot) {
+    #pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        double *wd = (double *)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+        for (int k = 0; k < K; ++k) wd[k] = w12o_bf16_to_double(w[(size_t)n * K + k]);
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0, aacc = 0.0;
+            for (int k = 0; k < K; ++k) {
+                double p = w12o_bf16_to_double(x[(size_t)m * K + k]) * wd[k];
+                acc += p;
+                aacc += fabs(p);
+            }
+            y[(size_t)m * N + n] = acc;
+            if (absdot) absdot[(size_t)m * N + n] = aacc;
+        }
+        free(wd);
+    }
+}
+
+/* the same sum for a list of sampled (m, n) output positions */
+void w12o_gemm_sampled(const uint16_t *x, const uint16_t *w, int K,
+                       const int32_t *ms, const int32_t *ns, int64_t count,
+                       double *y, double *absdot) {
+    #pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < count; ++i) {
+        double acc = 0.0, aacc = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double p = w12o_bf16_to_double(x[(size_t)ms[i] * K + k]) *
+                       w12o_bf16_to_double(w[(size_t)ns[i] * K + k]);
+            acc += p;
+            aacc += fabs(p);
+        }
+        y[i] = acc;
+        absdot[i] = aacc;
+    }
+}
+
+/* ---- argmax per row: [SP] §2.1 (greedy acceptance takes the target's argmax) --------------
+ * top1 = smallest index of the maximum; gap = max - (largest value at any other index);
+ * scale = max |y| over the row. */
+
+void w12o_argmax(const double *y, int M, int N, int32_t *idx, double *val, double *gap,
+                 double *scale) {
+    for (int m = 0; m < M; ++m) {
+        const double *row = y + (size_t)m * N;
+        int best = 0;
+        for (int n = 1; n < N; ++n)
+            if (row[n] > row[best]) best = n;
+        double second = -INFINITY, sc = 0.0;
+        for (int n = 0; n < N; ++n) {
+            if (n != best && row[n] > second) second = row[n];
+            if (fabs(row[n]) > sc) sc = fabs(row[n]);
+        }
+        idx[m] = best;
+        val[m] = row[best];
+        gap[m] = (N > 1) ? row[best] - second : INFINITY;
+        scale[m] = sc;
+    }
+}

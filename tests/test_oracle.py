@@ -1,0 +1,302 @@
+"""CPU pins of the W12 oracle against facts that do not come from the oracle itself.
+
+- the lossless invariant: decode(encode(W)) == W bit for bit (SpecPilot §4.1; Table A2 caption),
+  over all 65,536 bf16 patterns and over synthetic tensors;
+- the window rule against a brute-force count over every candidate base (SpecPilot §4.1);
+- the escape set against its definition, evaluated with float arithmetic on the values;
+- hand-derived bytes of a small ragged tensor (tests/golden/w12_layout_fixture.txt);
+- the fp64 GEMM against exact rational sums; the argmax against Python's own max over rows;
+- the Q view (SpecPilot §4.3) against value-level properties and against a second route through
+  the encoded records.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from lossless_bit_weight_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16_values(u16: np.ndarray) -> np.ndarray:
+    """Exact float64 values of bf16 patterns via numpy's float32 (independent of the oracle)."""
+    return (u16.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ---------------------------------------------------------------- lossless round trip
+
+
+def test_roundtrip_all_65536_patterns(orc):
+    w = synth.all_bf16_patterns(256)  # 256 channels, each a contiguous run of 256 patterns
+    e = orc.encode(w)
+    assert np.array_equal(orc.decode(e), w)
+    assert np.array_equal(orc.decode_csr(e), w)
+
+
+def test_roundtrip_all_patterns_shuffled_rows(orc):
+    rng = np.random.default_rng(7)
+    w = synth.all_bf16_patterns(512).reshape(-1)
+    w = rng.permutation(w).reshape(128, 512)  # every channel mixes NaN, Inf, ±0, subnormals
+    e = orc.encode(w)
+    assert np.array_equal(orc.decode(e), w)
+    assert np.array_equal(orc.decode_csr(e), w)
+
+
+@pytest.mark.parametrize("N,K", [(512, 256), (300, 200), (1, 8), (129, 65)])
+def test_roundtrip_synthetic(orc, N, K):
+    w = synth.bits(synth.weights(N, K, synth.TINY, seed=11 + N + K))
+    e = orc.encode(w)
+    assert np.array_equal(orc.decode(e), w)
+    assert np.array_equal(orc.decode_csr(e), w)
+
+
+# ---------------------------------------------------------------- window rule
+
+
+def brute_force_window(vals: np.ndarray) -> int:
+    """Largest coverage by direct counting over E in [16, 254]; ties -> smallest E.
+
+    Works on values: a weight is normal when 2^-126 <= |v| < inf, its binade is floor(log2|v|)."""
+    a = np.abs(vals)
+    normal = np.isfinite(a) & (a >= 2.0 ** -126)
+    binade = np.floor(np.log2(a[normal])).astype(np.int64) + 127  # biased exponent
+    best_E, best = None, -1
+    for E in range(16, 255):
+        c = int(np.count_nonzero((binade >= E - 15) & (binade <= E)))
+        if c > best:
+            best, best_E = c, E
+    return best_E
+
+
+def test_window_vs_brute_force(orc):
+    rng = np.random.default_rng(3)
+    rows = [synth.bits(synth.weights(4, 512, synth.TINY, seed=s)) for s in range(3)]
+    rows = [r for blk in rows for r in blk]
+    # wide spreads so the window really has to choose
+    for _ in range(12):
+        ex = rng.integers(60, 200, size=300)
+        v = np.ldexp(rng.uniform(1, 2, size=300), ex - 127) * rng.choice([-1, 1], size=300)
+        rows.append(synth.bits(torch.tensor(v, dtype=torch.float32).to(torch.bfloat16)))
+    rows.append(np.zeros(64, np.uint16))                       # no normal weight at all
+    rows.append(np.full(64, 0x7FC0, np.uint16))                # all NaN
+    rows.append(np.full(64, 0x0001, np.uint16))                # all subnormal
+    rows.append(np.array([0x0080] * 10 + [0x7F7F] * 10, np.uint16))  # extreme binades, a tie
+    for r in rows:
+        assert orc.window(r) == brute_force_window(bf16_values(r)), r[:8]
+
+
+def test_window_ties_take_smallest_base(orc):
+    # all weights in binade 127: every E in [127, 142] covers them all -> E_n = 127
+    assert orc.window(np.full(16, 0x3F80, np.uint16)) == 127
+    # two equal groups 20 binades apart: both windows cover 8; the lower one wins
+    row = np.array([0x3F80] * 8 + [0x4980] * 8, np.uint16)  # e=127 and e=147
+    assert orc.window(row) == 127
+
+
+# ---------------------------------------------------------------- escapes
+
+
+def test_escape_set_matches_definition(orc):
+    w = synth.bits(synth.weights(256, 320, synth.TINY, seed=5))
+    w[3, :] = 0                      # an all-zero channel
+    w[4, 10] = 0x7F80                # +Inf
+    w[5, 11] = 0xFFC1                # NaN with payload and sign
+    w[6, 12] = 0x0003                # subnormal
+    e = orc.encode(w)
+    vals = bf16_values(w)
+    n_expected = 0
+    for n in range(w.shape[0]):
+        En = int(e.base_exp[n])
+        a = np.abs(vals[n])
+        with np.errstate(divide="ignore", invalid="ignore"):
+            binade = np.floor(np.log2(a)) + 127
+        inside = np.isfinite(a) & (a >= 2.0 ** -126) & (binade >= En - 15) & (binade <= En)
+        ks = np.nonzero(~inside)[0]
+        lo, hi = int(e.esc_off[n]), int(e.esc_off[n + 1])
+        assert np.array_equal(e.esc_k[lo:hi], ks)
+        assert np.array_equal(e.esc_bits[lo:hi], w[n, ks])
+        n_expected += ks.size
+    assert e.esc_k.size == n_expected
+    assert int(e.base_exp[3]) == 16  # no normal weight: every window covers 0 -> smallest base
+
+
+def test_per_record_index_is_a_regrouping_of_the_csr(orc):
+    w = synth.bits(synth.weights(300, 200, synth.TINY, seed=9))
+    e = orc.encode(w)
+    from_csr = set()
+    for n in range(e.N):
+        for i in range(e.esc_off[n], e.esc_off[n + 1]):
+            from_csr.add((n, int(e.esc_k[i]), int(e.esc_bits[i])))
+    from_rec = set()
+    R = e.n_tiles * e.k_tiles
+    for r in range(R):
+        nt, kt = divmod(r, e.k_tiles)
+        seg = e.rec_esc[e.rec_esc_off[r]:e.rec_esc_off[r + 1]]
+        assert seg.size % 4 == 0
+        real = seg[seg != 0xFFFFFFFF]
+        pos = real & 0xFFFF
+        assert np.all(np.diff(pos.astype(np.int64)) > 0)
+        for ent in real:
+            p = int(ent) & 0xFFFF
+            from_rec.add((nt * 128 + p // 64, kt * 64 + p % 64, int(ent) >> 16))
+    assert from_csr == from_rec
+
+
+# ---------------------------------------------------------------- golden bytes
+
+
+def _parse_fixture(path):
+    lines = []
+    with open(path) as f:
+        for ln in f:
+            ln = ln.split("#", 1)[0].strip()
+            if ln:
+                lines.append(ln.split())
+    return lines
+
+
+def test_golden_layout_fixture(orc):
+    lines = _parse_fixture(os.path.join(GOLDEN, "w12_layout_fixture.txt"))
+    w = None
+    for t in lines:
+        if t[0] == "shape":
+            w = np.zeros((int(t[1]), int(t[2])), np.uint16)
+        elif t[0] == "fill":
+            w[:] = int(t[1], 16)
+        elif t[0] == "row":
+            w[int(t[1]), :] = int(t[2], 16)
+        elif t[0] == "set":
+            w[int(t[1]), int(t[2])] = int(t[3], 16)
+    e = orc.encode(w)
+    rec = e.records.reshape(-1, orc.RECORD_BYTES)
+    checked = 0
+    for t in lines:
+        k = t[0]
+        if k == "expect":
+            what, a = t[1], t[2:]
+            if what == "base_exp":
+                assert e.base_exp[int(a[0])] == int(a[1]), t
+            elif what == "view":
+                assert rec[int(a[0]), int(a[1])] == int(a[2], 16), t
+            elif what == "bnib":
+                off = int(a[1])
+                word = int.from_bytes(bytes(rec[int(a[0]), off:off + 4]), "little")
+                assert (word >> (4 * int(a[2]))) & 0xF == int(a[3], 16), t
+            elif what == "n_esc":
+                assert e.esc_k.size == int(a[0]), t
+            elif what == "esc_off":
+                assert e.esc_off[int(a[0])] == int(a[1]), t
+            elif what == "csr":
+                i = int(a[0])
+                assert (e.esc_k[i], e.esc_bits[i]) == (int(a[1]), int(a[2], 16)), t
+            elif what == "rec_esc_off":
+                assert list(e.rec_esc_off) == [int(v) for v in a], t
+            elif what == "rec_entry":
+                assert e.rec_esc[int(a[0])] == int(a[1], 16), t
+            else:
+                raise AssertionError(t)
+            checked += 1
+    assert checked > 40
+    assert np.array_equal(orc.decode(e), w)
+
+
+# ---------------------------------------------------------------- GEMM
+
+
+def _exact_dot(xr, wr):
+    s = Fraction(0)
+    for a, b in zip(xr, wr):
+        s += Fraction(float(a)) * Fraction(float(b))
+    return s
+
+
+def test_gemm_vs_exact_rational(orc):
+    rng = np.random.default_rng(1)
+    M, N, K = 3, 5, 37
+    x = synth.bits(torch.tensor(rng.standard_normal((M, K)), dtype=torch.float32).to(torch.bfloat16))
+    w = synth.bits(synth.weights(N, K, synth.TINY, seed=2))
+    w[0, 0] = 0x7F7F            # largest finite bf16
+    w[1, :4] = [0x0001, 0x8001, 0x0080, 0x0000]  # subnormals, smallest normal, zero
+    x[2, :] = x[1, ::-1]        # a row with a different summation profile
+    y, a = orc.gemm(x, w)
+    xv, wv = bf16_values(x), bf16_values(w)
+    for m in range(M):
+        for n in range(N):
+            exact = _exact_dot(xv[m], wv[n])
+            absexact = sum(abs(Fraction(float(p))) for p in xv[m] * wv[n])
+            # K sequential fp64 additions of exact products: |err| <= K * 2^-53 * sum|p|
+            assert abs(Fraction(y[m, n]) - exact) <= K * Fraction(1, 2 ** 53) * absexact
+            assert a[m, n] == pytest.approx(float(absexact), rel=1e-12)
+
+
+def test_gemm_sampled_matches_full(orc):
+    x = synth.bits(synth.activations(4, 96, seed=4))
+    w = synth.bits(synth.weights(40, 96, synth.TINY, seed=4))
+    y, a = orc.gemm(x, w)
+    ms = np.array([0, 3, 2, 1, 3], np.int32)
+    ns = np.array([0, 39, 17, 5, 5], np.int32)
+    ys, as_ = orc.gemm_sampled(x, w, ms, ns)
+    assert np.array_equal(ys, y[ms, ns]) and np.array_equal(as_, a[ms, ns])
+
+
+# ---------------------------------------------------------------- argmax
+
+
+def test_argmax_vs_python_max(orc):
+    rng = np.random.default_rng(8)
+    y = rng.standard_normal((6, 50))
+    y[1, 7] = y[1, 30] = 9.0          # exact tie for the maximum -> index 7, gap 0
+    y[2, :] = -1.0                    # constant row
+    y[3, 49] = 100.0                  # maximum at the end
+    y[4, :] = -np.abs(y[4, :])        # all negative
+    idx, val, gap, sc = orc.argmax(y)
+    for m in range(y.shape[0]):
+        row = list(y[m])
+        best = max(range(len(row)), key=lambda n: (row[n], -n))
+        rest = [row[n] for n in range(len(row)) if n != best]
+        assert idx[m] == best
+        assert val[m] == row[best]
+        assert gap[m] == row[best] - max(rest)
+        assert sc[m] == max(abs(v) for v in row)
+    assert idx[1] == 7 and gap[1] == 0.0
+    one = orc.argmax(np.array([[3.5]]))
+    assert one[0][0] == 0 and math.isinf(one[2][0])
+
+
+# ---------------------------------------------------------------- Q view
+
+
+def test_qview_value_properties(orc):
+    w = synth.bits(synth.weights(256, 256, synth.TINY, seed=12))
+    wq = orc.qview_weights(w)
+    e = orc.encode(w)
+    v, vq = bf16_values(w), bf16_values(wq)
+    for n in range(w.shape[0]):
+        En = int(e.base_exp[n])
+        lo_b, hi_b = 2.0 ** (En - 15 - 127), 2.0 ** (En - 127 + 1)
+        a = np.abs(v[n])
+        inside = (a >= lo_b) & (a < hi_b) & (a >= 2.0 ** -126)
+        # in-window weights: same sign, same binade, |wq - w| <= half of the dropped 4-bit range
+        assert np.all(np.sign(vq[n][inside]) == np.sign(v[n][inside]))
+        bq = np.floor(np.log2(np.abs(vq[n][inside])))
+        assert np.array_equal(bq, np.floor(np.log2(a[inside])))
+        ulp7 = 2.0 ** (bq - 7)  # one unit of the 7-bit mantissa; the low 4 bits span 16 units
+        assert np.all(np.abs(vq[n][inside] - v[n][inside]) <= 8 * ulp7)
+        # every Q-view weight is a normal number inside the channel's window
+        aq = np.abs(vq[n])
+        assert np.all((aq >= lo_b) & (aq < hi_b))
+
+
+def test_qview_equals_decode_of_truncated_records(orc):
+    """Second route: set every B nibble of the encoded records to 8, drop the escapes, decode."""
+    w = synth.bits(synth.weights(200, 136, synth.TINY, seed=13))
+    e = orc.encode(w)
+    rec = e.records.reshape(-1, orc.RECORD_BYTES).copy()
+    rec[:, 8192:] = 0x88
+    e2 = orc.Encoded(e.N, e.K, rec.reshape(-1), e.base_exp, e.esc_off, e.esc_k[:0],
+                     e.esc_bits[:0], np.zeros_like(e.rec_esc_off), e.rec_esc[:0])
+    assert np.array_equal(orc.decode(e2), orc.qview_weights(w))
