@@ -1,0 +1,367 @@
+#!/usr/bin/env python
+"""Benchmark of the W12 skinny GEMM on one GB300 (or N independent replicas, one per GPU).
+
+Workload: the MLP projection of a 27B-class dense layer, K=5120, N=17408, weights and activations
+drawn by the seeded synthetic recipe; one step = one W12 GEMM per verification-row count
+M in {1, 4, 8, 16, 32} (fp32 output). Metric: achieved HBM GB/s of the encoded (12-bit) weight
+stream. Weight copies rotate so that no call finds its weights in L2 (inputs larger than L2).
+
+Also reported on the same line: per-M times against a bf16 cuBLAS GEMM of the same shape, the
+LM-head fused argmax (K=5120, N=151936, M=32) in rows/s, the Q-view and M=192 GEMMs, encode and
+verify throughput, the roofline of the GEMM kernel, an end-to-end figure through host buffers
+and the CPU oracle's throughput on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from lossless_bit_weight_gb300 import synth  # noqa: E402
+
+K_HID, N_MLP, VOCAB = synth.HIDDEN, synth.MLP, synth.VOCAB
+MS = (1, 4, 8, 16, 32)
+METRIC = "W12 GEMM achieved HBM GB/s (% of GB300 peak) at M=1..32; LM-head rows/s"
+WORKLOAD = "mlp-projection K=5120 N=17408, M in {1,4,8,16,32}, fp32 out"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "w12_gemm_kernel_mlp_K5120_N17408.md")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def flush_l2(buf):
+    buf.add_(1)
+
+
+def profile_traffic():
+    """Per-launch DRAM bytes of the GEMM kernel from the committed ncu summary, if it still
+    describes the current kernel source."""
+    import hashlib
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    h = hashlib.sha256()
+    for f in ("lossless_bit_weight_gb300/csrc/w12_gemm.cu", "lossless_bit_weight_gb300/csrc/w12_internal.cuh"):
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    src = h.hexdigest()[:16]
+    got = {}
+    with open(PROFILE_SUMMARY) as f:
+        for ln in f:
+            if ln.startswith("- kernel_source_sha256_16:"):
+                got["sha"] = ln.split(":", 1)[1].strip()
+            if ln.startswith("- dram_bytes_per_launch_full_size:"):
+                got["bytes"] = float(ln.split(":", 1)[1].split()[0])
+    if got.get("sha") != src or "bytes" not in got:
+        return None
+    return got["bytes"]
+
+
+def cpu_baseline(seconds_target: float = 12.0):
+    """The oracle, as it stands, on the host cores: decode a row sample of the projection from
+    its W12 encoding and multiply it with x for every M of the sweep (fp64)."""
+    import oracle
+
+    oracle.build()
+    n_s = 128
+    w = synth.bits(synth.weights(n_s, K_HID, synth.PROJ, seed=synth.seed_for(1, 0)))
+    xs = {m: synth.bits(synth.activations(m, K_HID, seed=synth.seed_for(1, 100 + m))) for m in MS}
+    enc = oracle.encode(w)
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        for m in MS:
+            wd = oracle.decode(enc)
+            oracle.gemm(xs[m], wd)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el > seconds_target or reps >= 64:
+            break
+    w12_bytes = 1.5 * n_s * K_HID * len(MS) * reps
+    return {"value": w12_bytes / el / 1e9, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n_s} of {N_MLP} output channels (K={K_HID}), decode + fp64 GEMM for each M in "
+                      f"{list(MS)}, {reps} repetitions in {el:.1f} s; GB/s of 12-bit weight bytes"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cb = cpu_baseline(seconds_target=max(5.0, 6.0 * args.steps / max(args.steps, 1)))
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "K": K_HID, "N": N_MLP, "M": list(MS)},
+            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip the LM-head/encode/verify/cuBLAS lines")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    from lossless_bit_weight_gb300 import build, w12
+
+    ws, rank, local = dist_env()
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    build.build()
+    dev = torch.device("cuda", local)
+    hbm_peak, tc_peak, peak_kind = peaks()
+
+    # ---- weights: one encoded projection, replicated so every call streams from HBM
+    w = synth.weights(N_MLP, K_HID, synth.PROJ, seed=synth.seed_for(1, 0), device=dev)
+    t0 = w12.encode(w)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_copies = max(3, int(np.ceil(2.5 * l2 / t0.nbytes)) + 1)
+    copies = [t0] + [t0.clone_records() for _ in range(n_copies - 1)]
+    xs = {m: synth.activations(m, K_HID, seed=synth.seed_for(1, 100 + m), device=dev) for m in MS}
+    ys = {m: torch.empty((m, N_MLP), dtype=torch.float32, device=dev) for m in MS}
+    for c in copies:
+        for m in MS:
+            c.workspace(m, w12.OP_GEMM)
+    bytes_per_call = t0.gemm_bytes()
+    stream = torch.cuda.current_stream()
+
+    def step(it, ev=None):
+        for j, m in enumerate(MS):
+            c = copies[(it * len(MS) + j) % n_copies]
+            if ev is not None:
+                ev[j][0].record(stream)
+            w12.gemm(c, xs[m], out=ys[m])
+            if ev is not None:
+                ev[j][1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    w12.check(t0)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in MS]
+           for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, evs[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    for c in copies:
+        w12.check(c)
+    if dist:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    per_m_us = {m: statistics.median(evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in range(args.steps))
+                for j, m in enumerate(MS)}
+    all_launch_us = [evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in range(args.steps) for j in range(len(MS))]
+    total_bytes = bytes_per_call * len(MS) * args.steps * ws
+    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+
+    # algorithmic bytes per launch (roofline): encoded weights + x + y, averaged over the sweep
+    alg = [bytes_per_call + 2 * m * K_HID + 4 * m * N_MLP for m in MS]
+    avg_alg = sum(alg) / len(alg)
+    avg_launch_s = statistics.mean(all_launch_us) * 1e-6
+    achieved = avg_alg / avg_launch_s / 1e9
+    traffic = profile_traffic()
+
+    # ---- end to end through the C ABI with host buffers (pinned), one sweep per step
+    xh = {m: xs[m].cpu().pin_memory() for m in MS}
+    yh = {m: torch.empty((m, N_MLP), dtype=torch.float32).pin_memory() for m in MS}
+    xd = {m: torch.empty_like(xs[m]) for m in MS}
+    e2e_steps = max(3, args.steps // 2)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        for j, m in enumerate(MS):
+            c = copies[(i * len(MS) + j) % n_copies]
+            xd[m].copy_(xh[m], non_blocking=True)
+            w12.gemm(c, xd[m], out=ys[m])
+            yh[m].copy_(ys[m], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    e2e_value = bytes_per_call * len(MS) * e2e_steps / (e2e_ms * 1e-3) / 1e9
+    h2d = sum(2 * m * K_HID for m in MS)
+    d2h = sum(4 * m * N_MLP for m in MS)
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "K": K_HID, "N": N_MLP, "M": list(MS), "out": "fp32",
+                   "l2": f"inputs larger than L2: {n_copies} rotating weight copies of {t0.nbytes/1e6:.1f} MB "
+                         f"(L2 {l2/1e6:.0f} MB)", "parallelism": f"replicas x{ws}",
+                   "w12_bytes_per_call": bytes_per_call, "escapes": t0.n_esc},
+        "frac_of_peak": round(value / ws / hbm_peak, 4), "peak_gbs": hbm_peak, "peak_kind": peak_kind,
+        "per_m": {str(m): {"us": round(per_m_us[m], 2),
+                           "weight_gbs": round(bytes_per_call / (per_m_us[m] * 1e-6) / 1e9, 1),
+                           "tflops": round(2 * m * N_MLP * K_HID / (per_m_us[m] * 1e-6) / 1e12, 2)}
+                  for m in MS},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                     "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
+                     "kernel": "w12_gemm_kernel<exact>", "peak_kind": peak_kind,
+                     "alg_bytes_per_launch": round(avg_alg)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * len(MS),
+    }
+    s = clk.summary() if hasattr(clk, "out") else None
+    line["clocks"] = s
+
+    if not args.no_extras and rank == 0:
+        line.update(extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2))
+    del copies
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line))
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def _time(fn, reps=10, warm=3, flush=None):
+    st = torch.cuda.current_stream()
+    for _ in range(warm):
+        fn(0)
+    ts = []
+    for i in range(reps):
+        if flush is not None:
+            flush_l2(flush)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn(i)
+        b.record(st)
+        b.synchronize()
+        ts.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(ts)
+
+
+def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
+    from lossless_bit_weight_gb300 import w12
+
+    out = {}
+    flush = torch.empty(int(2 * l2) // 4, dtype=torch.float32, device=dev)
+    # cuBLAS bf16 on the same shapes, same cold-L2 treatment (rotating copies)
+    wcopies = [w] + [w.clone() for _ in range(2)]
+    cub = {}
+    for m in MS:
+        us = _time(lambda i: torch.nn.functional.linear(xs[m], wcopies[i % 3]), reps=15)
+        cub[str(m)] = round(us, 2)
+    out["cublas_bf16_us"] = cub
+    del wcopies
+    # Q view and M = 192 rows (the batched tree budget)
+    x192 = synth.activations(192, K_HID, seed=synth.seed_for(4, 192), device=dev)
+    n = len(copies)
+    q_us = _time(lambda i: w12.gemm(copies[i % n], xs[32], qview=True), reps=15)
+    e192 = _time(lambda i: w12.gemm(copies[i % n], x192), reps=15)
+    q192 = _time(lambda i: w12.gemm(copies[i % n], x192, qview=True), reps=15)
+    fl = 2 * 192 * N_MLP * K_HID
+    out["qview"] = {"M32_us": round(q_us, 2), "M32_view_gbs": round(t0.gemm_bytes(True) / (q_us * 1e-6) / 1e9, 1),
+                    "M192_us": round(q192, 2), "M192_tflops": round(fl / (q192 * 1e-6) / 1e12, 1)}
+    out["m192_exact"] = {"us": round(e192, 2), "tflops": round(fl / (e192 * 1e-6) / 1e12, 1),
+                         "frac_tensor_peak": round(fl / (e192 * 1e-6) / 1e12 / tc_peak, 3)}
+    # encode and verify (load time), bf16 GB/s read
+    enc_us = _time(lambda i: w12.encode(w), reps=3, warm=1)
+    ver_us = _time(lambda i: w12.verify(t0, w), reps=3, warm=1)
+    out["encode"] = {"us": round(enc_us, 1), "bf16_gbs": round(w.numel() * 2 / (enc_us * 1e-6) / 1e9, 1)}
+    out["verify"] = {"us": round(ver_us, 1),
+                     "gbs": round((w.numel() * 2 + t0.nbytes) / (ver_us * 1e-6) / 1e9, 1)}
+    # LM head with fused argmax at M = 32 rows
+    wh = synth.weights(VOCAB, K_HID, synth.HEAD, seed=synth.seed_for(2, 0), device=dev)
+    th = w12.encode(wh)
+    xh = synth.activations(32, K_HID, seed=synth.seed_for(2, 1), device=dev)
+    a_us = _time(lambda i: w12.lmhead_argmax(th, xh), reps=10, flush=flush)
+    c_us = _time(lambda i: torch.argmax(torch.nn.functional.linear(xh, wh), dim=1), reps=10, flush=flush)
+    w12.check(th)
+    out["lmhead"] = {"M": 32, "us": round(a_us, 1), "rows_per_s": round(32 / (a_us * 1e-6), 1),
+                     "weight_gbs": round(th.gemm_bytes() / (a_us * 1e-6) / 1e9, 1),
+                     "cublas_linear_argmax_us": round(c_us, 1)}
+    return out
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,175 @@
+/*
+ * w12.h — C ABI of the W12 library for one NVIDIA GB300 (sm_103a).
+ *
+ * W12 is the lossless 12-bit weight format of "SpecPilot: Autonomous Algorithm Discovery and
+ * Systems Optimization for Speculative Decoding" (arXiv 2611.02501), §4.1 "W12: A Lossless
+ * 12-bit Weight Format" and Fig. 5: each BF16 weight of an output channel is stored as three
+ * 4-bit planes (A: sign and top three mantissa bits; E: exponent offset inside the channel's
+ * 16-binade window [E_n-15, E_n]; B: low four mantissa bits); weights outside the window, zeros
+ * and denormals go to an exact escape list; 12 KB records cover 128x64 weight tiles with the
+ * 8-bit A+E view first and plane B last.
+ *
+ * Conventions for every call
+ *   - Memory: every data pointer is a DEVICE pointer owned by the caller. The library never
+ *     allocates or frees device memory and keeps no pointer after a call returns.
+ *   - Matrices are row-major and dense: W is bf16 [N, K] (row n = output channel), x is bf16
+ *     [M, K], y is [M, N]. bf16 values are passed as their raw 16-bit patterns (uint16_t).
+ *   - Execution: calls enqueue work on `stream` and return without waiting, except where a call
+ *     says it synchronises. Argument errors are detected on the host and returned before any
+ *     work is enqueued.
+ *   - Shapes: N >= 1, K >= 8 with K % 8 == 0 (rows must be 16-byte aligned for the tensor-memory
+ *     copies); N and K need not be multiples of the 128x64 tile. GEMM rows: 1 <= M <= 256.
+ *   - Device: the current device must be a compute capability 10.3 GPU (GB300);
+ *     otherwise W12_ERR_DEVICE.
+ *   - Determinism: for a given device, shape and input, every output is bitwise reproducible.
+ *   - Thread safety: calls may run concurrently on different streams only with separate
+ *     workspaces/scratch buffers.
+ */
+#ifndef W12_H
+#define W12_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *w12_stream_t; /* the same type as cudaStream_t; NULL = legacy stream */
+
+typedef enum {
+    W12_OK = 0,
+    W12_ERR_INVALID_ARG = 1,       /* null pointer, bad size, misaligned pointer, bad enum */
+    W12_ERR_UNSUPPORTED_SHAPE = 2, /* K % 8 != 0, M outside [1, 256], ... */
+    W12_ERR_WORKSPACE = 3,         /* workspace or scratch smaller than the size query says */
+    W12_ERR_CUDA = 4,              /* a CUDA runtime call failed (launch, copy, sync) */
+    W12_ERR_MISMATCH = 5,          /* w12_verify found decoded weights that differ */
+    W12_ERR_TIMEOUT = 6,           /* a kernel gave up a bounded wait; its outputs are invalid */
+    W12_ERR_DEVICE = 7             /* the current device is not compute capability 10.3 */
+} w12_status;
+
+enum {
+    W12_TILE_N = 128,        /* output channels per record */
+    W12_TILE_K = 64,         /* reduction elements per record */
+    W12_RECORD_BYTES = 12288,
+    W12_VIEW_BYTES = 8192,   /* the nested 8-bit A+E view: the first two thirds of a record */
+    W12_MAX_M = 256
+};
+
+enum { W12_OUT_F32 = 0, W12_OUT_BF16 = 1 };          /* y element type */
+enum { W12_OP_GEMM = 0, W12_OP_QVIEW_GEMM = 1, W12_OP_ARGMAX = 2, W12_OP_QVIEW_ARGMAX = 3 };
+
+/*
+ * An encoded tensor. The caller allocates every buffer with the sizes given below (n_esc and
+ * n_rec_esc come from w12_encode_sizes) and fills in the fields before w12_encode.
+ *   records      uint8  [n_tiles * k_tiles * 12288]  record r = nt * k_tiles + kt
+ *   base_exp     uint8  [n_tiles * 128]              E_n per channel (padding channels: 16)
+ *   esc_off      uint32 [N + 1]                      canonical per-channel escape list (CSR) ...
+ *   esc_k        uint32 [n_esc]                      ... k of each escape, increasing per channel
+ *   esc_bits     uint16 [n_esc]                      ... its exact bf16 pattern
+ *   rec_esc_off  uint32 [n_tiles * k_tiles + 1]      per-record index, offsets in entries
+ *   rec_esc      uint32 [n_rec_esc]                  entries pos | bits << 16, pos = 64*n_l + k_l,
+ *                                                    padded per record to 4 with 0xFFFFFFFF
+ * n_tiles = ceil(N / 128), k_tiles = ceil(K / 64). Buffers must be 16-byte aligned.
+ */
+typedef struct {
+    int32_t N, K;
+    int32_t n_tiles, k_tiles;
+    uint8_t *records;
+    uint8_t *base_exp;
+    uint32_t *esc_off;
+    uint32_t *esc_k;
+    uint16_t *esc_bits;
+    uint32_t *rec_esc_off;
+    uint32_t *rec_esc;
+    int64_t n_esc;
+    int64_t n_rec_esc;
+} w12_tensor;
+
+/* Human-readable name of a status code (static storage). */
+const char *w12_status_str(w12_status status);
+
+/* Fills t->n_tiles and t->k_tiles for a shape and returns the byte sizes of its fixed-size
+ * buffers (records, base_exp). Host only. */
+w12_status w12_tensor_shape(int N, int K, w12_tensor *t, size_t *records_bytes,
+                            size_t *base_exp_bytes);
+
+/* ---- a1: encode (SpecPilot §4.1, Fig. 5a) ----------------------------------------------- */
+
+/* Scratch bytes that w12_encode_sizes / w12_encode need for an [N, K] weight matrix. Host only. */
+w12_status w12_encode_scratch_size(int N, int K, size_t *bytes);
+
+/* Runs the window and counting passes on w (device bf16 [N, K]) and returns the number of
+ * escapes (n_esc) and of per-record index entries including padding (n_rec_esc).
+ * SYNCHRONISES `stream` to read the two counts back. */
+w12_status w12_encode_sizes(const uint16_t *w, int N, int K, void *scratch, size_t scratch_bytes,
+                            int64_t *n_esc, int64_t *n_rec_esc, w12_stream_t stream);
+
+/* Encodes w (device bf16 [N, K]) into the caller's buffers in *t (t->N, t->K, t->n_esc and
+ * t->n_rec_esc must match w12_encode_sizes). Writes never exceed the stated buffer sizes.
+ * SYNCHRONISES `stream` and returns W12_ERR_INVALID_ARG if the counts found differ from t's. */
+w12_status w12_encode(const uint16_t *w, int N, int K, void *scratch, size_t scratch_bytes,
+                      const w12_tensor *t, w12_stream_t stream);
+
+/* ---- a2: load-time check (SpecPilot §4.1: "checks every decoded tensor against the
+ *          checkpoint bit for bit"; Table A2 caption) ----------------------------------------- */
+
+/* Decodes the whole tensor into w_out (device bf16 [N, K]) from records, base_exp and the
+ * per-record escape index. Asynchronous. */
+w12_status w12_decode(const w12_tensor *t, uint16_t *w_out, w12_stream_t stream);
+
+/* Scratch bytes for w12_verify (host only). */
+w12_status w12_verify_scratch_size(size_t *bytes);
+
+/* Decodes every weight and compares it bit for bit with w_ref (device bf16 [N, K]); also checks
+ * each canonical (CSR) escape entry and that both escape lists hold the same number of entries.
+ * *n_mismatch receives the number of differing weights/entries. SYNCHRONISES `stream`.
+ * Returns W12_ERR_MISMATCH when *n_mismatch > 0. */
+w12_status w12_verify(const w12_tensor *t, const uint16_t *w_ref, void *scratch,
+                      size_t scratch_bytes, uint64_t *n_mismatch, w12_stream_t stream);
+
+/* ---- a3-a5: the skinny GEMMs ------------------------------------------------------------- */
+
+/* Workspace bytes for one of the W12_OP_* operations at M rows on the current device (host
+ * only). The workspace must be zero-filled once before its first use; every successful call
+ * leaves it zeroed again. Calls that share a workspace must not overlap on the GPU. */
+w12_status w12_workspace_size(const w12_tensor *t, int M, int op, size_t *bytes);
+
+/* a3 (SpecPilot §4.1 and Fig. 5b; §6.3): y[m, n] = sum_k x[m, k] * w[n, k] with every weight
+ * decoded exactly in registers and fp32 accumulation; y is fp32 or bf16 (round to nearest even)
+ * [M, N] by y_dtype. x: device bf16 [M, K], 16-byte aligned. Deterministic split of the
+ * reduction over thread blocks in a fixed order. Asynchronous. */
+w12_status w12_gemm(const w12_tensor *t, const uint16_t *x, int M, void *y, int y_dtype,
+                    void *workspace, size_t workspace_bytes, w12_stream_t stream);
+
+/* a5 (SpecPilot §4.3 "Zero-copy Q pass", Fig. 7): the same GEMM over the nested 8-bit view only
+ * (first 8192 bytes of each record): low mantissa bits := 1000b, escapes not patched.
+ * Asynchronous. */
+w12_status w12_qview_gemm(const w12_tensor *t, const uint16_t *x, int M, void *y, int y_dtype,
+                          void *workspace, size_t workspace_bytes, w12_stream_t stream);
+
+/* a4 (SpecPilot §2.1 greedy acceptance of the target argmax; §4.1 and App. E, the LM head): the
+ * GEMM fused with a per-row argmax; y is never written. Per row m: idx[m] = smallest n with the
+ * largest y[m, n]; val[m] = that value; gap[m] = val[m] - the largest y[m, n'] over n' != idx[m]
+ * (0 on an exact tie, +inf when N == 1). qview != 0 runs it over the 8-bit view as in
+ * w12_qview_gemm. NaN logits are not ranked. idx/val/gap: device arrays of M elements.
+ * Asynchronous. */
+w12_status w12_lmhead_argmax(const w12_tensor *t, const uint16_t *x, int M, int32_t *idx,
+                             float *val, float *gap, int qview, void *workspace,
+                             size_t workspace_bytes, w12_stream_t stream);
+
+/* SYNCHRONISES `stream`, then reports W12_ERR_TIMEOUT if a GEMM kernel that used this
+ * workspace gave up one of its bounded waits (its outputs are then invalid and the workspace
+ * must be zero-filled again); W12_OK otherwise. Clears the flag. */
+w12_status w12_check(void *workspace, size_t workspace_bytes, w12_stream_t stream);
+
+/* Kernel configuration a GEMM call would use (for reports): grid size, pipeline stages,
+ * dynamic shared memory bytes. Host only. */
+w12_status w12_gemm_config(const w12_tensor *t, int M, int op, int *grid, int *stages,
+                           int *smem_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W12_H */

@@ -1,0 +1,299 @@
+// Internal helpers of the W12 CUDA library (sm_103a only): status plumbing, inline-PTX wrappers
+// for mbarriers, bulk/tensor copies and the tcgen05 tensor-core instructions, bounded waits.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/w12.h"
+
+namespace w12 {
+
+constexpr int kTileN = 128;
+constexpr int kTileK = 64;
+constexpr int kRecordBytes = 12288;
+constexpr int kViewBytes = 8192;
+constexpr int kRecordWeights = kTileN * kTileK;  // 8192
+
+// ------------------------------------------------------------------------------------------
+// host side
+// ------------------------------------------------------------------------------------------
+
+#define W12_TRY(expr)                         \
+    do {                                      \
+        w12_status _st = (expr);              \
+        if (_st != W12_OK) return _st;        \
+    } while (0)
+
+#define W12_CUDA(expr)                                  \
+    do {                                                \
+        cudaError_t _e = (expr);                        \
+        if (_e != cudaSuccess) return W12_ERR_CUDA;     \
+    } while (0)
+
+// The current device must be a compute capability 10.3 GPU; checked once per device.
+w12_status require_device(int *sm_count);
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+w12_status check_shape(int N, int K);
+w12_status check_tensor(const w12_tensor *t);
+
+// ------------------------------------------------------------------------------------------
+// device side
+// ------------------------------------------------------------------------------------------
+
+// error bits written to the workspace error word by a kernel that gives up a wait
+enum : int {
+    kErrProducer = 1,
+    kErrEscape = 2,
+    kErrDecode = 4,
+    kErrMma = 8,
+    kErrEpilogue = 16,
+    kErrDrain = 32,
+};
+
+// bounded waits give up after this long (ns of %globaltimer)
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+constexpr uint64_t kDrainLimitNs = 100ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity to complete. Gives up (returns false) when
+// another role of the block has raised `abort`, or after kWaitLimitNs; in the latter case it
+// raises `abort` and records `code` in the global error word.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int *gerr, int code) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                *abort = 1;
+                atomicOr(gerr, code);
+                return false;
+            }
+        }
+    }
+}
+
+// Short wait used only while draining on the way out of a kernel.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > kDrainLimitNs) return false;
+    }
+    return true;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0, both 16B aligned)
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared (box and swizzle from the tensor map)
+__device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                           uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// ---- tcgen05 (5th-generation tensor cores, tensor memory) ---------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                 ::"r"(slot_smem), "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16 with bf16 inputs and fp32 accumulation, M = 128.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+        ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Each lane stores 32 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, "
+        "%29, %30, %31, %32};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+        "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]),
+        "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]),
+        "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+        "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+// Each lane loads 16 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+        "%11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile stored with the 128-byte swizzle
+// (rows of 64 bf16 = 128 B, 8-row atoms 1024 B apart), as a TMA SWIZZLE_128B box lays it out.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);        // start address
+    d |= static_cast<uint64_t>(1u) << 16;                       // leading byte offset (unused)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;               // stride byte offset: 8 rows
+    d |= static_cast<uint64_t>(1u) << 46;                       // descriptor version
+    d |= static_cast<uint64_t>(2u) << 61;                       // swizzle: 128B
+    return d;
+}
+
+// Instruction descriptor for kind::f16: bf16 A and B (K-major), fp32 D, shape 128 x n.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
+    return (1u << 4)              // D format: f32
+         | (1u << 7)              // A format: bf16
+         | (1u << 10)             // B format: bf16
+         | ((n >> 3) << 17)       // N / 8
+         | ((m >> 4) << 24);      // M / 16
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(const void *p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(smem_u32(p)));
+    return v;
+}
+
+// ---- in-register W12 decode -------------------------------------------------------------
+//
+// Two weights (k = 2p, 2p+1) become one bf16x2 word, low half = even k.
+//   x     = view bytes of the two weights at bits 0..7 and 16..23 (byte = E<<4 | m_hi<<1 | s)
+//   bs    = plane-B word shifted so the two low-mantissa nibbles sit at bits 0..3 and 16..19
+//   base2 = (E_n - 15) << 7 in both halves
+// x << 3 puts m_hi at bits 4..6 and E at 7..10 (its stray sign bit lands at bit 3, which the
+// nibble select overwrites); x << 15 puts each sign at bit 15 / 31. Adding base2 turns E into
+// the biased exponent; E + E_n - 15 <= 254, so the sum never carries into the sign bit.
+template <bool kQView>
+__device__ __forceinline__ uint32_t decode_pair(uint32_t x, uint32_t bs, uint32_t base2) {
+    const uint32_t t = x << 3, u = x << 15;
+    const uint32_t r1 = (u & 0x80008000u) | (t & 0x7FFF7FFFu);
+    if (kQView) return (r1 & 0xFFF0FFF0u) + (base2 + 0x00080008u);  // low mantissa := 1000b
+    return ((bs & 0x000F000Fu) | (r1 & 0xFFF0FFF0u)) + base2;
+}
+
+// Sixteen weights k_l = 16c .. 16c+15 of one channel row -> 8 bf16x2 words.
+//   v = the row's 16 view bytes of chunk c; b = the row's 16 plane-B bytes of chunk c >> 1;
+//   kOdd = c & 1 (selects which half of the plane-B chunk holds these k).
+template <bool kQView, int kOdd>
+__device__ __forceinline__ void decode_chunk16(const uint4 &v, const uint4 &b, uint32_t base2,
+                                               uint32_t *out) {
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t B = bw[2 * kOdd + (q >> 1)];
+        const int sh = 8 * (q & 1);
+        out[2 * q] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4140u), B >> sh, base2);
+        out[2 * q + 1] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4342u), B >> (sh + 4), base2);
+    }
+}
+
+__device__ __forceinline__ uint32_t base2_of(int En) {
+    const uint32_t b = static_cast<uint32_t>(En - 15) << 7;
+    return b | (b << 16);
+}
+
+}  // namespace w12

@@ -1,0 +1,260 @@
+"""Thin Python binding of the W12 C ABI (``include/w12.h``, ``libw12.so``).
+
+It only marshals torch CUDA tensors into the C calls: every step of encode, verify, decode and
+the GEMMs runs in the library's CUDA kernels. torch provides device memory and the current
+stream. There is no CPU or eager fallback: if the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libw12.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_MISMATCH, ERR_TIMEOUT, \
+    ERR_DEVICE = range(8)
+OUT_F32, OUT_BF16 = 0, 1
+OP_GEMM, OP_QVIEW_GEMM, OP_ARGMAX, OP_QVIEW_ARGMAX = range(4)
+TILE_N, TILE_K, RECORD_BYTES, VIEW_BYTES, MAX_M = 128, 64, 12288, 8192, 256
+
+
+class W12Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_str(status)}")
+        self.status = status
+
+
+class CTensor(ctypes.Structure):
+    """Mirror of ``w12_tensor``."""
+
+    _fields_ = [
+        ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("n_tiles", ctypes.c_int32), ("k_tiles", ctypes.c_int32),
+        ("records", ctypes.c_void_p), ("base_exp", ctypes.c_void_p),
+        ("esc_off", ctypes.c_void_p), ("esc_k", ctypes.c_void_p), ("esc_bits", ctypes.c_void_p),
+        ("rec_esc_off", ctypes.c_void_p), ("rec_esc", ctypes.c_void_p),
+        ("n_esc", ctypes.c_int64), ("n_rec_esc", ctypes.c_int64),
+    ]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libw12.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"W12 CUDA library not built: {LIB_PATH} is missing "
+                               "(run lossless_bit_weight_gb300.build.build())")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        T = ctypes.POINTER(CTensor)
+        sig = {
+            "w12_status_str": ([i32], ctypes.c_char_p),
+            "w12_tensor_shape": ([i32, i32, T, ctypes.POINTER(sz), ctypes.POINTER(sz)], i32),
+            "w12_encode_scratch_size": ([i32, i32, ctypes.POINTER(sz)], i32),
+            "w12_encode_sizes": ([P, i32, i32, P, sz, ctypes.POINTER(i64), ctypes.POINTER(i64), P], i32),
+            "w12_encode": ([P, i32, i32, P, sz, T, P], i32),
+            "w12_decode": ([T, P, P], i32),
+            "w12_verify_scratch_size": ([ctypes.POINTER(sz)], i32),
+            "w12_verify": ([T, P, P, sz, ctypes.POINTER(ctypes.c_uint64), P], i32),
+            "w12_workspace_size": ([T, i32, i32, ctypes.POINTER(sz)], i32),
+            "w12_gemm": ([T, P, i32, P, i32, P, sz, P], i32),
+            "w12_qview_gemm": ([T, P, i32, P, i32, P, sz, P], i32),
+            "w12_lmhead_argmax": ([T, P, i32, P, P, P, i32, P, sz, P], i32),
+            "w12_check": ([P, sz, P], i32),
+            "w12_gemm_config": ([T, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                 ctypes.POINTER(i32)], i32),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().w12_status_str(status).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != OK:
+        raise W12Error(status, what)
+
+
+def _ptr(t: torch.Tensor | None):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _bits(t: torch.Tensor) -> torch.Tensor:
+    if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError("expected a contiguous bf16 CUDA tensor")
+    return t
+
+
+@dataclass
+class W12Tensor:
+    """An encoded weight matrix: the device buffers of ``w12_tensor`` plus its descriptor."""
+
+    N: int
+    K: int
+    records: torch.Tensor
+    base_exp: torch.Tensor
+    esc_off: torch.Tensor
+    esc_k: torch.Tensor
+    esc_bits: torch.Tensor
+    rec_esc_off: torch.Tensor
+    rec_esc: torch.Tensor
+    n_esc: int
+    n_rec_esc: int
+    c: CTensor = field(default=None, repr=False)
+    _ws: dict = field(default_factory=dict, repr=False)
+
+    def __post_init__(self):
+        self.c = CTensor(self.N, self.K, (self.N + TILE_N - 1) // TILE_N, (self.K + TILE_K - 1) // TILE_K,
+                         self.records.data_ptr(), self.base_exp.data_ptr(), self.esc_off.data_ptr(),
+                         self.esc_k.data_ptr(), self.esc_bits.data_ptr(), self.rec_esc_off.data_ptr(),
+                         self.rec_esc.data_ptr(), self.n_esc, self.n_rec_esc)
+
+    @property
+    def n_tiles(self) -> int:
+        return self.c.n_tiles
+
+    @property
+    def k_tiles(self) -> int:
+        return self.c.k_tiles
+
+    @property
+    def nbytes(self) -> int:
+        """Bytes of the encoded tensor (records, bases, both escape lists and their offsets)."""
+        return sum(t.numel() * t.element_size() for t in (
+            self.records, self.base_exp, self.esc_off, self.esc_k, self.esc_bits,
+            self.rec_esc_off, self.rec_esc))
+
+    def gemm_bytes(self, qview: bool = False) -> int:
+        """Encoded bytes one GEMM call streams: records (or their 8-bit views), bases, and the
+        per-record escape index with its offsets (the exact GEMM only)."""
+        R = self.n_tiles * self.k_tiles
+        if qview:
+            return R * VIEW_BYTES + self.base_exp.numel()
+        return (R * RECORD_BYTES + self.base_exp.numel() + 4 * (R + 1) + 4 * self.n_rec_esc)
+
+    def workspace(self, M: int, op: int) -> tuple[torch.Tensor, int]:
+        """A zero-filled workspace for (M, op), cached on this tensor and reused across calls."""
+        key = (M, op, torch.cuda.current_device())
+        if key not in self._ws:
+            nb = ctypes.c_size_t()
+            _check(lib().w12_workspace_size(ctypes.byref(self.c), M, op, ctypes.byref(nb)), "w12_workspace_size")
+            self._ws[key] = (torch.zeros(max(int(nb.value), 16), dtype=torch.uint8, device="cuda"), int(nb.value))
+        return self._ws[key]
+
+    def clone_records(self) -> "W12Tensor":
+        """A second encoded tensor with copied buffers (to stream weights that are not in L2)."""
+        return W12Tensor(self.N, self.K, self.records.clone(), self.base_exp.clone(), self.esc_off.clone(),
+                         self.esc_k.clone(), self.esc_bits.clone(), self.rec_esc_off.clone(),
+                         self.rec_esc.clone(), self.n_esc, self.n_rec_esc)
+
+
+def encode(w: torch.Tensor, stream=None) -> W12Tensor:
+    """Encode a bf16 [N, K] CUDA tensor (``w12_encode_sizes`` then ``w12_encode``)."""
+    _bits(w)
+    N, K = w.shape
+    L = lib()
+    nb = ctypes.c_size_t()
+    _check(L.w12_encode_scratch_size(N, K, ctypes.byref(nb)), "w12_encode_scratch_size")
+    scratch = torch.empty(int(nb.value), dtype=torch.uint8, device=w.device)
+    n_esc, n_rec = ctypes.c_int64(), ctypes.c_int64()
+    st = _stream(stream)
+    _check(L.w12_encode_sizes(_ptr(w), N, K, _ptr(scratch), nb, ctypes.byref(n_esc), ctypes.byref(n_rec), st),
+           "w12_encode_sizes")
+    shape = CTensor()
+    rb, bb = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(L.w12_tensor_shape(N, K, ctypes.byref(shape), ctypes.byref(rb), ctypes.byref(bb)), "w12_tensor_shape")
+    R = shape.n_tiles * shape.k_tiles
+    dev = w.device
+    t = W12Tensor(
+        N, K,
+        records=torch.empty(int(rb.value), dtype=torch.uint8, device=dev),
+        base_exp=torch.empty(int(bb.value), dtype=torch.uint8, device=dev),
+        esc_off=torch.empty(N + 1, dtype=torch.int32, device=dev),
+        esc_k=torch.empty(max(n_esc.value, 4), dtype=torch.int32, device=dev),
+        esc_bits=torch.empty(max(n_esc.value, 8), dtype=torch.int16, device=dev),
+        rec_esc_off=torch.empty(R + 1, dtype=torch.int32, device=dev),
+        rec_esc=torch.empty(max(n_rec.value, 4), dtype=torch.int32, device=dev),
+        n_esc=n_esc.value, n_rec_esc=n_rec.value,
+    )
+    _check(L.w12_encode(_ptr(w), N, K, _ptr(scratch), nb, ctypes.byref(t.c), st), "w12_encode")
+    return t
+
+
+def decode(t: W12Tensor, stream=None) -> torch.Tensor:
+    out = torch.empty((t.N, t.K), dtype=torch.bfloat16, device=t.records.device)
+    _check(lib().w12_decode(ctypes.byref(t.c), _ptr(out), _stream(stream)), "w12_decode")
+    return out
+
+
+def verify(t: W12Tensor, w_ref: torch.Tensor, stream=None) -> int:
+    """Number of weights/escape entries that do not decode to ``w_ref`` bit for bit (0 = lossless)."""
+    _bits(w_ref)
+    nb = ctypes.c_size_t()
+    _check(lib().w12_verify_scratch_size(ctypes.byref(nb)), "w12_verify_scratch_size")
+    scratch = torch.empty(int(nb.value), dtype=torch.uint8, device=w_ref.device)
+    bad = ctypes.c_uint64()
+    st = lib().w12_verify(ctypes.byref(t.c), _ptr(w_ref), _ptr(scratch), nb, ctypes.byref(bad), _stream(stream))
+    if st not in (OK, ERR_MISMATCH):
+        _check(st, "w12_verify")
+    return int(bad.value)
+
+
+def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = False,
+         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """y = x @ W^T over the exact weights (or the 8-bit view when ``qview``)."""
+    _bits(x)
+    M = x.shape[0]
+    if x.shape[1] != t.K:
+        raise ValueError("x must be [M, K]")
+    ydt = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    if out is None:
+        out = torch.empty((M, t.N), dtype=out_dtype, device=x.device)
+    ws, nb = t.workspace(M, OP_QVIEW_GEMM if qview else OP_GEMM)
+    fn = lib().w12_qview_gemm if qview else lib().w12_gemm
+    _check(fn(ctypes.byref(t.c), _ptr(x), M, _ptr(out), ydt, _ptr(ws), nb, _stream(stream)),
+           "w12_qview_gemm" if qview else "w12_gemm")
+    return out
+
+
+def lmhead_argmax(t: W12Tensor, x: torch.Tensor, qview: bool = False, stream=None):
+    """(idx int32[M], val f32[M], gap f32[M]) of y = x @ W^T without materialising y."""
+    _bits(x)
+    M = x.shape[0]
+    idx = torch.empty(M, dtype=torch.int32, device=x.device)
+    val = torch.empty(M, dtype=torch.float32, device=x.device)
+    gap = torch.empty(M, dtype=torch.float32, device=x.device)
+    ws, nb = t.workspace(M, OP_QVIEW_ARGMAX if qview else OP_ARGMAX)
+    _check(lib().w12_lmhead_argmax(ctypes.byref(t.c), _ptr(x), M, _ptr(idx), _ptr(val), _ptr(gap),
+                                   1 if qview else 0, _ptr(ws), nb, _stream(stream)), "w12_lmhead_argmax")
+    return idx, val, gap
+
+
+def check(t: W12Tensor, stream=None) -> None:
+    """Synchronise and raise if any GEMM kernel on one of t's workspaces gave up a bounded wait."""
+    for ws, nb in t._ws.values():
+        _check(lib().w12_check(_ptr(ws), nb, _stream(stream)), "w12_check")
+
+
+def gemm_config(t: W12Tensor, M: int, op: int) -> dict:
+    g, s, m = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    _check(lib().w12_gemm_config(ctypes.byref(t.c), M, op, ctypes.byref(g), ctypes.byref(s), ctypes.byref(m)),
+           "w12_gemm_config")
+    return {"grid": g.value, "stages": s.value, "smem_bytes": m.value}

@@ -56,6 +56,7 @@ def _load():
         lib.w12o_argmax.argtypes = [P, i32, i32, P, P, P, P]
         lib.w12o_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.w12o_bf16_to_double.restype = ctypes.c_double
+        lib.w12o_threads.restype = i32
         _lib = lib
     return _lib
 
@@ -185,6 +186,11 @@ def argmax(y) -> tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]:
     sc = np.zeros(M, np.float64)
     _load().w12o_argmax(_p(y), M, N, _p(idx), _p(val), _p(gap), _p(sc))
     return idx, val, gap, sc
+
+
+def threads() -> int:
+    """OpenMP threads the oracle's parallel loops use."""
+    return int(_load().w12o_threads())
 
 
 def bf16_to_double(u: int) -> float:

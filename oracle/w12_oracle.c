@@ -325,3 +325,11 @@ void w12o_argmax(const double *y, int M, int N, int32_t *idx, double *val, doubl
         scale[m] = sc;
     }
 }
+
+/* number of OpenMP threads the parallel loops above use */
+#ifdef _OPENMP
+#include <omp.h>
+int w12o_threads(void) { return omp_get_max_threads(); }
+#else
+int w12o_threads(void) { return 1; }
+#endif

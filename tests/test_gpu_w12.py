@@ -1,0 +1,222 @@
+"""GPU parity of the W12 CUDA path against the CPU oracle, through the C ABI.
+
+- encode: byte-identical records, window bases and both escape lists (SpecPilot §4.1, Fig. 5a);
+- decode / verify: bit-exact round trip, corruption detected (SpecPilot §4.1 load-time check);
+- GEMM, Q-view GEMM (SpecPilot §4.3) and fused argmax (SpecPilot §2.1) within the stated
+  bounds, on ragged shapes that span several tiles, at every row count class, and repeatably.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from lossless_bit_weight_gb300 import synth
+from w12_testutil import argmax_check, gemm_violations, to_np_u16
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w12():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    from lossless_bit_weight_gb300 import build, w12 as mod
+
+    build.build()
+    oracle.build()
+    return mod
+
+
+def _u32(t):
+    return t.cpu().numpy().view(np.uint32)
+
+
+def _assert_same_encoding(t, e):
+    R = t.n_tiles * t.k_tiles
+    assert np.array_equal(t.records.cpu().numpy(), e.records)
+    assert np.array_equal(t.base_exp.cpu().numpy(), e.base_exp)
+    assert np.array_equal(_u32(t.esc_off), e.esc_off)
+    assert t.n_esc == e.esc_k.size
+    assert np.array_equal(_u32(t.esc_k)[: t.n_esc], e.esc_k)
+    assert np.array_equal(t.esc_bits.cpu().numpy().view(np.uint16)[: t.n_esc], e.esc_bits)
+    assert np.array_equal(_u32(t.rec_esc_off), e.rec_esc_off)
+    assert t.n_rec_esc == e.rec_esc.size
+    assert np.array_equal(_u32(t.rec_esc)[: t.n_rec_esc], e.rec_esc)
+    assert t.rec_esc_off.numel() == R + 1
+
+
+def _weights(kind, N, K, seed):
+    if kind == "synthetic":
+        return synth.weights(N, K, synth.TINY, seed=seed, device="cuda")
+    if kind == "all_patterns":
+        return synth.from_bits(synth.all_bf16_patterns(K), device="cuda")
+    if kind == "shuffled_patterns":
+        rng = np.random.default_rng(seed)
+        return synth.from_bits(rng.permutation(synth.all_bf16_patterns(512).reshape(-1)).reshape(N, K), "cuda")
+    if kind == "zero_heavy":  # > 256 escapes in some records: the kernel's overflow path
+        w = synth.weights(N, K, synth.TINY, seed=seed, device="cuda")
+        w[:64, :] = 0
+        w[200:210, 64:128] = 0
+        return w
+    raise ValueError(kind)
+
+
+ENCODE_CASES = [
+    ("synthetic", 512, 256), ("synthetic", 300, 200), ("synthetic", 1, 8), ("synthetic", 129, 72),
+    ("all_patterns", 256, 256), ("shuffled_patterns", 128, 512), ("zero_heavy", 384, 320),
+]
+
+
+@pytest.mark.parametrize("kind,N,K", ENCODE_CASES)
+def test_encode_matches_oracle_bytes(w12, kind, N, K):
+    w = _weights(kind, N, K, seed=N + K)
+    t = w12.encode(w)
+    e = oracle.encode(to_np_u16(w))
+    _assert_same_encoding(t, e)
+
+
+@pytest.mark.parametrize("kind,N,K", ENCODE_CASES)
+def test_decode_and_verify_bit_exact(w12, kind, N, K):
+    w = _weights(kind, N, K, seed=N + K)
+    t = w12.encode(w)
+    assert torch.equal(w12.decode(t).view(torch.int16), w.view(torch.int16))
+    assert w12.verify(t, w) == 0
+
+
+def test_verify_detects_corruption(w12):
+    w = synth.weights(300, 200, synth.TINY, seed=21, device="cuda")
+    t = w12.encode(w)
+    assert t.n_esc > 0
+    t.records[5000] ^= 0x10            # one view byte
+    assert w12.verify(t, w) >= 1
+    t.records[5000] ^= 0x10
+    assert w12.verify(t, w) == 0
+    t.records[12288 + 9000] ^= 0x01    # one plane-B nibble in record 1
+    assert w12.verify(t, w) >= 1
+    t.records[12288 + 9000] ^= 0x01
+    old = int(t.rec_esc[0])
+    t.rec_esc[0] = old ^ (1 << 16)     # the bits of one escape entry
+    assert w12.verify(t, w) >= 1
+    t.rec_esc[0] = old
+    t.esc_bits[0] ^= 1                 # the canonical list too
+    assert w12.verify(t, w) >= 1
+    t.esc_bits[0] ^= 1
+    assert w12.verify(t, w) == 0
+
+
+def _gemm_case(w12, N, K, M, seed, recipe=synth.TINY, qview=False, out_dtype=torch.float32, w=None):
+    if w is None:
+        w = synth.weights(N, K, recipe, seed=seed, device="cuda")
+    x = synth.activations(M, K, seed=seed + 1, device="cuda")
+    t = w12.encode(w)
+    y = w12.gemm(t, x, out_dtype=out_dtype, qview=qview)
+    w12.check(t)
+    wb = to_np_u16(w)
+    if qview:
+        wb = oracle.qview_weights(wb)
+    y_ref, absdot = oracle.gemm(to_np_u16(x), wb)
+    yv = y.float().cpu().numpy()
+    return t, x, y, yv, y_ref, absdot
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16, 17, 32, 33, 64, 100, 192, 256])
+def test_gemm_ragged_all_row_classes(w12, M):
+    _, _, _, yv, y_ref, ad = _gemm_case(w12, 300, 200, M, seed=100 + M)
+    assert gemm_violations(yv, y_ref, ad) == 0
+
+
+@pytest.mark.parametrize("N,K,M", [(512, 256, 1), (1024, 1024, 4), (640, 5120, 32), (2176, 320, 8)])
+def test_gemm_shapes(w12, N, K, M):
+    _, _, _, yv, y_ref, ad = _gemm_case(w12, N, K, M, seed=N + K + M)
+    assert gemm_violations(yv, y_ref, ad) == 0
+
+
+@pytest.mark.parametrize("M", [1, 32, 192])
+def test_gemm_bf16_output(w12, M):
+    _, _, _, yv, y_ref, ad = _gemm_case(w12, 640, 512, M, seed=7 + M, out_dtype=torch.bfloat16)
+    assert gemm_violations(yv, y_ref, ad, bf16=True) == 0
+
+
+def test_gemm_escape_overflow_path(w12):
+    w = _weights("zero_heavy", 384, 320, seed=3)
+    _, _, _, yv, y_ref, ad = _gemm_case(w12, 384, 320, 16, seed=3, w=w)
+    assert gemm_violations(yv, y_ref, ad) == 0
+
+
+def test_gemm_special_weights(w12):
+    """Inf, NaN, signed zeros, subnormals and extreme binades, all restored through escapes."""
+    w = synth.weights(256, 128, synth.TINY, seed=5, device="cuda")
+    bits = w.view(torch.int16)
+    for (n, k, u) in [(0, 0, 0x7F80),    # +Inf
+                      (1, 3, 0x8000),    # -0
+                      (2, 5, 0x0001),    # subnormal
+                      (3, 7, 0x7E00),    # 2^125: top binade, no fp32 overflow after the sum
+                      (4, 9, 0x0080),    # smallest normal
+                      (5, 11, 0xFF80)]:  # -Inf
+        bits[n, k] = int(np.array(u, np.uint16).view(np.int16))
+    x = synth.activations(4, 128, seed=6, device="cuda")
+    t = w12.encode(w)
+    y = w12.gemm(t, x).cpu().numpy()
+    y_ref, ad = oracle.gemm(to_np_u16(x), to_np_u16(w))
+    finite = np.isfinite(y_ref)
+    assert np.array_equal(np.isinf(y), np.isinf(y_ref))
+    assert np.array_equal(np.sign(y[~finite]), np.sign(y_ref[~finite]))
+    assert gemm_violations(y[finite], y_ref[finite], ad[finite]) == 0
+
+
+def test_gemm_bitwise_reproducible(w12):
+    w = synth.weights(2048, 2048, synth.PROJ, seed=9, device="cuda")
+    x = synth.activations(32, 2048, seed=10, device="cuda")
+    t = w12.encode(w)
+    a = w12.gemm(t, x)
+    b = w12.gemm(t, x)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    ia, va, ga = w12.lmhead_argmax(t, x)
+    ib, vb, gb = w12.lmhead_argmax(t, x)
+    assert torch.equal(ia, ib) and torch.equal(va.view(torch.int32), vb.view(torch.int32))
+
+
+def test_workspace_counters_left_zeroed(w12):
+    """Counters and the error word (the head of the workspace) are back at zero after a call, so
+    the next call can reuse the workspace without clearing it; partial sums need no clearing."""
+    w = synth.weights(1000, 640, synth.TINY, seed=11, device="cuda")
+    x = synth.activations(8, 640, seed=12, device="cuda")
+    t = w12.encode(w)
+    for _ in range(2):
+        w12.gemm(t, x)
+        w12.lmhead_argmax(t, x)
+    torch.cuda.synchronize()
+    align = lambda v: (v + 255) // 256 * 256
+    head = 256 + align(4 * t.n_tiles) + 256  # error word, per-tile counters, completion counter
+    for ws, nb in t._ws.values():
+        assert int(ws[:head].count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("M", [1, 16, 64, 192])
+def test_qview_gemm(w12, M):
+    _, _, _, yv, y_ref, ad = _gemm_case(w12, 300, 200, M, seed=300 + M, qview=True)
+    assert gemm_violations(yv, y_ref, ad) == 0
+
+
+@pytest.mark.parametrize("N,K,M,qview", [(3000, 512, 32, False), (1000, 256, 1, False),
+                                         (3000, 512, 64, True), (129, 64, 5, False)])
+def test_lmhead_argmax(w12, N, K, M, qview):
+    w = synth.weights(N, K, synth.HEAD, seed=N + M, device="cuda")
+    x = synth.activations(M, K, seed=N + M + 1, device="cuda")
+    t = w12.encode(w)
+    idx, val, gap = w12.lmhead_argmax(t, x, qview=qview)
+    w12.check(t)
+    wb = to_np_u16(w)
+    if qview:
+        wb = oracle.qview_weights(wb)
+    y_ref, ad = oracle.gemm(to_np_u16(x), wb)
+    checked, near, wrong, details = argmax_check(idx.cpu().numpy(), val.cpu().numpy(),
+                                                 gap.cpu().numpy(), y_ref, ad)
+    assert wrong == 0, details
+    assert checked + near == M and checked >= M - 2
+    # the gap is the difference of two GEMM outputs: within their summed bounds
+    ridx, rval, rgap, _ = oracle.argmax(y_ref)
+    g = gap.cpu().numpy().astype(np.float64)
+    for m in range(M):
+        if int(idx[m]) == ridx[m]:
+            assert abs(g[m] - rgap[m]) <= 2 * (2e-3 * ad[m].max() + 1e-6)
