@@ -69,7 +69,8 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(1.5)  # nvidia-smi needs a moment before its first sample
         except OSError:
             self.proc = None
         return self
@@ -129,7 +130,7 @@ def cpu_baseline(seconds_target: float = 12.0):
     import oracle
 
     oracle.build()
-    n_s = 128
+    n_s = 1024
     w = synth.bits(synth.weights(n_s, K_HID, synth.PROJ, seed=synth.seed_for(1, 0)))
     xs = {m: synth.bits(synth.activations(m, K_HID, seed=synth.seed_for(1, 100 + m))) for m in MS}
     enc = oracle.encode(w)
@@ -141,7 +142,7 @@ def cpu_baseline(seconds_target: float = 12.0):
             oracle.gemm(xs[m], wd)
         reps += 1
         el = time.perf_counter() - t0
-        if el > seconds_target or reps >= 64:
+        if el > seconds_target:
             break
     w12_bytes = 1.5 * n_s * K_HID * len(MS) * reps
     return {"value": w12_bytes / el / 1e9, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
@@ -166,13 +167,18 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the LM-head/encode/verify/cuBLAS lines")
+    ap.add_argument("--profile-gemm", type=int, default=0, metavar="M",
+                    help="only run `--steps` W12 GEMM launches at M rows on the projection (for ncu)")
+    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_gemm:
+        return profile_gemm(args)
 
     from lossless_bit_weight_gb300 import build, w12
 
@@ -216,14 +222,16 @@ def main():
     if dist:
         dist.barrier()
 
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in MS]
-           for _ in range(args.steps)]
+    ev_every = max(1, args.steps // 400)  # per-launch events on every ev_every-th step
+    ev_steps = list(range(0, args.steps, ev_every))
+    evs = {i: [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in MS]
+           for i in ev_steps}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            step(args.warmup + i, evs[i])
+            step(args.warmup + i, evs.get(i))
         stop.record(stream)
         torch.cuda.synchronize()
     if dist:
@@ -235,9 +243,9 @@ def main():
         tt = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tt.item())
-    per_m_us = {m: statistics.median(evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in range(args.steps))
+    per_m_us = {m: statistics.median(evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in ev_steps)
                 for j, m in enumerate(MS)}
-    all_launch_us = [evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in range(args.steps) for j in range(len(MS))]
+    all_launch_us = [evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in ev_steps for j in range(len(MS))]
     total_bytes = bytes_per_call * len(MS) * args.steps * ws
     value = total_bytes / (elapsed_ms * 1e-3) / 1e9
 
@@ -252,7 +260,7 @@ def main():
     xh = {m: xs[m].cpu().pin_memory() for m in MS}
     yh = {m: torch.empty((m, N_MLP), dtype=torch.float32).pin_memory() for m in MS}
     xd = {m: torch.empty_like(xs[m]) for m in MS}
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = max(3, min(args.steps, 400))
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -301,6 +309,39 @@ def main():
     if dist:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def profile_gemm(args):
+    """A few launches of one GEMM variant on the projection (or the LM head for argmax), with
+    rotating weight copies; prints the median launch time. Used as the command under ncu."""
+    from lossless_bit_weight_gb300 import build, w12
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    M = args.profile_gemm
+    N = VOCAB if args.profile_op == "argmax" else N_MLP
+    rec = synth.HEAD if args.profile_op == "argmax" else synth.PROJ
+    w = synth.weights(N, K_HID, rec, seed=synth.seed_for(1, 0), device=dev)
+    t = w12.encode(w)
+    del w
+    copies = [t] + [t.clone_records() for _ in range(2 if N == N_MLP else 0)]
+    x = synth.activations(M, K_HID, seed=synth.seed_for(1, 100 + M), device=dev)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        c = copies[i % len(copies)]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        if args.profile_op == "argmax":
+            w12.lmhead_argmax(c, x)
+        else:
+            w12.gemm(c, x, qview=args.profile_op == "qview")
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            ts.append(a.elapsed_time(b) * 1e3)
+    w12.check(t)
+    print(json.dumps({"op": args.profile_op, "M": M, "N": N, "K": K_HID, "launch_us_median": statistics.median(ts),
+                      "bytes": t.gemm_bytes(args.profile_op == "qview")}))
 
 
 def _time(fn, reps=10, warm=3, flush=None):

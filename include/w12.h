@@ -67,9 +67,11 @@ enum { W12_OP_GEMM = 0, W12_OP_QVIEW_GEMM = 1, W12_OP_ARGMAX = 2, W12_OP_QVIEW_A
  *   esc_off      uint32 [N + 1]                      canonical per-channel escape list (CSR) ...
  *   esc_k        uint32 [n_esc]                      ... k of each escape, increasing per channel
  *   esc_bits     uint16 [n_esc]                      ... its exact bf16 pattern
- *   rec_esc_off  uint32 [n_tiles * k_tiles + 1]      per-record index, offsets in entries
- *   rec_esc      uint32 [n_rec_esc]                  entries pos | bits << 16, pos = 64*n_l + k_l,
- *                                                    padded per record to 4 with 0xFFFFFFFF
+ *   rec_esc_off  uint32 [n_tiles * k_tiles + 1]      per-record index, offsets in 32-bit words
+ *   rec_esc      uint32 [n_rec_esc]                  per record with escapes: 4 header words (word q
+ *                                                    = entries with n_l < 32*(q+1)), then entries
+ *                                                    pos | bits << 16 (pos = 64*n_l + k_l, increasing),
+ *                                                    padded to a multiple of 4 words with 0xFFFFFFFF
  * n_tiles = ceil(N / 128), k_tiles = ceil(K / 64). Buffers must be 16-byte aligned.
  */
 typedef struct {

@@ -42,7 +42,9 @@ decode_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ b
                     make_uint4(out[4 * g], out[4 * g + 1], out[4 * g + 2], out[4 * g + 3]);
     }
     __syncthreads();  // escapes overwrite placeholders written above by other threads
-    for (uint32_t i = rec_off[r] + threadIdx.x; i < rec_off[r + 1]; i += blockDim.x) {
+    // a non-empty segment starts with a 4-word header of quarter ends
+    const uint32_t first = rec_off[r] + (rec_off[r + 1] > rec_off[r] ? 4u : 0u);
+    for (uint32_t i = first + threadIdx.x; i < rec_off[r + 1]; i += blockDim.x) {
         const uint32_t e = rec_esc[i];
         const uint32_t pos = e & 0xFFFFu;
         if (pos >= static_cast<uint32_t>(kRecordWeights)) continue;  // padding entry
@@ -72,12 +74,16 @@ verify_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ b
               int K, int k_tiles, const uint16_t *__restrict__ w_ref,
               unsigned long long *counters) {
     __shared__ uint32_t esc_map[kRecordWeights / 32];
+    __shared__ uint32_t quarter_cnt[4];
     const int r = blockIdx.x;
     const int nt = r / k_tiles, kt = r % k_tiles;
     for (int i = threadIdx.x; i < kRecordWeights / 32; i += blockDim.x) esc_map[i] = 0;
+    if (threadIdx.x < 4) quarter_cnt[threadIdx.x] = 0;
     __syncthreads();
     uint32_t bad = 0, entries = 0;
-    for (uint32_t i = rec_off[r] + threadIdx.x; i < rec_off[r + 1]; i += blockDim.x) {
+    const uint32_t seg_lo = rec_off[r], seg_hi = rec_off[r + 1];
+    const uint32_t first = seg_lo + (seg_hi > seg_lo ? 4u : 0u);
+    for (uint32_t i = first + threadIdx.x; i < seg_hi; i += blockDim.x) {
         const uint32_t e = rec_esc[i];
         if (e == 0xFFFFFFFFu) continue;  // padding entry
         const uint32_t pos = e & 0xFFFFu;
@@ -88,8 +94,18 @@ verify_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ b
             continue;
         }
         ++entries;
+        atomicAdd(&quarter_cnt[pos >> 11], 1u);
         atomicOr(&esc_map[pos >> 5], 1u << (pos & 31u));
         if (static_cast<uint16_t>(e >> 16) != w_ref[static_cast<size_t>(en) * K + ek]) ++bad;
+    }
+    __syncthreads();
+    // the header the GEMM reads must hold the cumulative quarter counts
+    if (threadIdx.x == 0 && seg_hi > seg_lo) {
+        uint32_t run = 0;
+        for (int q = 0; q < 4; ++q) {
+            run += quarter_cnt[q];
+            if (rec_esc[seg_lo + q] != run) ++bad;
+        }
     }
     __syncthreads();
     const int nl = threadIdx.x >> 1, half = threadIdx.x & 1;

@@ -180,10 +180,16 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
     reinterpret_cast<uint4 *>(rec + 2048 * (2 * half + 1) + 16 * nl)[0] = make_uint4(vw[4], vw[5], vw[6], vw[7]);
     reinterpret_cast<uint4 *>(rec + kViewBytes + 2048 * half + 16 * nl)[0] = make_uint4(bw[0], bw[1], bw[2], bw[3]);
 
-    // per-record index: entries in increasing pos = 64*n_l + k_l, i.e. in thread order
+    // per-record index: a 4-word header of quarter ends, then the entries in increasing
+    // pos = 64*n_l + k_l (thread order), then padding to a multiple of 4 words
     uint32_t total;
     const uint32_t rank = block_excl_scan256(cnt, &total);
-    const int64_t rbase = static_cast<int64_t>(a.rec_off[r]) + rank;
+    const int64_t seg = static_cast<int64_t>(a.rec_off[r]);
+    if (total > 0 && (threadIdx.x & 63) == 63) {  // last thread of 32-row quarter q
+        const int64_t hi = seg + (threadIdx.x >> 6);
+        if (hi < a.rec_cap) a.rec_esc[hi] = rank + cnt;
+    }
+    const int64_t rbase = seg + 4 + rank;
     // canonical per-channel list: this channel's escapes in earlier k tiles come first
     const int64_t cbase = (n < a.N) ? static_cast<int64_t>(a.chan_off[n]) +
                                           a.ct[static_cast<size_t>(n) * a.k_tiles + kt] +
@@ -204,9 +210,9 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
             ++seen;
         }
     }
-    if (threadIdx.x == 255) {
+    if (threadIdx.x == 255 && total > 0) {
         const int64_t end = a.rec_off[r + 1];
-        for (int64_t i = static_cast<int64_t>(a.rec_off[r]) + total; i < end; ++i)
+        for (int64_t i = seg + 4 + total; i < end; ++i)
             if (i < a.rec_cap) a.rec_esc[i] = 0xFFFFFFFFu;
     }
 }
@@ -224,9 +230,13 @@ __global__ void rowscan_kernel(uint32_t *ct, int n_pad, int k_tiles, uint32_t *c
     chan_cnt[n] = run;
 }
 
-// out[i] = sum_{j<i} in'[j], out[count] = total, with in' = in rounded up to 4 if pad4
+// words of a record's index segment with c escapes: none, or a 4-word header + c entries
+// rounded up to a multiple of 4
+__device__ __forceinline__ uint32_t segment_words(uint32_t c) { return c ? 4u + ((c + 3u) & ~3u) : 0u; }
+
+// out[i] = sum_{j<i} in'[j], out[count] = total, with in' = in, or segment_words(in) if seg
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t *in, int64_t count,
-                                                            uint32_t *out, int pad4) {
+                                                            uint32_t *out, int seg) {
     __shared__ uint32_t warp_sums[kScanThreads / 32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int64_t chunk = (count + kScanThreads - 1) / kScanThreads;
@@ -234,7 +244,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t *in, 
     uint32_t local = 0;
     for (int64_t i = lo; i < hi; ++i) {
         const uint32_t v = in[i];
-        local += pad4 ? (v + 3u) & ~3u : v;
+        local += seg ? segment_words(v) : v;
     }
     uint32_t incl = local;
 #pragma unroll
@@ -253,7 +263,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t *in, 
     for (int64_t i = lo; i < hi; ++i) {
         const uint32_t v = in[i];
         out[i] = run;
-        run += pad4 ? (v + 3u) & ~3u : v;
+        run += seg ? segment_words(v) : v;
     }
     if (t == 0) out[count] = all;
 }

@@ -5,16 +5,22 @@
 // result is deterministic; §6.3 and App. E: it is bound by weight bytes at 1-32 rows; §4.3: the
 // Q pass reads only the nested 8-bit view; §2.1: greedy verification takes the row argmax.
 //
-// Design on GB300 (one persistent block per SM, 16 warps):
-//   warp 0       producer: one 1-D bulk copy per 12 KB record (8 KB for the Q view) and one
-//                128B-swizzled TMA box of the activations' k-slice per stage
+// Design on GB300 (one persistent block per SM, 16 warps). Work moves through a ring of
+// `stages` slots; a slot holds `rps` consecutive records (2 for up to 64 rows, else 1) with
+// their activation tiles and escape entries in shared memory, plus one 32-column tensor-memory
+// buffer per record for the decoded weights. Each slot has three barriers: full (copies
+// landed), afull (decoded weights stored) and empty (the MMAs that read it completed).
+//   warp 0       producer: one bulk copy of the slot's records (contiguous in memory), one
+//                128B-swizzled TMA box of the activations' k-slice per record
 //   warp 1       allocates tensor memory; one thread issues tcgen05.mma (M=128 weight rows from
 //                tensor memory, N = rows of x padded to 16 from shared memory, K=16)
-//   warp 2       escape feeder: bulk-copies each record's escape entries next to the record
+//   warp 2       escape feeder: bulk-copies the slot's escape entries next to its records
 //   warps 4-7    epilogue: tensor memory -> registers; y, split-K partials or the row argmax
-//   warps 8-15   two decode groups on alternate records: each thread owns one weight row, turns
-//                its 64 view bytes + 32 plane-B bytes into 32 bf16x2 words, patches escapes and
+//   warps 8-15   two decode groups: each thread owns one weight row of a record, turns its 64
+//                view bytes + 32 plane-B bytes into 32 bf16x2 words, patches its escapes and
 //                stores them into its tensor-memory lane (the MMA's A operand)
+// The single-thread roles wait on a barrier once per slot, not once per record: a barrier
+// round trip costs a few hundred cycles, comparable to the HBM time of one 12 KB record.
 // Work split: the R = n_tiles*k_tiles records are cut into `grid` contiguous, equal ranges
 // (stream-K). A tile covered by several blocks is finished by whichever arrives last, summing
 // the blocks' fp32 partials in increasing block order: no float atomics, bitwise reproducible.
@@ -28,32 +34,38 @@
 namespace w12 {
 namespace {
 
-constexpr int kThreads = 512;
+#ifndef W12_DECODE_GROUPS
+#define W12_DECODE_GROUPS 3
+#endif
+constexpr int kDecGroups = W12_DECODE_GROUPS;     // decode groups of 4 warps (one per lane quarter)
+constexpr int kThreads = 32 * (8 + 4 * kDecGroups);
+static_assert(kDecGroups >= 1 && kDecGroups <= 4, "one to four decode groups");
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpEscape = 2;
 constexpr int kWarpEpi0 = 4;
 constexpr int kWarpDec0 = 8;
-constexpr int kDecGroups = 2;
-constexpr int kEscCap = 256;       // escape entries staged per record; more -> read from global
-constexpr int kASlots = 4;         // tensor-memory A buffers (32 columns each)
-constexpr int kACols = 32;
-constexpr int kAccCol0 = kASlots * kACols;
+constexpr int kEscCap = 512;       // escape entries staged per slot; more -> read from global
+constexpr int kACols = 32;         // tensor-memory columns of one decoded record (64 bf16/lane)
 constexpr int kMaxStages = 8;
 constexpr int kMaxM = 256;
+constexpr int kTmemCols = 512;
 constexpr int kSmemLimit = 232448;       // opt-in maximum per block
 constexpr int kSmemFloor = 120 * 1024;   // keeps one block per SM
 constexpr int kEpiBar = 1;               // named barrier of the 128 epilogue threads
 
 struct Ctrl {
-    uint64_t full[kMaxStages], empty[kMaxStages];
-    uint64_t afull[kASlots], aempty[kASlots];
+    uint64_t full[kMaxStages], afull[kMaxStages], empty[kMaxStages];
     uint64_t accfull[2], accempty[2];
     uint64_t done;
-    uint32_t esc_hdr[kMaxStages], esc_src[kMaxStages];
+    uint32_t esc_cnt[kMaxStages];    // entries of the slot (bit 31: too many, read from global)
+    uint32_t esc_split[kMaxStages];  // entries that belong to the slot's first record
+    uint32_t esc_src[kMaxStages];    // index of the slot's first entry in the global index
     uint32_t tmem_base;
     int abort;
-    int fix;
+    int fix;          // block-wide flag of the final argmax merge
+    int mode[2];      // how a split tile ends (by segment parity)
+    int last[2];      // this block published last and sums the tile (by segment parity)
     int pad_;
     float4 wtop[4][kMaxM];  // per-warp top-2 of the current tile (argmax)
     float4 ctop[kMaxM];     // running top-2 of this block (argmax)
@@ -64,7 +76,8 @@ struct Params {
     const uint8_t *base_exp;
     const uint32_t *rec_esc_off;
     const uint32_t *rec_esc;
-    int N, K, M, n_tiles, k_tiles, npad, stages, nacc, ncols, grid;
+    int N, K, M, n_tiles, k_tiles, npad, stages, rps, nacc, acc_cols, grid;
+    uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
     int64_t R;
     void *y;
     int y_bf16;
@@ -83,6 +96,20 @@ __device__ __forceinline__ int64_t range_start(int64_t c, int64_t R, int64_t G) 
 __device__ __forceinline__ int64_t owner_of(int64_t i, int64_t R, int64_t G) {
     return ((i + 1) * G + R - 1) / R - 1;
 }
+
+// Position in a ring of `size` slots: index and the parity of its phase. Advanced
+// incrementally so no per-record integer division is needed.
+struct Ring {
+    int idx = 0;
+    uint32_t phase = 0;
+    __device__ __forceinline__ void advance(int by, int size) {
+        idx += by;
+        while (idx >= size) {
+            idx -= size;
+            phase ^= 1u;
+        }
+    }
+};
 
 // ---- argmax helpers: a top-2 is (v1, i1, v2); order = larger value, then smaller index ----
 __device__ __forceinline__ bool better(float v, int i, float w, int j) {
@@ -107,24 +134,6 @@ __device__ __forceinline__ void warp_top2(float &v1, int &i1, float &v2) {
     }
 }
 
-// overwrite one bf16 half of register word `col` (warp-uniform) in the lanes that own it
-__device__ __forceinline__ void patch_word(uint32_t (&w)[32], int col, uint32_t keep, uint32_t val) {
-#define W12_PATCH_CASE(i) \
-    case i: w[i] = (w[i] & keep) | val; break;
-    switch (col) {
-        W12_PATCH_CASE(0) W12_PATCH_CASE(1) W12_PATCH_CASE(2) W12_PATCH_CASE(3)
-        W12_PATCH_CASE(4) W12_PATCH_CASE(5) W12_PATCH_CASE(6) W12_PATCH_CASE(7)
-        W12_PATCH_CASE(8) W12_PATCH_CASE(9) W12_PATCH_CASE(10) W12_PATCH_CASE(11)
-        W12_PATCH_CASE(12) W12_PATCH_CASE(13) W12_PATCH_CASE(14) W12_PATCH_CASE(15)
-        W12_PATCH_CASE(16) W12_PATCH_CASE(17) W12_PATCH_CASE(18) W12_PATCH_CASE(19)
-        W12_PATCH_CASE(20) W12_PATCH_CASE(21) W12_PATCH_CASE(22) W12_PATCH_CASE(23)
-        W12_PATCH_CASE(24) W12_PATCH_CASE(25) W12_PATCH_CASE(26) W12_PATCH_CASE(27)
-        W12_PATCH_CASE(28) W12_PATCH_CASE(29) W12_PATCH_CASE(30) W12_PATCH_CASE(31)
-        default: break;
-    }
-#undef W12_PATCH_CASE
-}
-
 template <bool kQView, bool kArgmax>
 __global__ void __launch_bounds__(kThreads, 1)
 w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
@@ -132,225 +141,299 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    const int S = p.stages;
+    const int S = p.stages, RPS = p.rps;
     const int xbytes = p.npad * 128;
     constexpr int rbytes = kQView ? kViewBytes : kRecordBytes;
     constexpr int ebytes = kQView ? 0 : kEscCap * 4;
-    const int sbytes = xbytes + rbytes + ebytes;
+    const int sbytes = RPS * (xbytes + rbytes) + ebytes;
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + S * sbytes);
-    auto stage_x = [&](int s) { return smem + s * sbytes; };
-    auto stage_rec = [&](int s) { return smem + s * sbytes + xbytes; };
-    auto stage_esc = [&](int s) { return smem + s * sbytes + xbytes + rbytes; };
+    auto stage_x = [&](int s, int q) { return smem + s * sbytes + q * xbytes; };
+    auto stage_rec = [&](int s, int q) { return smem + s * sbytes + RPS * xbytes + q * rbytes; };
+    auto stage_esc = [&](int s) { return smem + s * sbytes + RPS * (xbytes + rbytes); };
 
     const int c = blockIdx.x;
-    const int64_t R = p.R, G = p.grid;
+    const int64_t R = p.R, G = p.grid, kt64 = p.k_tiles;
     const int64_t r0 = range_start(c, R, G), r1 = range_start(c + 1, R, G);
     const int nrec = static_cast<int>(r1 - r0);
-    const int64_t kt64 = p.k_tiles;
+    const int nst = (nrec + RPS - 1) / RPS;  // slots this block fills
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(smem_u32(&ctrl->full[s]), kQView ? 1 : 2);
-            mbar_init(smem_u32(&ctrl->empty[s]), 1);
+    int issued = 0;  // producer: slots handed to the copy engine; mma: slots issued
+    // producer state: its slot ring, the k tile of its next record, the next record's bytes
+    Ring pst;
+    int pkt = 0;
+    const uint8_t *psrc = nullptr;
+    auto produce = [&](int js) {  // fill ring slot pst.idx with the records of slot js
+        const int s = pst.idx;
+        const int nr = min(RPS, nrec - js * RPS);
+        const uint32_t fb = smem_u32(&ctrl->full[s]);
+        mbar_arrive_expect_tx_elect(fb, nr * (rbytes + xbytes));
+        if (kQView) {  // the 8-bit views only: the B planes between them stay in memory
+            for (int q = 0; q < nr; ++q)
+                bulk_g2s_elect(smem_u32(stage_rec(s, q)), psrc + q * kRecordBytes, rbytes, fb);
+        } else {       // consecutive records are contiguous: one copy
+            bulk_g2s_elect(smem_u32(stage_rec(s, 0)), psrc, nr * rbytes, fb);
         }
-        for (int t = 0; t < kASlots; ++t) {
-            mbar_init(smem_u32(&ctrl->afull[t]), 128);
-            mbar_init(smem_u32(&ctrl->aempty[t]), 1);
+        for (int q = 0; q < nr; ++q) {
+            tma_2d_g2s_elect(smem_u32(stage_x(s, q)), &xmap, pkt * kTileK, 0, fb);
+            if (++pkt == p.k_tiles) pkt = 0;
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&ctrl->accfull[b]), 1);
-            mbar_init(smem_u32(&ctrl->accempty[b]), 128);
+        psrc += nr * kRecordBytes;
+        issued = js + 1;
+        pst.advance(1, S);
+    };
+
+    if (warp == kWarpProducer) {
+        // the producer initialises the barriers and starts the first copies right away: every
+        // slot is free at start, so the HBM latency of the first records overlaps the rest of
+        // the block's set-up
+        if (lane == 0) {
+            for (int s = 0; s < S; ++s) {
+                mbar_init(smem_u32(&ctrl->full[s]), kQView ? 1 : 2);
+                mbar_init(smem_u32(&ctrl->afull[s]), 128);
+                mbar_init(smem_u32(&ctrl->empty[s]), 1);
+            }
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(smem_u32(&ctrl->accfull[b]), 1);
+                mbar_init(smem_u32(&ctrl->accempty[b]), 128);
+            }
+            mbar_init(smem_u32(&ctrl->done), 1);
+            ctrl->abort = 0;
+            ctrl->fix = 0;
+            fence_barrier_init();
+            prefetch_tensormap(&xmap);
         }
-        mbar_init(smem_u32(&ctrl->done), 1);
-        ctrl->abort = 0;
-        ctrl->fix = 0;
-        fence_barrier_init();
+        __syncwarp();
+        pkt = static_cast<int>(r0 % kt64);
+        psrc = p.records + r0 * kRecordBytes;
+        for (int js = 0; js < min(S, nst); ++js) produce(js);
     }
     if (kArgmax) {
         for (int m = threadIdx.x; m < p.M; m += kThreads)
             ctrl->ctop[m] = make_float4(-INFINITY, __int_as_float(0x7FFFFFFF), -INFINITY, 0.f);
     }
     if (warp == kWarpMma) {
-        tmem_alloc(smem_u32(&ctrl->tmem_base), p.ncols);
+        tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
         tc_fence_before();
     }
-    if (warp == kWarpProducer && lane == 0) prefetch_tensormap(&xmap);
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
+    auto a_slot = [&](int s, int q) { return tmem + p.acc_cols + (s * RPS + q) * kACols; };
     volatile int *abort = &ctrl->abort;
-    int issued = 0;  // producer: stages handed to the copy engine; mma: records issued
 
     if (warp == kWarpProducer) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            for (int j = 0; j < nrec; ++j) {
-                const int s = j % S;
-                const uint32_t ph = (j / S) & 1;
-                if (!mbar_wait(smem_u32(&ctrl->empty[s]), ph ^ 1, abort, p.err, kErrProducer)) break;
-                const int64_t r = r0 + j;
-                const int kt = static_cast<int>(r % kt64);
-                const uint32_t fb = smem_u32(&ctrl->full[s]);
-                mbar_arrive_expect_tx(fb, rbytes + xbytes);
-                bulk_g2s(smem_u32(stage_rec(s)), p.records + r * kRecordBytes, rbytes, fb);
-                tma_2d_g2s(smem_u32(stage_x(s)), &xmap, kt * kTileK, 0, fb);
-                issued = j + 1;
-            }
+        // ---------------------------------------------------------------- producer (warp-wide)
+        for (int js = min(S, nst); js < nst; ++js) {
+            const bool ok = mbar_wait(smem_u32(&ctrl->empty[pst.idx]), pst.phase ^ 1, abort, p.err, kErrProducer);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            produce(js);
         }
     } else if (warp == kWarpMma) {
-        // ---------------------------------------------------------------- MMA issuer
-        if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, p.npad);
-            int jseg = 0;
-            int64_t r = r0;
+        // ---------------------------------------------------------------- MMA issuer (warp-wide)
+        const uint32_t idesc = idesc_bf16_f32(128, p.npad);
+        Ring st;
+        int jseg = 0;
+        bool open = false;
+        int b = 0;
+        uint32_t d = 0;
+        int64_t seg_start = r0;
+        int64_t seg_end = min(r1, (r0 / kt64 + 1) * kt64);
+        for (int js = 0; js < nst; ++js) {
+            const int s = st.idx;
+            const bool okw = mbar_wait(smem_u32(&ctrl->afull[s]), st.phase, abort, p.err, kErrMma);
+            if (!__all_sync(0xFFFFFFFFu, okw)) break;
+            tc_fence_after();
+            const int nr = min(RPS, nrec - js * RPS);
             bool ok = true;
-            while (ok && r < r1) {
-                const int64_t tile = r / kt64;
-                const int64_t seg_start = r, seg_end = min(r1, (tile + 1) * kt64);
-                const int b = (p.nacc == 2) ? (jseg & 1) : 0;
-                const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
-                if (!mbar_wait(smem_u32(&ctrl->accempty[b]), phb ^ 1, abort, p.err, kErrMma)) break;
-                tc_fence_after();
-                const uint32_t d = tmem + kAccCol0 + b * p.npad;
-                for (; r < seg_end; ++r) {
-                    const int j = static_cast<int>(r - r0);
-                    const int s = j % S, t = j % kASlots;
-                    if (!mbar_wait(smem_u32(&ctrl->full[s]), (j / S) & 1, abort, p.err, kErrMma) ||
-                        !mbar_wait(smem_u32(&ctrl->afull[t]), (j / kASlots) & 1, abort, p.err, kErrMma)) {
+            for (int q = 0; q < nr; ++q) {
+                const int64_t r = r0 + js * RPS + q;
+                if (!open) {
+                    b = (p.nacc == 2) ? (jseg & 1) : 0;
+                    const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
+                    const bool oka = mbar_wait(smem_u32(&ctrl->accempty[b]), phb ^ 1, abort, p.err, kErrMma);
+                    if (!__all_sync(0xFFFFFFFFu, oka)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint64_t bdesc = smem_desc_sw128(smem_u32(stage_x(s)));
-#pragma unroll
-                    for (int kk = 0; kk < kTileK / 16; ++kk)
-                        mma_bf16_ts(d, tmem + t * kACols + kk * 8, bdesc + 2 * kk, idesc,
-                                    (r != seg_start || kk != 0) ? 1u : 0u);
-                    mma_commit(smem_u32(&ctrl->aempty[t]));
-                    mma_commit(smem_u32(&ctrl->empty[s]));
-                    issued = j + 1;
+                    d = tmem + b * p.npad;
+                    open = true;
                 }
-                if (!ok) break;
-                mma_commit(smem_u32(&ctrl->accfull[b]));
-                ++jseg;
+                const uint64_t bdesc = smem_desc_sw128(smem_u32(stage_x(s, q)));
+                const uint32_t a = a_slot(s, q);
+#pragma unroll
+                for (int kk = 0; kk < kTileK / 16; ++kk)
+                    mma_bf16_ts_elect(d, a + kk * 8, bdesc + 2 * kk, idesc, (r != seg_start || kk != 0) ? 1u : 0u);
+                if (r + 1 == seg_end) {
+                    mma_commit_elect(smem_u32(&ctrl->accfull[b]));
+                    ++jseg;
+                    open = false;
+                    seg_start = seg_end;
+                    seg_end = min(r1, seg_end + kt64);
+                }
             }
+            if (!ok) break;
+            mma_commit_elect(smem_u32(&ctrl->empty[s]));
+            issued = js + 1;
+            st.advance(1, S);
         }
     } else if (warp == kWarpEscape) {
-        // ---------------------------------------------------------------- escape feeder
+        // ---------------------------------------------------------------- escape feeder (warp-wide)
         if (!kQView) {
-            auto load_pair = [&](int base, uint32_t &lo, uint32_t &hi) {
-                const int64_t i = r0 + base + lane;
-                lo = (i <= R) ? __ldg(p.rec_esc_off + i) : 0u;
-                hi = (i + 1 <= R) ? __ldg(p.rec_esc_off + i + 1) : 0u;
+            // lane l holds rec_esc_off[r0 + base + l] (cur) and [r0 + base + 32 + l] (nxt)
+            int base = 0;
+            auto load = [&](int b0) -> uint32_t {
+                const int64_t i = r0 + b0 + lane;
+                return (i <= R) ? __ldg(p.rec_esc_off + i) : 0u;
             };
-            uint32_t lo_c, hi_c, lo_n, hi_n;
-            load_pair(0, lo_c, hi_c);
-            load_pair(32, lo_n, hi_n);
-            for (int j = 0; j < nrec; ++j) {
-                if (j > 0 && (j & 31) == 0) {
-                    lo_c = lo_n;
-                    hi_c = hi_n;
-                    load_pair(j + 32, lo_n, hi_n);
+            uint32_t cur = load(0), nxt = load(32);
+            auto off_of = [&](int i) -> uint32_t {  // requires i - base in [0, 64)
+                const int dd = i - base;
+                const uint32_t a = __shfl_sync(0xFFFFFFFFu, cur, dd & 31);
+                const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, nxt, dd & 31);
+                return dd < 32 ? a : b2;
+            };
+            Ring st;
+            for (int js = 0; js < nst; ++js, st.advance(1, S)) {
+                const int first = js * RPS;
+                const int nr = min(RPS, nrec - first);
+                if (first >= base + 32) {
+                    base += 32;
+                    cur = nxt;
+                    nxt = load(base + 32);
                 }
-                const uint32_t lo = __shfl_sync(0xFFFFFFFFu, lo_c, j & 31);
-                const uint32_t hi = __shfl_sync(0xFFFFFFFFu, hi_c, j & 31);
-                int ok = 1;
+                const uint32_t lo = off_of(first);
+                const uint32_t mid = off_of(first + 1);
+                const uint32_t hi = off_of(first + nr);
+                const int s = st.idx;
+                const bool ok = mbar_wait(smem_u32(&ctrl->empty[s]), st.phase ^ 1, abort, p.err, kErrEscape);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                const uint32_t fb = smem_u32(&ctrl->full[s]);
+                const uint32_t cnt = hi - lo;
                 if (lane == 0) {
-                    const int s = j % S;
-                    ok = mbar_wait(smem_u32(&ctrl->empty[s]), ((j / S) & 1) ^ 1, abort, p.err, kErrEscape);
-                    if (ok) {
-                        const uint32_t fb = smem_u32(&ctrl->full[s]);
-                        const uint32_t cnt = hi - lo;
-                        if (cnt == 0) {
-                            ctrl->esc_hdr[s] = 0;
-                            mbar_arrive(fb);
-                        } else if (cnt <= static_cast<uint32_t>(kEscCap)) {
-                            ctrl->esc_hdr[s] = cnt;
-                            mbar_arrive_expect_tx(fb, cnt * 4);
-                            bulk_g2s(smem_u32(stage_esc(s)), p.rec_esc + lo, cnt * 4, fb);
-                        } else {
-                            ctrl->esc_hdr[s] = cnt | 0x80000000u;
-                            ctrl->esc_src[s] = lo;
-                            mbar_arrive(fb);
-                        }
-                    }
+                    ctrl->esc_split[s] = (nr == 2) ? mid - lo : cnt;
+                    ctrl->esc_cnt[s] = (cnt <= static_cast<uint32_t>(kEscCap)) ? cnt : (cnt | 0x80000000u);
+                    ctrl->esc_src[s] = lo;
                 }
-                if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) break;
+                __syncwarp();  // the header stores come before the arrive that publishes them
+                if (cnt == 0 || cnt > static_cast<uint32_t>(kEscCap)) {
+                    mbar_arrive_elect(fb);
+                } else {
+                    mbar_arrive_expect_tx_elect(fb, cnt * 4);
+                    bulk_g2s_elect(smem_u32(stage_esc(s)), p.rec_esc + lo, cnt * 4, fb);
+                }
             }
         }
     } else if (warp >= kWarpDec0) {
         // ---------------------------------------------------------------- decode groups
+        // Group g decodes every record of slots g, g + G, g + 2G, ... (G = kDecGroups). With
+        // two records per slot, a thread decodes its row of the first record, stores it to tensor
+        // memory, and decodes the second while that store is in flight; one wait covers both.
         const int g = (warp - kWarpDec0) >> 2;
         const int qw = warp & 3;
         const int nl = 32 * qw + lane;
+        const uint32_t m3 = p.m3, m15 = p.m15;
         int64_t cur_tile = -1;
-        uint32_t base2 = 0;
-        for (int j = g; j < nrec; j += kDecGroups) {
-            const int s = j % S, t = j % kASlots;
-            const bool ok_full = mbar_wait(smem_u32(&ctrl->full[s]), (j / S) & 1, abort, p.err, kErrDecode);
-            if (!__all_sync(0xFFFFFFFFu, ok_full)) break;
-            const int64_t r = r0 + j;
-            const int64_t tile = r / kt64;
+        uint32_t cur_base2 = 0;
+        auto base2_for = [&](int64_t tile) -> uint32_t {
             if (tile != cur_tile) {
                 cur_tile = tile;
-                base2 = base2_of(__ldg(p.base_exp + tile * kTileN + nl));
+                cur_base2 = base2_of(__ldg(p.base_exp + tile * kTileN + nl));
             }
-            const uint8_t *rec = stage_rec(s);
-            uint32_t w[32];
+            return cur_base2;
+        };
+        // decode this thread's row of record q of slot s into w (escapes patched)
+        auto decode_record = [&](int s, int q, uint32_t base2, uint32_t (&w)[32]) {
+            const uint8_t *rec = stage_rec(s, q);
             const uint4 v0 = lds128(rec + 0 * 2048 + 16 * nl);
             const uint4 v1 = lds128(rec + 1 * 2048 + 16 * nl);
             const uint4 v2 = lds128(rec + 2 * 2048 + 16 * nl);
             const uint4 v3 = lds128(rec + 3 * 2048 + 16 * nl);
             if (kQView) {
                 const uint4 z = make_uint4(0, 0, 0, 0);
-                decode_chunk16<true, 0>(v0, z, base2, w);
-                decode_chunk16<true, 1>(v1, z, base2, w + 8);
-                decode_chunk16<true, 0>(v2, z, base2, w + 16);
-                decode_chunk16<true, 1>(v3, z, base2, w + 24);
-            } else {
-                const uint4 b0 = lds128(rec + kViewBytes + 16 * nl);
-                const uint4 b1 = lds128(rec + kViewBytes + 2048 + 16 * nl);
-                decode_chunk16<false, 0>(v0, b0, base2, w);
-                decode_chunk16<false, 1>(v1, b0, base2, w + 8);
-                decode_chunk16<false, 0>(v2, b1, base2, w + 16);
-                decode_chunk16<false, 1>(v3, b1, base2, w + 24);
-                // escapes of this record that fall in this warp's 32 rows
-                const uint32_t hdr = ctrl->esc_hdr[s];
-                const uint32_t cnt = hdr & 0x7FFFFFFFu;
-                const bool from_global = (hdr >> 31) != 0;
-                const uint32_t *gsrc = p.rec_esc + (from_global ? ctrl->esc_src[s] : 0u);
-                const uint32_t *ssrc = reinterpret_cast<const uint32_t *>(stage_esc(s));
-                for (uint32_t base = 0; base < cnt; base += 32) {
-                    uint32_t e = 0xFFFFFFFFu;
-                    if (base + lane < cnt) e = from_global ? __ldg(gsrc + base + lane) : ssrc[base + lane];
-                    const uint32_t pos = e & 0xFFFFu;
-                    uint32_t mine = __ballot_sync(0xFFFFFFFFu, pos < static_cast<uint32_t>(kRecordWeights) &&
-                                                                   (pos >> 11) == static_cast<uint32_t>(qw));
-                    while (mine) {
-                        const int sl = __ffs(mine) - 1;
-                        mine &= mine - 1;
-                        const uint32_t ent = __shfl_sync(0xFFFFFFFFu, e, sl);
-                        const uint32_t ps = ent & 0xFFFFu;
-                        const int owner = static_cast<int>((ps >> 6) & 31u);
-                        const int kl = static_cast<int>(ps & 63u);
-                        const bool hi = kl & 1;
-                        const bool me = lane == owner;
-                        const uint32_t keep = me ? (hi ? 0x0000FFFFu : 0xFFFF0000u) : 0xFFFFFFFFu;
-                        const uint32_t val = me ? (hi ? (ent & 0xFFFF0000u) : (ent >> 16)) : 0u;
-                        patch_word(w, kl >> 1, keep, val);
-                    }
-                }
+                decode_chunk16<true, 0>(v0, z, base2, w, m3, m15);
+                decode_chunk16<true, 1>(v1, z, base2, w + 8, m3, m15);
+                decode_chunk16<true, 0>(v2, z, base2, w + 16, m3, m15);
+                decode_chunk16<true, 1>(v3, z, base2, w + 24, m3, m15);
+                return;
             }
-            const bool ok_a = mbar_wait(smem_u32(&ctrl->aempty[t]), ((j / kASlots) & 1) ^ 1, abort, p.err, kErrDecode);
-            if (!__all_sync(0xFFFFFFFFu, ok_a)) break;
+            const uint4 b0 = lds128(rec + kViewBytes + 16 * nl);
+            const uint4 b1 = lds128(rec + kViewBytes + 2048 + 16 * nl);
+            decode_chunk16<false, 0>(v0, b0, base2, w, m3, m15);
+            decode_chunk16<false, 1>(v1, b0, base2, w + 8, m3, m15);
+            decode_chunk16<false, 0>(v2, b1, base2, w + 16, m3, m15);
+            decode_chunk16<false, 1>(v3, b1, base2, w + 24, m3, m15);
+        };
+        // Restore the escapes of record q of slot s that fall in this warp's 32 rows, in tensor
+        // memory after the decoded record was stored there: read the entry's column, let the
+        // owner lane overwrite its half, write the column back. One entry per round trip (a
+        // few instructions each; the typical warp has 0-3). The segment header gives the
+        // warp's entry range directly; every lane reads the same entry (a broadcast), so the
+        // control flow is warp-uniform.
+        auto patch_record = [&](int s, int q) {
+            const uint32_t hdr = ctrl->esc_cnt[s];
+            const uint32_t total = hdr & 0x7FFFFFFFu;
+            const uint32_t split = ctrl->esc_split[s];
+            const uint32_t sg0 = (q == 0) ? 0u : split, sg1 = (q == 0) ? split : total;
+            if (sg1 <= sg0) return;
+            const uint32_t *seg = ((hdr >> 31) ? p.rec_esc + ctrl->esc_src[s]
+                                               : reinterpret_cast<const uint32_t *>(stage_esc(s))) + sg0;
+            const uint32_t i_hi = seg[qw];
+            const uint32_t tbase = a_slot(s, q) + (static_cast<uint32_t>(32 * qw) << 16);
+            for (uint32_t i = (qw == 0) ? 0u : seg[qw - 1]; i < i_hi; ++i) {
+                const uint32_t ent = seg[4 + i];
+                const uint32_t taddr = tbase + ((ent & 63u) >> 1);
+                const uint32_t old = tmem_ld_32x32b_x1(taddr);
+                tmem_wait_ld();
+                const uint32_t nv = (ent & 1u) ? ((old & 0x0000FFFFu) | (ent & 0xFFFF0000u))
+                                               : ((old & 0xFFFF0000u) | (ent >> 16));
+                tmem_st_32x32b_x1(taddr, lane == static_cast<int>((ent >> 6) & 31u) ? nv : old);
+                tmem_wait_st();
+            }
+        };
+        int js = g;
+        Ring st;
+        st.advance(js, S);
+        int64_t tile = (r0 + static_cast<int64_t>(js) * RPS) / kt64;  // tile and k tile of the
+        int kt = static_cast<int>((r0 + static_cast<int64_t>(js) * RPS) % kt64);  // slot's first record
+        uint32_t wa[32], wb[32];
+        for (; js < nst; js += kDecGroups) {
+            const int s = st.idx;
+            const bool ok_full = mbar_wait(smem_u32(&ctrl->full[s]), st.phase, abort, p.err, kErrDecode);
+            if (!__all_sync(0xFFFFFFFFu, ok_full)) break;
+            const int nr = min(RPS, nrec - js * RPS);
+            // the slot's tensor-memory buffers are free: the producer refilled this slot only
+            // after the MMAs that last read it completed
+            decode_record(s, 0, base2_for(tile), wa);
             tc_fence_after();
-            tmem_st_32x32b_x32(tmem + (static_cast<uint32_t>(32 * qw) << 16) + t * kACols, w);
+            tmem_st_32x32b_x32(a_slot(s, 0) + (static_cast<uint32_t>(32 * qw) << 16), wa);
+            if (nr == 2) {
+                const int64_t tile1 = (kt + 1 == p.k_tiles) ? tile + 1 : tile;
+                decode_record(s, 1, base2_for(tile1), wb);
+                tmem_st_32x32b_x32(a_slot(s, 1) + (static_cast<uint32_t>(32 * qw) << 16), wb);
+            }
             tmem_wait_st();
+            if (!kQView) {
+                patch_record(s, 0);
+                if (nr == 2) patch_record(s, 1);
+            }
             tc_fence_before();
-            mbar_arrive(smem_u32(&ctrl->afull[t]));
+            mbar_arrive(smem_u32(&ctrl->afull[s]));
+            st.advance(kDecGroups, S);
+            kt += RPS * kDecGroups;
+            while (kt >= p.k_tiles) {
+                kt -= p.k_tiles;
+                ++tile;
+            }
         }
     } else if (warp >= kWarpEpi0 && warp < kWarpEpi0 + 4) {
         // ---------------------------------------------------------------- epilogue
+        // A segment that covers a whole tile is written directly. A tile split between blocks
+        // is summed in increasing block order by the block that finishes it: if every other
+        // block has already published its partial (the usual case for a block's last segment),
+        // this block adds them to its own values straight from tensor memory; otherwise it
+        // publishes its partial and whichever block publishes last sums all of them. Both
+        // routes add the same values in the same order.
         const int qw = warp & 3;
         const int nl = 32 * qw + lane;
         const int et = threadIdx.x - kWarpEpi0 * 32;  // 0..127
@@ -358,11 +441,33 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         bool dead = false;
         int jseg = 0;
         int64_t r = r0;
+        auto store_y = [&](int m, int n, float f) {
+            if (p.y_bf16)
+                reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(f);
+            else
+                reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] = f;
+        };
+        // one output value of row m (warp-uniform call): y, or this warp's top-2 of the row
+        auto emit = [&](int m, int n, float f) {
+            if (kArgmax) {
+                float v1 = (n < p.N && !isnan(f)) ? f : -INFINITY, v2 = -INFINITY;
+                int i1 = n;
+                warp_top2(v1, i1, v2);
+                if (lane == 0) ctrl->wtop[qw][m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
+            } else if (n < p.N) {
+                store_y(m, n, f);
+            }
+        };
+        auto partial_of = [&](int64_t cc, int64_t tile, int m) {  // block cc's partial of tile
+            const int sl = (range_start(cc, R, G) / kt64 == tile) ? 0 : 1;
+            return p.partials + ((static_cast<size_t>(cc) * 2 + sl) * M + m) * kTileN + nl;
+        };
         while (r < r1) {
             const int64_t tile = r / kt64;
             const int64_t seg_start = r, seg_end = min(r1, (tile + 1) * kt64);
             r = seg_end;
             const bool full = seg_start == tile * kt64 && seg_end == (tile + 1) * kt64;
+            const int par = jseg & 1;
             const int slot = (jseg == 0) ? 0 : 1;
             const int b = (p.nacc == 2) ? (jseg & 1) : 0;
             const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
@@ -371,85 +476,100 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             bool ok = !dead && mbar_wait(smem_u32(&ctrl->accfull[b]), phb, abort, p.err, kErrEpilogue);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) dead = true;
+            const int64_t c_lo = full ? c : owner_of(tile * kt64, R, G);
+            const int64_t c_hi = full ? c : owner_of((tile + 1) * kt64 - 1, R, G);
+            // 0: whole tile here; 1: publish a partial; 2: sum here from the published partials
+            int mode = 0;
+            if (!full) {
+                if (et == 0)
+                    ctrl->mode[par] = (ld_acquire_gpu(&p.tile_cnt[tile]) == static_cast<uint32_t>(c_hi - c_lo)) ? 2 : 1;
+                named_bar_sync(kEpiBar, 128);
+                mode = ctrl->mode[par];
+                if (mode == 2) fence_acq_rel_gpu();
+            }
             float *part = p.partials + (static_cast<size_t>(c) * 2 + slot) * M * kTileN;
             if (!dead) {
                 tc_fence_after();
-                const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * qw) << 16) + kAccCol0 + b * p.npad;
+                const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * qw) << 16) + b * p.npad;
                 for (int m0 = 0; m0 < M; m0 += 16) {
                     uint32_t v[16];
                     tmem_ld_32x32b_x16(tbase + m0, v);
                     tmem_wait_ld();
+                    float f[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                    if (mode == 2) {
+                        float acc[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+                        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+                            if (cc == c) {
+#pragma unroll
+                                for (int i = 0; i < 16; ++i) acc[i] += f[i];
+                            } else {
+                                const float *src = partial_of(cc, tile, m0);
+#pragma unroll
+                                for (int i = 0; i < 16; ++i)
+                                    if (m0 + i < M) acc[i] += __ldcg(src + static_cast<size_t>(i) * kTileN);
+                            }
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = acc[i];
+                    }
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const int m = m0 + i;
                         if (m >= M) break;
-                        const float f = __uint_as_float(v[i]);
-                        if (!full) {
-                            part[static_cast<size_t>(m) * kTileN + nl] = f;
-                        } else if (kArgmax) {
-                            float v1 = (n < p.N && !isnan(f)) ? f : -INFINITY, v2 = -INFINITY;
-                            int i1 = n;
-                            warp_top2(v1, i1, v2);
-                            if (lane == 0) ctrl->wtop[qw][m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
-                        } else if (n < p.N) {
-                            if (p.y_bf16)
-                                reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(f);
-                            else
-                                reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] = f;
-                        }
+                        if (mode == 1)
+                            part[static_cast<size_t>(m) * kTileN + nl] = f[i];
+                        else
+                            emit(m, n, f[i]);
                     }
                 }
                 tc_fence_before();
             }
             mbar_arrive(smem_u32(&ctrl->accempty[b]));
 
-            bool emitted = full;
-            if (!full) {
-                // split tile: the last block to arrive sums every block's partial in block order
-                __threadfence();
+            bool emitted = (mode != 1);
+            if (mode == 1) {
+                fence_acq_rel_gpu();  // this thread's partial stores come before the count
                 named_bar_sync(kEpiBar, 128);
                 if (et == 0) {
-                    const int64_t c_lo = owner_of(tile * kt64, R, G);
-                    const int64_t c_hi = owner_of((tile + 1) * kt64 - 1, R, G);
                     const uint32_t old = atomicAdd(&p.tile_cnt[tile], 1u);
-                    ctrl->fix = (old == static_cast<uint32_t>(c_hi - c_lo)) ? 1 : 0;
+                    ctrl->last[par] = (old == static_cast<uint32_t>(c_hi - c_lo)) ? 1 : 0;
                 }
                 named_bar_sync(kEpiBar, 128);
-                emitted = ctrl->fix != 0;
-                if (emitted) {
-                    __threadfence();
-                    const int64_t c_lo = owner_of(tile * kt64, R, G);
-                    const int64_t c_hi = owner_of((tile + 1) * kt64 - 1, R, G);
-                    for (int m = 0; m < M; ++m) {
-                        float f = 0.f;
+                emitted = ctrl->last[par] != 0;
+                if (emitted) {  // published last: sum every block's partial, 16 rows at a time
+                    fence_acq_rel_gpu();
+                    for (int m0 = 0; m0 < M; m0 += 16) {
+                        float f[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = 0.f;
                         for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
-                            const int sl = (range_start(cc, R, G) / kt64 == tile) ? 0 : 1;
-                            f += __ldcg(p.partials + ((static_cast<size_t>(cc) * 2 + sl) * M + m) * kTileN + nl);
+                            const float *src = partial_of(cc, tile, m0);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                if (m0 + i < M) f[i] += __ldcg(src + static_cast<size_t>(i) * kTileN);
                         }
-                        if (kArgmax) {
-                            float v1 = (n < p.N && !isnan(f)) ? f : -INFINITY, v2 = -INFINITY;
-                            int i1 = n;
-                            warp_top2(v1, i1, v2);
-                            if (lane == 0) ctrl->wtop[qw][m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
-                        } else if (n < p.N) {
-                            if (p.y_bf16)
-                                reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(f);
-                            else
-                                reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] = f;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (m0 + i >= M) break;
+                            emit(m0 + i, n, f[i]);
                         }
                     }
-                    if (et == 0) p.tile_cnt[tile] = 0;  // leave the workspace zeroed
                 }
             }
+            if (mode != 0 && emitted && et == 0) p.tile_cnt[tile] = 0;  // leave the workspace zeroed
             if (kArgmax && emitted) {
                 named_bar_sync(kEpiBar, 128);
                 for (int m = et; m < M; m += 128) {
-                    float4 a = ctrl->ctop[m];
-                    float v1 = a.x, v2 = a.z;
-                    int i1 = __float_as_int(a.y);
+                    float4 a4 = ctrl->ctop[m];
+                    float v1 = a4.x, v2 = a4.z;
+                    int i1 = __float_as_int(a4.y);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float4 o = ctrl->wtop[q][m];
+                    for (int qq = 0; qq < 4; ++qq) {
+                        const float4 o = ctrl->wtop[qq][m];
                         top2_merge(v1, i1, v2, o.x, __float_as_int(o.y), o.z);
                     }
                     ctrl->ctop[m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
@@ -489,17 +609,17 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
     __syncthreads();
     if (warp == kWarpProducer && lane == 0 && ctrl->abort) {
         // let copies still in flight land before the block's shared memory is released
-        for (int j = (issued > S ? issued - S : 0); j < issued; ++j)
-            if (!mbar_wait_drain(smem_u32(&ctrl->full[j % S]), (j / S) & 1)) atomicOr(p.err, kErrDrain);
+        for (int js = (issued > S ? issued - S : 0); js < issued; ++js)  // cold path
+            if (!mbar_wait_drain(smem_u32(&ctrl->full[js % S]), (js / S) & 1)) atomicOr(p.err, kErrDrain);
     }
     if (warp == kWarpMma) {
-        if (lane == 0 && issued > 0) {
-            mma_commit(smem_u32(&ctrl->done));
-            if (!mbar_wait_drain(smem_u32(&ctrl->done), 0)) atomicOr(p.err, kErrDrain);
+        if (issued > 0) {
+            mma_commit_elect(smem_u32(&ctrl->done));  // same elected lane that issued the MMAs
+            if (!mbar_wait_drain(smem_u32(&ctrl->done), 0) && lane == 0) atomicOr(p.err, kErrDrain);
         }
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, p.ncols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -522,7 +642,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 struct Layout {
-    int npad, stages, nacc, ncols, grid, smem;
+    int npad, stages, rps, nacc, acc_cols, grid, smem;
     int64_t R;
     size_t ws_bytes, off_err, off_tile, off_done, off_part, off_top;
 };
@@ -535,16 +655,21 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX);
     L->R = static_cast<int64_t>(t->n_tiles) * t->k_tiles;
     L->npad = (M + 15) / 16 * 16;
-    const int sbytes = L->npad * 128 + (q ? kViewBytes : kRecordBytes) + (q ? 0 : kEscCap * 4);
+    // two records per ring slot while the activation tiles are small
+    L->rps = (L->npad <= 64) ? 2 : 1;
+    const int sbytes = L->rps * (L->npad * 128 + (q ? kViewBytes : kRecordBytes)) + (q ? 0 : kEscCap * 4);
     const int ctrl = static_cast<int>(align_up(sizeof(Ctrl), 1024));
-    L->stages = (kSmemLimit - 1024 - ctrl) / sbytes;
-    if (L->stages > kMaxStages) L->stages = kMaxStages;
-    if (L->stages < 2) return W12_ERR_UNSUPPORTED_SHAPE;
-    L->smem = 1024 + L->stages * sbytes + ctrl;
+    int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
+    if (stages > kMaxStages) stages = kMaxStages;
+    // tensor memory: nacc accumulators of npad columns, then 32 columns per record in flight
+    L->nacc = (2 * L->npad + 4 * L->rps * kACols <= kTmemCols) ? 2 : 1;
+    L->acc_cols = L->nacc * L->npad;
+    const int tmem_stages = (kTmemCols - L->acc_cols) / (L->rps * kACols);
+    if (stages > tmem_stages) stages = tmem_stages;
+    if (stages < 2) return W12_ERR_UNSUPPORTED_SHAPE;
+    L->stages = stages;
+    L->smem = 1024 + stages * sbytes + ctrl;
     if (L->smem < kSmemFloor) L->smem = kSmemFloor;
-    L->nacc = (kAccCol0 + 2 * L->npad <= 512) ? 2 : 1;
-    const int cols = kAccCol0 + L->nacc * L->npad;
-    L->ncols = cols <= 256 ? 256 : 512;
     L->grid = static_cast<int>(L->R < sms ? L->R : sms);
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -607,8 +732,11 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.k_tiles = t->k_tiles;
     p.npad = L.npad;
     p.stages = L.stages;
+    p.rps = L.rps;
+    p.m3 = 8u;
+    p.m15 = 32768u;
     p.nacc = L.nacc;
-    p.ncols = L.ncols;
+    p.acc_cols = L.acc_cols;
     p.grid = L.grid;
     p.R = L.R;
     p.y = y;

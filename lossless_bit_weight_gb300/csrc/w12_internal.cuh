@@ -87,14 +87,30 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Non-blocking probe of a phase (no suspension; the fast path of a wait that is already done).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Blocking probe: the thread sleeps (issuing nothing) until the phase completes or about
+// `kSuspendNs` pass, so waiting warps leave the issue slots to the working ones.
+constexpr uint32_t kSuspendNs = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
         : "memory");
     return ok != 0;
 }
@@ -104,11 +120,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // raises `abort` and records `code` in the global error word.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
                                           int *gerr, int code) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
+        if ((it & 3u) == 0) {
             if (*abort) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 *abort = 1;
@@ -151,6 +167,45 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
+// ---- issue from a converged warp -------------------------------------------------------------
+// The copy-engine and tensor-core instructions below are issued once per warp by the lane that
+// elect.sync picks (the same lane every time when the whole warp is active), with the rest of the
+// warp converged and computing the same operands. Issuing them from a single diverged thread
+// costs several times more cycles per instruction on sm_103.
+
+__device__ __forceinline__ void mbar_arrive_expect_tx_elect(uint32_t bar, uint32_t bytes) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+        "@P mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n\t}"
+        ::"r"(bar), "r"(bytes)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+        "@P mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}"
+        ::"r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_elect(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+        "@P cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n\t}"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_2d_g2s_elect(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+        "@P cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];\n\t}"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
 // ---- tcgen05 (5th-generation tensor cores, tensor memory) ---------------------------------
 
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
@@ -183,6 +238,27 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
         : "memory");
 }
 
+// The same MMA issued by the elected lane of a converged warp.
+__device__ __forceinline__ void mma_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                  uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t.reg .pred A;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "setp.ne.b32 A, %4, 0;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, A;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Commit from the elected lane (the lane that issued the MMAs it must track).
+__device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+        "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(bar)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
@@ -210,6 +286,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
         "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
+}
+
+// One 32-bit column of the warp's 32 lanes (each lane its own value).
+__device__ __forceinline__ uint32_t tmem_ld_32x32b_x1(uint32_t taddr) {
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 
 // Each lane loads 16 consecutive 32-bit columns of its own TMEM lane.
@@ -245,6 +331,14 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
          | ((m >> 4) << 24);      // M / 16
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -263,15 +357,20 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
 //   x     = view bytes of the two weights at bits 0..7 and 16..23 (byte = E<<4 | m_hi<<1 | s)
 //   bs    = plane-B word shifted so the two low-mantissa nibbles sit at bits 0..3 and 16..19
 //   base2 = (E_n - 15) << 7 in both halves
-// x << 3 puts m_hi at bits 4..6 and E at 7..10 (its stray sign bit lands at bit 3, which the
-// nibble select overwrites); x << 15 puts each sign at bit 15 / 31. Adding base2 turns E into
-// the biased exponent; E + E_n - 15 <= 254, so the sum never carries into the sign bit.
+//   m3 = 8, m15 = 32768 (the multipliers of the two shifts)
+// t = x*8 + base2 puts m_hi at bits 4..6 and E + E_n - 15 (<= 254: no carry into the sign) at
+// bits 7..14; its stray sign bit lands at bit 3, which the nibble select overwrites.
+// u = x*32768 puts each sign at bit 15 / 31. Callers that are bound by the integer ALU pass
+// the multipliers as run-time values so both run as multiply-adds on the FMA pipe; the ALU
+// then does one byte permute and two 3-input logic ops per word.
 template <bool kQView>
-__device__ __forceinline__ uint32_t decode_pair(uint32_t x, uint32_t bs, uint32_t base2) {
-    const uint32_t t = x << 3, u = x << 15;
+__device__ __forceinline__ uint32_t decode_pair(uint32_t x, uint32_t bs, uint32_t base2, uint32_t m3,
+                                                uint32_t m15) {
+    const uint32_t t = x * m3 + base2;
+    const uint32_t u = x * m15;
     const uint32_t r1 = (u & 0x80008000u) | (t & 0x7FFF7FFFu);
-    if (kQView) return (r1 & 0xFFF0FFF0u) + (base2 + 0x00080008u);  // low mantissa := 1000b
-    return ((bs & 0x000F000Fu) | (r1 & 0xFFF0FFF0u)) + base2;
+    if (kQView) return (r1 & 0xFFF0FFF0u) | 0x00080008u;  // low mantissa := 1000b
+    return (bs & 0x000F000Fu) | (r1 & 0xFFF0FFF0u);
 }
 
 // Sixteen weights k_l = 16c .. 16c+15 of one channel row -> 8 bf16x2 words.
@@ -279,15 +378,16 @@ __device__ __forceinline__ uint32_t decode_pair(uint32_t x, uint32_t bs, uint32_
 //   kOdd = c & 1 (selects which half of the plane-B chunk holds these k).
 template <bool kQView, int kOdd>
 __device__ __forceinline__ void decode_chunk16(const uint4 &v, const uint4 &b, uint32_t base2,
-                                               uint32_t *out) {
+                                               uint32_t *out, uint32_t m3 = 8u,
+                                               uint32_t m15 = 32768u) {
     const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
     const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         const uint32_t B = bw[2 * kOdd + (q >> 1)];
         const int sh = 8 * (q & 1);
-        out[2 * q] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4140u), B >> sh, base2);
-        out[2 * q + 1] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4342u), B >> (sh + 4), base2);
+        out[2 * q] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4140u), B >> sh, base2, m3, m15);
+        out[2 * q + 1] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4342u), B >> (sh + 4), base2, m3, m15);
     }
 }
 

@@ -110,7 +110,7 @@ static void store_u32le(uint8_t *p, uint32_t v) {
 
 /* ---- sizes ------------------------------------------------------------------------------- */
 
-/* Counts of the canonical escape list and of the padded per-record index. */
+/* Counts of the canonical escape list and of the per-record index (words, headers included). */
 void w12o_count(const uint16_t *w, int N, int K, int64_t *n_esc, int64_t *n_rec_esc) {
     int n_tiles = (N + W12O_TILE_N - 1) / W12O_TILE_N;
     int k_tiles = (K + W12O_TILE_K - 1) / W12O_TILE_K;
@@ -130,7 +130,7 @@ void w12o_count(const uint16_t *w, int N, int K, int64_t *n_esc, int64_t *n_rec_
                 }
             }
             total += c;
-            total_rec += (c + 3) / 4 * 4;
+            total_rec += (c > 0) ? 4 + (c + 3) / 4 * 4 : 0;
         }
     free(En);
     *n_esc = total;
@@ -165,7 +165,9 @@ void w12o_encode(const uint16_t *w, int N, int K,
     }
     esc_off[N] = pos;
 
-    /* step 3: records (planes) and the per-record escape index */
+    /* step 3: records (planes) and the per-record escape index: per record with escapes, a
+     * header of 4 cumulative quarter counts (rows < 32, < 64, < 96, < 128), its entries in
+     * increasing pos, then padding to a multiple of 4 words */
     memset(records, 0, (size_t)n_tiles * k_tiles * W12O_RECORD_BYTES);
     uint32_t rpos = 0;
     for (int nt = 0; nt < n_tiles; ++nt)
@@ -173,6 +175,9 @@ void w12o_encode(const uint16_t *w, int N, int K,
             size_t r = (size_t)nt * k_tiles + kt;
             uint8_t *rec = records + r * W12O_RECORD_BYTES;
             rec_esc_off[r] = rpos;
+            uint32_t quarter_end[4] = {0, 0, 0, 0};
+            uint32_t count = 0;
+            /* first pass: planes, and the escapes counted per quarter */
             for (int nl = 0; nl < W12O_TILE_N; ++nl)
                 for (int kl = 0; kl < W12O_TILE_K; ++kl) {
                     int n = nt * W12O_TILE_N + nl, k = kt * W12O_TILE_K + kl;
@@ -186,9 +191,20 @@ void w12o_encode(const uint16_t *w, int N, int K,
                     word |= (uint32_t)b << (4 * b_nibble_pos(kl));
                     store_u32le(bw, word);
                     if (!in_window(u, base_exp[n])) {
-                        rec_esc[rpos] = (uint32_t)(nl * W12O_TILE_K + kl) | ((uint32_t)u << 16);
-                        rpos += 1;
+                        count += 1;
+                        for (int q = nl / 32; q < 4; ++q) quarter_end[q] += 1;
                     }
+                }
+            if (count == 0) continue; /* no escapes: an empty segment */
+            for (int q = 0; q < 4; ++q) rec_esc[rpos++] = quarter_end[q];
+            /* second pass: the entries, in increasing pos = 64 * n_l + k_l */
+            for (int nl = 0; nl < W12O_TILE_N; ++nl)
+                for (int kl = 0; kl < W12O_TILE_K; ++kl) {
+                    int n = nt * W12O_TILE_N + nl, k = kt * W12O_TILE_K + kl;
+                    if (n >= N || k >= K) continue;
+                    uint16_t u = w[(size_t)n * K + k];
+                    if (!in_window(u, base_exp[n]))
+                        rec_esc[rpos++] = (uint32_t)(nl * W12O_TILE_K + kl) | ((uint32_t)u << 16);
                 }
             while (rpos % 4 != 0) rec_esc[rpos++] = 0xFFFFFFFFu;
         }
@@ -216,7 +232,9 @@ void w12o_decode(const uint8_t *records, const uint8_t *base_exp,
                     int e = E + base_exp[n] - 15;
                     w_out[(size_t)n * K + k] = (uint16_t)((s << 15) | (e << 7) | (mhi << 4) | b);
                 }
-            for (uint32_t i = rec_esc_off[r]; i < rec_esc_off[r + 1]; ++i) {
+            /* a non-empty segment starts with its 4-word quarter header */
+            uint32_t first = rec_esc_off[r] + (rec_esc_off[r + 1] > rec_esc_off[r] ? 4u : 0u);
+            for (uint32_t i = first; i < rec_esc_off[r + 1]; ++i) {
                 uint32_t ent = rec_esc[i];
                 uint32_t p = ent & 0xFFFF;
                 if (p >= (uint32_t)(W12O_TILE_N * W12O_TILE_K)) continue; /* padding entry */

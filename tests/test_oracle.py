@@ -126,6 +126,7 @@ def test_escape_set_matches_definition(orc):
 
 def test_per_record_index_is_a_regrouping_of_the_csr(orc):
     w = synth.bits(synth.weights(300, 200, synth.TINY, seed=9))
+    w[130:200, 70:100] = 0  # escapes in several 32-row quarters of a record
     e = orc.encode(w)
     from_csr = set()
     for n in range(e.N):
@@ -137,9 +138,16 @@ def test_per_record_index_is_a_regrouping_of_the_csr(orc):
         nt, kt = divmod(r, e.k_tiles)
         seg = e.rec_esc[e.rec_esc_off[r]:e.rec_esc_off[r + 1]]
         assert seg.size % 4 == 0
-        real = seg[seg != 0xFFFFFFFF]
+        if seg.size == 0:
+            continue
+        header, body = seg[:4], seg[4:]
+        real = body[body != 0xFFFFFFFF]
+        assert real.size > 0 and int(header[3]) == real.size
         pos = real & 0xFFFF
         assert np.all(np.diff(pos.astype(np.int64)) > 0)
+        quarter = (pos >> 11).astype(np.int64)
+        for q in range(4):
+            assert int(header[q]) == int(np.count_nonzero(quarter <= q))
         for ent in real:
             p = int(ent) & 0xFFFF
             from_rec.add((nt * 128 + p // 64, kt * 64 + p % 64, int(ent) >> 16))
@@ -200,7 +208,7 @@ def test_golden_layout_fixture(orc):
             else:
                 raise AssertionError(t)
             checked += 1
-    assert checked > 40
+    assert checked > 50
     assert np.array_equal(orc.decode(e), w)
 
 
