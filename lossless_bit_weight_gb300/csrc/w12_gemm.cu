@@ -43,6 +43,7 @@ static_assert(kDecGroups >= 1 && kDecGroups <= 4, "one to four decode groups");
 constexpr int kWarpProducer = 0;
 constexpr int kWarpMma = 1;
 constexpr int kWarpEscape = 2;
+constexpr int kWarpMma2 = 3;  // second MMA issuer (the second record of each slot)
 constexpr int kWarpEpi0 = 4;
 constexpr int kWarpDec0 = 8;
 constexpr int kEscCap = 512;       // escape entries staged per slot; more -> read from global
@@ -57,7 +58,7 @@ constexpr int kEpiBar = 1;               // named barrier of the 128 epilogue th
 struct Ctrl {
     uint64_t full[kMaxStages], afull[kMaxStages], empty[kMaxStages];
     uint64_t accfull[2], accempty[2];
-    uint64_t done;
+    uint64_t done[2];
     uint32_t esc_cnt[kMaxStages];    // entries of the slot (bit 31: too many, read from global)
     uint32_t esc_split[kMaxStages];  // entries that belong to the slot's first record
     uint32_t esc_src[kMaxStages];    // index of the slot's first entry in the global index
@@ -190,13 +191,14 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             for (int s = 0; s < S; ++s) {
                 mbar_init(smem_u32(&ctrl->full[s]), kQView ? 1 : 2);
                 mbar_init(smem_u32(&ctrl->afull[s]), 128);
-                mbar_init(smem_u32(&ctrl->empty[s]), 1);
+                mbar_init(smem_u32(&ctrl->empty[s]), RPS);  // one commit per MMA issuer
             }
             for (int b = 0; b < 2; ++b) {
-                mbar_init(smem_u32(&ctrl->accfull[b]), 1);
+                mbar_init(smem_u32(&ctrl->accfull[b]), RPS);
                 mbar_init(smem_u32(&ctrl->accempty[b]), 128);
             }
-            mbar_init(smem_u32(&ctrl->done), 1);
+            mbar_init(smem_u32(&ctrl->done[0]), 1);
+            mbar_init(smem_u32(&ctrl->done[1]), 1);
             ctrl->abort = 0;
             ctrl->fix = 0;
             fence_barrier_init();
@@ -228,54 +230,57 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             produce(js);
         }
-    } else if (warp == kWarpMma) {
-        // ---------------------------------------------------------------- MMA issuer (warp-wide)
+    } else if (warp == kWarpMma || (warp == kWarpMma2 && RPS == 2)) {
+        // ---------------------------------------------------------------- MMA issuers (warp-wide)
+        // With two records per slot, issuer mq = 0 (warp 1) takes the first record of every slot
+        // and issuer mq = 1 (warp 3) the second, each into an accumulator of its own: a single
+        // warp cannot issue the MMAs of both records in the time the copy engine brings them.
+        // Per segment each issuer overwrites its accumulator with its first record, adds the
+        // rest, and commits (or, without a record in the segment, just arrives on) accfull.
+        const int mq = (warp == kWarpMma) ? 0 : 1;
         const uint32_t idesc = idesc_bf16_f32(128, p.npad);
         Ring st;
+        int js_next = 0;  // ring position of st: the slot of this issuer's next record
         int jseg = 0;
-        bool open = false;
-        int b = 0;
-        uint32_t d = 0;
-        int64_t seg_start = r0;
-        int64_t seg_end = min(r1, (r0 / kt64 + 1) * kt64);
-        for (int js = 0; js < nst; ++js) {
-            const int s = st.idx;
-            const bool okw = mbar_wait(smem_u32(&ctrl->afull[s]), st.phase, abort, p.err, kErrMma);
-            if (!__all_sync(0xFFFFFFFFu, okw)) break;
+        bool ok = true;
+        for (int64_t seg_start = r0; ok && seg_start < r1; ++jseg) {
+            const int64_t seg_end = min(r1, (seg_start / kt64 + 1) * kt64);
+            const int b = (p.nacc == 2) ? (jseg & 1) : 0;
+            const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
+            // this issuer's records r in [seg_start, seg_end) have (r - r0) % RPS == mq
+            int64_t r = seg_start + ((seg_start - r0 - mq) & (RPS - 1));
+            const int64_t first = r;
+            const bool oka = mbar_wait(smem_u32(&ctrl->accempty[b]), phb ^ 1, abort, p.err, kErrMma);
+            if (!__all_sync(0xFFFFFFFFu, oka)) break;
             tc_fence_after();
-            const int nr = min(RPS, nrec - js * RPS);
-            bool ok = true;
-            for (int q = 0; q < nr; ++q) {
-                const int64_t r = r0 + js * RPS + q;
-                if (!open) {
-                    b = (p.nacc == 2) ? (jseg & 1) : 0;
-                    const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
-                    const bool oka = mbar_wait(smem_u32(&ctrl->accempty[b]), phb ^ 1, abort, p.err, kErrMma);
-                    if (!__all_sync(0xFFFFFFFFu, oka)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    d = tmem + b * p.npad;
-                    open = true;
+            const uint32_t d = tmem + (mq * p.nacc + b) * p.npad;
+            for (; r < seg_end; r += RPS) {
+                const int js = static_cast<int>((r - r0) / RPS);
+                st.advance(js - js_next, S);
+                js_next = js;
+                const int s = st.idx;
+                const bool okw = mbar_wait(smem_u32(&ctrl->afull[s]), st.phase, abort, p.err, kErrMma);
+                if (!__all_sync(0xFFFFFFFFu, okw)) {
+                    ok = false;
+                    break;
                 }
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(stage_x(s, q)));
-                const uint32_t a = a_slot(s, q);
-#pragma unroll
-                for (int kk = 0; kk < kTileK / 16; ++kk)
-                    mma_bf16_ts_elect(d, a + kk * 8, bdesc + 2 * kk, idesc, (r != seg_start || kk != 0) ? 1u : 0u);
-                if (r + 1 == seg_end) {
-                    mma_commit_elect(smem_u32(&ctrl->accfull[b]));
-                    ++jseg;
-                    open = false;
-                    seg_start = seg_end;
-                    seg_end = min(r1, seg_end + kt64);
-                }
+                tc_fence_after();
+                const uint64_t bdesc = smem_desc_sw128(smem_u32(stage_x(s, mq)));
+                const uint32_t a = a_slot(s, mq);
+                // the issuer's first MMA of a segment overwrites its accumulator; the rest add
+                mma_bf16_ts_elect(d, a, bdesc, idesc, r != first ? 1u : 0u);
+                mma_bf16_ts_acc_elect(d, a + 8, bdesc + 2, idesc);
+                mma_bf16_ts_acc_elect(d, a + 16, bdesc + 4, idesc);
+                mma_bf16_ts_acc_elect(d, a + 24, bdesc + 6, idesc);
+                mma_commit_elect(smem_u32(&ctrl->empty[s]));
+                issued = js + 1;
             }
             if (!ok) break;
-            mma_commit_elect(smem_u32(&ctrl->empty[s]));
-            issued = js + 1;
-            st.advance(1, S);
+            if (first < seg_end)
+                mma_commit_elect(smem_u32(&ctrl->accfull[b]));
+            else
+                mbar_arrive_elect(smem_u32(&ctrl->accfull[b]));
+            seg_start = seg_end;
         }
     } else if (warp == kWarpEscape) {
         // ---------------------------------------------------------------- escape feeder (warp-wide)
@@ -490,14 +495,30 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             float *part = p.partials + (static_cast<size_t>(c) * 2 + slot) * M * kTileN;
             if (!dead) {
                 tc_fence_after();
-                const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * qw) << 16) + b * p.npad;
+                // the accumulator of each MMA issuer that had a record in this segment, added in
+                // a fixed order (issuer 0, then issuer 1)
+                const uint32_t lanes = static_cast<uint32_t>(32 * qw) << 16;
+                const bool has0 = ((seg_start - r0) & (RPS - 1)) == 0 || seg_end - seg_start >= 2;
+                const bool has1 = RPS == 2 && (((seg_start - r0) & 1) == 1 || seg_end - seg_start >= 2);
+                const uint32_t t0 = tmem + lanes + (0 * p.nacc + b) * p.npad;
+                const uint32_t t1 = tmem + lanes + (1 * p.nacc + b) * p.npad;
                 for (int m0 = 0; m0 < M; m0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(tbase + m0, v);
-                    tmem_wait_ld();
                     float f[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                    for (int i = 0; i < 16; ++i) f[i] = 0.f;
+                    uint32_t v[16];
+                    if (has0) {
+                        tmem_ld_32x32b_x16(t0 + m0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                    }
+                    if (has1) {
+                        tmem_ld_32x32b_x16(t1 + m0, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = has0 ? f[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
+                    }
                     if (mode == 2) {
                         float acc[16];
 #pragma unroll
@@ -612,11 +633,13 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         for (int js = (issued > S ? issued - S : 0); js < issued; ++js)  // cold path
             if (!mbar_wait_drain(smem_u32(&ctrl->full[js % S]), (js / S) & 1)) atomicOr(p.err, kErrDrain);
     }
+    if ((warp == kWarpMma || (warp == kWarpMma2 && RPS == 2)) && issued > 0) {
+        const int mq = (warp == kWarpMma) ? 0 : 1;
+        mma_commit_elect(smem_u32(&ctrl->done[mq]));  // same elected lane that issued the MMAs
+        if (!mbar_wait_drain(smem_u32(&ctrl->done[mq]), 0) && lane == 0) atomicOr(p.err, kErrDrain);
+    }
+    __syncthreads();  // both issuers drained before the tensor memory is released
     if (warp == kWarpMma) {
-        if (issued > 0) {
-            mma_commit_elect(smem_u32(&ctrl->done));  // same elected lane that issued the MMAs
-            if (!mbar_wait_drain(smem_u32(&ctrl->done), 0) && lane == 0) atomicOr(p.err, kErrDrain);
-        }
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -662,8 +685,9 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
     if (stages > kMaxStages) stages = kMaxStages;
     // tensor memory: nacc accumulators of npad columns, then 32 columns per record in flight
-    L->nacc = (2 * L->npad + 4 * L->rps * kACols <= kTmemCols) ? 2 : 1;
-    L->acc_cols = L->nacc * L->npad;
+    // one accumulator set per MMA issuer (rps issuers), double-buffered when it fits
+    L->nacc = (2 * L->rps * L->npad + 4 * L->rps * kACols <= kTmemCols) ? 2 : 1;
+    L->acc_cols = L->rps * L->nacc * L->npad;
     const int tmem_stages = (kTmemCols - L->acc_cols) / (L->rps * kACols);
     if (stages > tmem_stages) stages = tmem_stages;
     if (stages < 2) return W12_ERR_UNSUPPORTED_SHAPE;

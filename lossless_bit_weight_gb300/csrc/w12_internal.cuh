@@ -250,6 +250,18 @@ __device__ __forceinline__ void mma_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tm
         : "memory");
 }
 
+// The same, always accumulating into D (no predicate to compute).
+__device__ __forceinline__ void mma_bf16_ts_acc_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                      uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t.reg .pred A;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "setp.eq.u32 A, 1, 1;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, A;\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc)
+        : "memory");
+}
+
 // Commit from the elected lane (the lane that issued the MMAs it must track).
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(
