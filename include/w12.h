@@ -160,6 +160,23 @@ w12_status w12_lmhead_argmax(const w12_tensor *t, const uint16_t *x, int M, int3
                              float *val, float *gap, int qview, void *workspace,
                              size_t workspace_bytes, w12_stream_t stream);
 
+/* The paper has no counterpart of this call. It is w12_gemm for callers that cannot allocate
+ * device memory: a plug-in whose host framework owns all device memory and hands none out, or a
+ * serving loop that must not call cudaMalloc because cudaMalloc can synchronise the device. The
+ * workspace lives in a fixed array of about 8.5 MB inside the library; every GPU that loads the
+ * library holds it until the process exits. The caller still passes x and y (device pointers,
+ * laid out as for w12_gemm).
+ * Limits: 1 <= M <= 32, at most 4096 tiles of 128 output channels (N <= 524288) and at most 256
+ * thread blocks; larger problems return W12_ERR_UNSUPPORTED_SHAPE. The call allocates nothing:
+ * it clears the array's counters and error word with cudaMemsetAsync on `stream`, then launches
+ * the GEMM kernel. The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture. All calls on a device share the one array, so calls that overlap on the GPU race:
+ * order them (one stream, or events). A kernel that gives up one of its bounded waits is not
+ * reported by this call (use w12_gemm with w12_check where that matters). Asynchronous. */
+w12_status w12_gemm_noalloc(const w12_tensor *t, const uint16_t *x, int M, void *y, int y_dtype,
+                            w12_stream_t stream);
+
 /* SYNCHRONISES `stream`, then reports W12_ERR_TIMEOUT if a GEMM kernel that used this
  * workspace gave up one of its bounded waits (its outputs are then invalid and the workspace
  * must be zero-filled again); W12_OK otherwise. Clears the flag. */

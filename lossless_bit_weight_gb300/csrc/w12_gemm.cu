@@ -823,6 +823,69 @@ extern "C" w12_status w12_lmhead_argmax(const w12_tensor *t, const uint16_t *x, 
                     val, gap, workspace, workspace_bytes, stream);
 }
 
+// ------------------------------------------------------------------------------------------
+// w12_gemm_noalloc: the GEMM with its workspace in a fixed device array
+// ------------------------------------------------------------------------------------------
+//
+// Some callers cannot allocate device memory: a plug-in inside a host framework that owns all
+// device memory and hands none out, or a serving loop that must not call cudaMalloc because it
+// synchronises the device and can stall every stream. For them the workspace of the plain GEMM
+// (the split-K counters, the error word and the fp32 partial sums of split tiles) lives in the
+// file-scope array below instead. Every GPU that loads this library holds the array until the
+// process exits. Its size bounds the problems this entry point accepts:
+//   M <= kNoAllocMaxM rows, at most kNoAllocMaxTiles tiles of 128 output channels, and a grid of
+//   at most kNoAllocMaxGrid blocks (one per SM).
+constexpr int kNoAllocMaxM = 32;
+constexpr int kNoAllocMaxTiles = 4096;
+constexpr int kNoAllocMaxGrid = 256;
+constexpr size_t kNoAllocBytes =
+    256                                                          // error word
+    + sizeof(uint32_t) * kNoAllocMaxTiles                        // per-tile counters
+    + 256                                                        // completion counter
+    + sizeof(float) * kNoAllocMaxGrid * 2 * kNoAllocMaxM * w12::kTileN  // partial sums
+    + sizeof(float4) * kNoAllocMaxGrid * kNoAllocMaxM;           // per-block top-2 (argmax only)
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+// The array's device address, looked up once per device (with that device current). In host
+// code the symbol itself is only a host-side stand-in for the array, never a device address.
+constexpr int kNoAllocDevices = 64;
+void *g_noalloc_ptr[kNoAllocDevices];
+std::mutex g_noalloc_mu;
+
+w12_status noalloc_scratch(void **ptr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return W12_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocDevices) return W12_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return W12_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *ptr = g_noalloc_ptr[dev];
+    return W12_OK;
+}
+}  // namespace
+
+extern "C" w12_status w12_gemm_noalloc(const w12_tensor *t, const uint16_t *x, int M, void *y,
+                                       int y_dtype, w12_stream_t stream) {
+    using namespace w12;
+    W12_TRY(check_tensor(t));
+    if (M < 1) return W12_ERR_INVALID_ARG;
+    if (M > kNoAllocMaxM || t->n_tiles > kNoAllocMaxTiles) return W12_ERR_UNSUPPORTED_SHAPE;
+    Layout L{};
+    W12_TRY(plan(t, M, W12_OP_GEMM, &L));
+    if (L.grid > kNoAllocMaxGrid || L.ws_bytes > kNoAllocBytes) return W12_ERR_UNSUPPORTED_SHAPE;
+    void *ws = nullptr;
+    W12_TRY(noalloc_scratch(&ws));
+    // the counters and the error word must start at zero; the partial sums need no clearing
+    if (cudaMemsetAsync(ws, 0, L.off_part, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return W12_ERR_CUDA;
+    return run(t, x, M, W12_OP_GEMM, y, y_dtype, nullptr, nullptr, nullptr, ws, kNoAllocBytes, stream);
+}
+
 extern "C" w12_status w12_check(void *workspace, size_t workspace_bytes, w12_stream_t stream) {
     if (!workspace || workspace_bytes < 16) return W12_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             "w12_qview_gemm": ([T, P, i32, P, i32, P, sz, P], i32),
             "w12_lmhead_argmax": ([T, P, i32, P, P, P, i32, P, sz, P], i32),
             "w12_check": ([P, sz, P], i32),
+            "w12_gemm_noalloc": ([T, P, i32, P, i32, P], i32),
             "w12_gemm_config": ([T, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32)], i32),
         }
@@ -245,6 +246,18 @@ def lmhead_argmax(t: W12Tensor, x: torch.Tensor, qview: bool = False, stream=Non
     _check(lib().w12_lmhead_argmax(ctypes.byref(t.c), _ptr(x), M, _ptr(idx), _ptr(val), _ptr(gap),
                                    1 if qview else 0, _ptr(ws), nb, _stream(stream)), "w12_lmhead_argmax")
     return idx, val, gap
+
+
+def gemm_noalloc(t: W12Tensor, x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 y = x @ W^T through ``w12_gemm_noalloc``: no workspace is allocated (the library's
+    fixed device array serves as workspace; M <= 32)."""
+    _bits(x)
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty((M, t.N), dtype=torch.float32, device=x.device)
+    _check(lib().w12_gemm_noalloc(ctypes.byref(t.c), _ptr(x), M, _ptr(out), OUT_F32, _stream(stream)),
+           "w12_gemm_noalloc")
+    return out
 
 
 def check(t: W12Tensor, stream=None) -> None:
