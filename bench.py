@@ -101,6 +101,20 @@ def flush_l2(buf):
     buf.add_(1)
 
 
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The largest of every rank's x (the whole job ends when its slowest rank ends)."""
+    if dist is None:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank: float, world_size: int, elapsed_ms_max: float) -> float:
+    """Whole-job throughput: the bytes all ranks streamed over the slowest rank's time."""
+    return bytes_per_rank * world_size / (elapsed_ms_max * 1e-3) / 1e9
+
+
 def profile_traffic():
     """Per-launch DRAM bytes of the GEMM kernel from the committed ncu summary, if it still
     describes the current kernel source."""
@@ -124,42 +138,78 @@ def profile_traffic():
     return got["bytes"]
 
 
-def cpu_baseline(seconds_target: float = 12.0):
-    """The oracle, as it stands, on the host cores: decode a row sample of the projection from
-    its W12 encoding and multiply it with x for every M of the sweep (fp64)."""
-    import oracle
+class OracleSample:
+    """The oracle, as it stands, on a bounded sample of the projection workload: an n-channel
+    matrix drawn by the projection's recipe (K=5120), encoded once; one step decodes it from its
+    W12 encoding and multiplies it with x for every M of the sweep, in fp64 on the host cores."""
 
-    oracle.build()
-    n_s = 1024
-    w = synth.bits(synth.weights(n_s, K_HID, synth.PROJ, seed=synth.seed_for(1, 0)))
-    xs = {m: synth.bits(synth.activations(m, K_HID, seed=synth.seed_for(1, 100 + m))) for m in MS}
-    enc = oracle.encode(w)
+    def __init__(self, n_channels: int):
+        import oracle
+
+        oracle.build()
+        self.oracle = oracle
+        self.n = n_channels
+        w = synth.bits(synth.weights(n_channels, K_HID, synth.PROJ, seed=synth.seed_for(1, 0)))
+        self.xs = {m: synth.bits(synth.activations(m, K_HID, seed=synth.seed_for(1, 100 + m))) for m in MS}
+        self.enc = oracle.encode(w)
+
+    def step(self):
+        for m in MS:
+            self.oracle.gemm(self.xs[m], self.oracle.decode(self.enc))
+
+    @property
+    def bytes_per_step(self) -> float:
+        return 1.5 * self.n * K_HID * len(MS)
+
+    def describe(self, reps: int, el: float) -> str:
+        return (f"a {self.n}-channel matrix (K={K_HID}) drawn by the {N_MLP}-channel projection's recipe; "
+                f"decode + fp64 GEMM for each M in {list(MS)}; {reps} steps in {el:.1f} s; "
+                f"GB/s of 12-bit weight bytes")
+
+
+def cpu_baseline(seconds_target: float = 12.0):
+    """The oracle's throughput on about `seconds_target` seconds of host work."""
+    o = OracleSample(1024)
     t0 = time.perf_counter()
     reps = 0
     while True:
-        for m in MS:
-            wd = oracle.decode(enc)
-            oracle.gemm(xs[m], wd)
+        o.step()
         reps += 1
         el = time.perf_counter() - t0
         if el > seconds_target:
             break
-    w12_bytes = 1.5 * n_s * K_HID * len(MS) * reps
-    return {"value": w12_bytes / el / 1e9, "unit": "GB/s", "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{n_s} of {N_MLP} output channels (K={K_HID}), decode + fp64 GEMM for each M in "
-                      f"{list(MS)}, {reps} repetitions in {el:.1f} s; GB/s of 12-bit weight bytes"}
+    return {"value": o.bytes_per_step * reps / el / 1e9, "unit": "GB/s", "cores": o.oracle.threads(),
+            "kind": "oracle", "sample": o.describe(reps, el)}
 
 
-def run_reference(args):
+def run_reference(args, budget_s: float = 90.0):
+    """The reference arm: the oracle timed over `warmup` untimed and `steps` timed steps, each
+    step sized so that the whole run stays within about `budget_s` seconds (rank 0 only)."""
     ws, rank, _ = dist_env()
     if rank != 0:
         return
-    cb = cpu_baseline(seconds_target=max(5.0, 6.0 * args.steps / max(args.steps, 1)))
-    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": 0,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "K": K_HID, "N": N_MLP, "M": list(MS)},
-            "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+    probe = OracleSample(128)
+    t0 = time.perf_counter()
+    probe.step()
+    per_channel = (time.perf_counter() - t0) / probe.n
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    n = int(min(1024, max(16, per_step / max(per_channel, 1e-9))))
+    o = probe if n == probe.n else OracleSample(n)
+    for _ in range(args.warmup):
+        o.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        o.step()
+    el = time.perf_counter() - t0
+    value = o.bytes_per_step * args.steps / el / 1e9
+    cb = {"value": value, "unit": "GB/s", "cores": o.oracle.threads(), "kind": "oracle",
+          "sample": o.describe(args.steps, el)}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / max(args.steps, 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "K": K_HID, "N": N_MLP, "M": list(MS),
+                                            "sample_channels": o.n},
+            "cpu_baseline": cb, "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                                         "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
@@ -239,15 +289,11 @@ def main():
     elapsed_ms = start.elapsed_time(stop)
     for c in copies:
         w12.check(c)
-    if dist:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     per_m_us = {m: statistics.median(evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in ev_steps)
                 for j, m in enumerate(MS)}
     all_launch_us = [evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in ev_steps for j in range(len(MS))]
-    total_bytes = bytes_per_call * len(MS) * args.steps * ws
-    value = total_bytes / (elapsed_ms * 1e-3) / 1e9
+    value = job_gbs(bytes_per_call * len(MS) * args.steps, ws, elapsed_ms)
 
     # algorithmic bytes per launch (roofline): encoded weights + x + y, averaged over the sweep
     alg = [bytes_per_call + 2 * m * K_HID + 4 * m * N_MLP for m in MS]
@@ -262,6 +308,8 @@ def main():
     xd = {m: torch.empty_like(xs[m]) for m in MS}
     e2e_steps = max(3, min(args.steps, 400))
     torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for i in range(e2e_steps):
@@ -272,8 +320,8 @@ def main():
             yh[m].copy_(ys[m], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    e2e_value = bytes_per_call * len(MS) * e2e_steps / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    e2e_value = job_gbs(bytes_per_call * len(MS) * e2e_steps, ws, e2e_ms)
     h2d = sum(2 * m * K_HID for m in MS)
     d2h = sum(4 * m * N_MLP for m in MS)
 

@@ -5,20 +5,24 @@
 // result is deterministic; §6.3 and App. E: it is bound by weight bytes at 1-32 rows; §4.3: the
 // Q pass reads only the nested 8-bit view; §2.1: greedy verification takes the row argmax.
 //
-// Design on GB300 (one persistent block per SM, 16 warps). Work moves through a ring of
+// Design on GB300 (one persistent block per SM, 8 + 4*G warps with G = W12_DECODE_GROUPS decode
+// groups, 20 warps by default). Work moves through a ring of
 // `stages` slots; a slot holds `rps` consecutive records (2 for up to 64 rows, else 1) with
 // their activation tiles and escape entries in shared memory, plus one 32-column tensor-memory
 // buffer per record for the decoded weights. Each slot has three barriers: full (copies
 // landed), afull (decoded weights stored) and empty (the MMAs that read it completed).
 //   warp 0       producer: one bulk copy of the slot's records (contiguous in memory), one
 //                128B-swizzled TMA box of the activations' k-slice per record
-//   warp 1       allocates tensor memory; one thread issues tcgen05.mma (M=128 weight rows from
-//                tensor memory, N = rows of x padded to 16 from shared memory, K=16)
+//   warps 1, 3   warp 1 allocates tensor memory; one elected thread of each issues tcgen05.mma
+//                (M=128 weight rows from tensor memory, N = rows of x padded to 16 from shared
+//                memory, K=16): warp 1 for the first record of every slot, warp 3 for the second,
+//                each into an fp32 accumulator of its own
 //   warp 2       escape feeder: bulk-copies the slot's escape entries next to its records
 //   warps 4-7    epilogue: tensor memory -> registers; y, split-K partials or the row argmax
-//   warps 8-15   two decode groups: each thread owns one weight row of a record, turns its 64
-//                view bytes + 32 plane-B bytes into 32 bf16x2 words, patches its escapes and
-//                stores them into its tensor-memory lane (the MMA's A operand)
+//   warps 8-     G decode groups of 4 warps, taking slots in turn: each thread owns one weight
+//                row of a record, turns its 64 view bytes + 32 plane-B bytes into 32 bf16x2
+//                words, patches its escapes and stores them into its tensor-memory lane (the
+//                MMA's A operand)
 // The single-thread roles wait on a barrier once per slot, not once per record: a barrier
 // round trip costs a few hundred cycles, comparable to the HBM time of one 12 KB record.
 // Work split: the R = n_tiles*k_tiles records are cut into `grid` contiguous, equal ranges

@@ -1,0 +1,107 @@
+"""The C-ABI library without a GPU: it builds for sm_103a, loads, exports every function that
+include/w12.h declares, and answers its host-only calls (status names, shapes, scratch sizes,
+argument errors caught before any device work). No call here reaches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from lossless_bit_weight_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "w12.h")
+
+
+def declared_functions() -> list[str]:
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(w12_\w+)\s*\(", src, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def w12():
+    libbuild.build()
+    from lossless_bit_weight_gb300 import w12 as mod
+
+    mod.lib()
+    return mod
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("w12_encode_sizes", "w12_encode", "w12_decode", "w12_verify", "w12_gemm",
+              "w12_qview_gemm", "w12_lmhead_argmax", "w12_workspace_size", "w12_status_str"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(w12):
+    raw = ctypes.CDLL(w12.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+    # and the binding knows the signature of each
+    L = w12.lib()
+    for n in declared_functions():
+        assert getattr(L, n).restype is not None or n == "w12_status_str"
+
+
+def test_library_is_built_for_sm103a():
+    objs = [os.path.join(libbuild.BUILD, s.replace(".cu", ".o")) for s in libbuild.SOURCES]
+    assert all(os.path.exists(o) for o in objs)
+    assert "arch=compute_103a,code=sm_103a" in libbuild.ARCH
+
+
+def test_status_names(w12):
+    names = [w12.status_str(i) for i in range(8)]
+    assert names == ["W12_OK", "W12_ERR_INVALID_ARG", "W12_ERR_UNSUPPORTED_SHAPE", "W12_ERR_WORKSPACE",
+                     "W12_ERR_CUDA", "W12_ERR_MISMATCH", "W12_ERR_TIMEOUT", "W12_ERR_DEVICE"]
+    assert w12.status_str(99) == "W12_ERR_UNKNOWN"
+
+
+@pytest.mark.parametrize("N,K", [(512, 256), (17408, 5120), (151936, 5120), (1, 8), (130, 72)])
+def test_tensor_shape(w12, N, K):
+    t = w12.CTensor()
+    rb, bb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert w12.lib().w12_tensor_shape(N, K, ctypes.byref(t), ctypes.byref(rb), ctypes.byref(bb)) == w12.OK
+    nt, kt = -(-N // 128), -(-K // 64)
+    assert (t.N, t.K, t.n_tiles, t.k_tiles) == (N, K, nt, kt)
+    assert rb.value == nt * kt * 12288 and bb.value == nt * 128
+
+
+def test_shape_errors(w12):
+    L = w12.lib()
+    t = w12.CTensor()
+    rb, bb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.w12_tensor_shape(16, 12, ctypes.byref(t), ctypes.byref(rb), ctypes.byref(bb)) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_tensor_shape(0, 64, ctypes.byref(t), ctypes.byref(rb), ctypes.byref(bb)) == w12.ERR_INVALID_ARG
+    # 2^31 + 1 weights would overflow the 32-bit escape offsets
+    assert L.w12_tensor_shape(262145, 8192, ctypes.byref(t), None, None) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_tensor_shape(64, 64, None, None, None) == w12.ERR_INVALID_ARG
+
+
+def test_scratch_sizes(w12):
+    L = w12.lib()
+    nb = ctypes.c_size_t()
+    assert L.w12_encode_scratch_size(17408, 5120, ctypes.byref(nb)) == w12.OK
+    # at least the per-(channel, k tile) escape counts and the per-record counts
+    assert nb.value >= 4 * 17408 * 80
+    assert L.w12_encode_scratch_size(17408, 5120, None) == w12.ERR_INVALID_ARG
+    assert L.w12_verify_scratch_size(ctypes.byref(nb)) == w12.OK and nb.value == 32
+    assert L.w12_verify_scratch_size(None) == w12.ERR_INVALID_ARG
+
+
+def test_null_tensor_is_rejected_before_device_work(w12):
+    L = w12.lib()
+    nb = ctypes.c_size_t()
+    assert L.w12_decode(None, None, None) == w12.ERR_INVALID_ARG
+    assert L.w12_workspace_size(None, 1, 0, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    assert L.w12_gemm(None, None, 1, None, 0, None, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_gemm_noalloc(None, None, 1, None, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_encode(None, 64, 64, None, 0, None, None) == w12.ERR_INVALID_ARG
+
+
+def test_binding_fails_loudly_without_the_library(w12, monkeypatch):
+    monkeypatch.setattr(w12, "_lib", None)
+    monkeypatch.setattr(w12, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libw12.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        w12.lib()
