@@ -57,6 +57,7 @@ enum {
 };
 
 enum { W12_OUT_F32 = 0, W12_OUT_BF16 = 1 };          /* y element type */
+enum { W12_LAUNCH_OVERLAP = 1 };                     /* w12_gemm_ex flags */
 enum { W12_OP_GEMM = 0, W12_OP_QVIEW_GEMM = 1, W12_OP_ARGMAX = 2, W12_OP_QVIEW_ARGMAX = 3 };
 
 /*
@@ -159,6 +160,27 @@ w12_status w12_qview_gemm(const w12_tensor *t, const uint16_t *x, int M, void *y
 w12_status w12_lmhead_argmax(const w12_tensor *t, const uint16_t *x, int M, int32_t *idx,
                              float *val, float *gap, int qview, void *workspace,
                              size_t workspace_bytes, w12_stream_t stream);
+
+/* The GEMM family with launch options (the paper has no counterpart of the options).
+ * op is one of W12_OP_*. The GEMM ops write y (y_dtype) and take idx, val and gap as NULL. The
+ * argmax ops write idx, val and gap and take y as NULL. Any other argument combination returns
+ * W12_ERR_INVALID_ARG.
+ * flags = 0 behaves exactly as w12_gemm, w12_qview_gemm or w12_lmhead_argmax.
+ * flags = W12_LAUNCH_OVERLAP uses a programmatic dependent launch: the kernel may start while the
+ * kernel before it on `stream` is still finishing, and meanwhile fetches and decodes its
+ * weights. It reads x, reads and writes the workspace, and writes its outputs only after that
+ * kernel has completed and its memory is visible.
+ * Contract for the overlap: nothing the preceding kernel does may write t's buffers (records,
+ * base_exp, rec_esc_off, rec_esc). They must already hold their final contents when the
+ * preceding kernel starts, as they do for weights loaded once and reused.
+ * This launch also lets the next kernel on the stream start early. That next kernel must itself
+ * wait for this one before using its results, as kernels launched with this flag do.
+ * The kernel's bounded waits give up after about a second, so the preceding kernel must not run
+ * much longer than that after this launch begins.
+ * Asynchronous. */
+w12_status w12_gemm_ex(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, int y_dtype,
+                       int32_t *idx, float *val, float *gap, unsigned flags, void *workspace,
+                       size_t workspace_bytes, w12_stream_t stream);
 
 /* The paper has no counterpart of this call. It is w12_gemm for callers that cannot allocate
  * device memory: a plug-in whose host framework owns all device memory and hands none out, or a

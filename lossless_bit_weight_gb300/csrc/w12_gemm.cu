@@ -58,9 +58,13 @@ constexpr int kTmemCols = 512;
 constexpr int kSmemLimit = 232448;       // opt-in maximum per block
 constexpr int kSmemFloor = 120 * 1024;   // keeps one block per SM
 constexpr int kEpiBar = 1;               // named barrier of the 128 epilogue threads
+// Whole tiles per block are used when the busiest block then has at most this factor of the
+// average work: up to 15% imbalance costs less than splitting tiles and summing the partials
+// at the end (measured on the 136-tile MLP projection on 152 SMs).
+constexpr double kTileSplitSlack = 1.15;
 
 struct Ctrl {
-    uint64_t full[kMaxStages], afull[kMaxStages], empty[kMaxStages];
+    uint64_t full[kMaxStages], afull[kMaxStages], empty[kMaxStages], xfull[kMaxStages];
     uint64_t accfull[2], accempty[2];
     uint64_t done[2];
     uint32_t esc_cnt[kMaxStages];    // entries of the slot (bit 31: too many, read from global)
@@ -71,7 +75,7 @@ struct Ctrl {
     int fix;          // block-wide flag of the final argmax merge
     int mode[2];      // how a split tile ends (by segment parity)
     int last[2];      // this block published last and sums the tile (by segment parity)
-    int pad_;
+    int pre;          // the last segment's other block had published before its MMAs completed
     float4 wtop[4][kMaxM];  // per-warp top-2 of the current tile (argmax)
     float4 ctop[kMaxM];     // running top-2 of this block (argmax)
 };
@@ -82,8 +86,9 @@ struct Params {
     const uint32_t *rec_esc_off;
     const uint32_t *rec_esc;
     int N, K, M, n_tiles, k_tiles, npad, stages, rps, nacc, acc_cols, grid;
+    int unit;  // records per unit of the work split: 1 (stream-K) or k_tiles (whole tiles)
     uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
-    int64_t R;
+    int R;  // records: n_tiles * k_tiles (< 2^22)
     void *y;
     int y_bf16;
     float *partials;     // [grid][2][M][128]
@@ -96,10 +101,14 @@ struct Params {
     int *err;
 };
 
-__device__ __forceinline__ int64_t range_start(int64_t c, int64_t R, int64_t G) { return c * R / G; }
+// Record counts fit in 32 bits with room to spare (R <= 2^21 since N*K <= 2^31, and G <= 256),
+// so block ranges use 32-bit arithmetic: a 64-bit division is a long software routine.
+__device__ __forceinline__ int range_start(int c, int R, int G) {
+    return static_cast<int>(static_cast<uint32_t>(c) * static_cast<uint32_t>(R) / static_cast<uint32_t>(G));
+}
 // the block whose range holds record i
-__device__ __forceinline__ int64_t owner_of(int64_t i, int64_t R, int64_t G) {
-    return ((i + 1) * G + R - 1) / R - 1;
+__device__ __forceinline__ int owner_of(int i, int R, int G) {
+    return static_cast<int>((static_cast<uint32_t>(i + 1) * G + R - 1) / static_cast<uint32_t>(R)) - 1;
 }
 
 // Position in a ring of `size` slots: index and the parity of its phase. Advanced
@@ -145,6 +154,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the next grid on the stream may start as soon as SMs free up; it waits for this grid's
+    // completion itself before it reads activations or its workspace
+    grid_launch_dependents();
 
     const int S = p.stages, RPS = p.rps;
     const int xbytes = p.npad * 128;
@@ -157,45 +169,61 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
     auto stage_esc = [&](int s) { return smem + s * sbytes + RPS * (xbytes + rbytes); };
 
     const int c = blockIdx.x;
-    const int64_t R = p.R, G = p.grid, kt64 = p.k_tiles;
-    const int64_t r0 = range_start(c, R, G), r1 = range_start(c + 1, R, G);
-    const int nrec = static_cast<int>(r1 - r0);
+    const int R = p.R, G = p.grid, KT = p.k_tiles, U = p.unit;
+    // block cc's range starts at record block_start(cc); owner(i) is the block holding record i
+    auto block_start = [&](int cc) { return U * range_start(cc, R / U, G); };
+    auto owner = [&](int i) { return owner_of(i / U, R / U, G); };
+    const int r0 = block_start(c), r1 = block_start(c + 1);
+    const int nrec = r1 - r0;
     const int nst = (nrec + RPS - 1) / RPS;  // slots this block fills
 
-    int issued = 0;  // producer: slots handed to the copy engine; mma: slots issued
+    int issued = 0;   // producer: slots whose records were handed to the copy engine; mma: slots issued
+    int xissued = 0;  // producer: slots whose activation tiles were handed to the copy engine
     // producer state: its slot ring, the k tile of its next record, the next record's bytes
     Ring pst;
     int pkt = 0;
     const uint8_t *psrc = nullptr;
-    auto produce = [&](int js) {  // fill ring slot pst.idx with the records of slot js
+    // The records of a slot (full barrier, with the escape entries) and its activation tiles
+    // (xfull barrier) arrive separately: records are weights, which no earlier kernel writes,
+    // so they may be fetched and decoded before the previous grid on the stream has finished;
+    // x and the workspace may not be touched before that (grid_dependency_wait).
+    auto produce_rec = [&](int js) {  // ring slot pst.idx gets the records of slot js
         const int s = pst.idx;
         const int nr = min(RPS, nrec - js * RPS);
         const uint32_t fb = smem_u32(&ctrl->full[s]);
-        mbar_arrive_expect_tx_elect(fb, nr * (rbytes + xbytes));
+        mbar_arrive_expect_tx_elect(fb, nr * rbytes);
         if (kQView) {  // the 8-bit views only: the B planes between them stay in memory
             for (int q = 0; q < nr; ++q)
                 bulk_g2s_elect(smem_u32(stage_rec(s, q)), psrc + q * kRecordBytes, rbytes, fb);
         } else {       // consecutive records are contiguous: one copy
             bulk_g2s_elect(smem_u32(stage_rec(s, 0)), psrc, nr * rbytes, fb);
         }
-        for (int q = 0; q < nr; ++q) {
-            tma_2d_g2s_elect(smem_u32(stage_x(s, q)), &xmap, pkt * kTileK, 0, fb);
-            if (++pkt == p.k_tiles) pkt = 0;
-        }
         psrc += nr * kRecordBytes;
         issued = js + 1;
         pst.advance(1, S);
     };
+    auto produce_x = [&](int js, int s) {  // ring slot s gets the activation tiles of slot js
+        const int nr = min(RPS, nrec - js * RPS);
+        const uint32_t xb = smem_u32(&ctrl->xfull[s]);
+        mbar_arrive_expect_tx_elect(xb, nr * xbytes);
+        for (int q = 0; q < nr; ++q) {
+            tma_2d_g2s_elect(smem_u32(stage_x(s, q)), &xmap, pkt * kTileK, 0, xb);
+            if (++pkt == p.k_tiles) pkt = 0;
+        }
+        xissued = js + 1;
+    };
 
     if (warp == kWarpProducer) {
-        // the producer initialises the barriers and starts the first copies right away: every
-        // slot is free at start, so the HBM latency of the first records overlaps the rest of
-        // the block's set-up
+        // the producer initialises the barriers and starts the first slot's copies before the
+        // block-wide barrier, so their HBM latency overlaps the rest of the set-up; the other
+        // slots follow right after the barrier (issuing all of them here would hold every
+        // other warp at the barrier while the copy engine takes them in)
         if (lane == 0) {
             for (int s = 0; s < S; ++s) {
                 mbar_init(smem_u32(&ctrl->full[s]), kQView ? 1 : 2);
                 mbar_init(smem_u32(&ctrl->afull[s]), 128);
                 mbar_init(smem_u32(&ctrl->empty[s]), RPS);  // one commit per MMA issuer
+                mbar_init(smem_u32(&ctrl->xfull[s]), 1);
             }
             for (int b = 0; b < 2; ++b) {
                 mbar_init(smem_u32(&ctrl->accfull[b]), RPS);
@@ -209,9 +237,20 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             prefetch_tensormap(&xmap);
         }
         __syncwarp();
-        pkt = static_cast<int>(r0 % kt64);
-        psrc = p.records + r0 * kRecordBytes;
-        for (int js = 0; js < min(S, nst); ++js) produce(js);
+        pkt = r0 % KT;
+        psrc = p.records + static_cast<size_t>(r0) * kRecordBytes;
+        if (nst > 0) produce_rec(0);
+    }
+    // escape feeder: lane l holds rec_esc_off[r0 + base + l] (cur) and [r0 + base + 32 + l]
+    // (nxt); the first loads start here so their latency also overlaps the set-up
+    auto esc_load = [&](int b0) -> uint32_t {
+        const int i = r0 + b0 + lane;
+        return (i <= R) ? __ldg(p.rec_esc_off + i) : 0u;
+    };
+    uint32_t esc_cur = 0, esc_nxt = 0;
+    if (!kQView && warp == kWarpEscape) {
+        esc_cur = esc_load(0);
+        esc_nxt = esc_load(32);
     }
     if (kArgmax) {
         for (int m = threadIdx.x; m < p.M; m += kThreads)
@@ -229,10 +268,16 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
 
     if (warp == kWarpProducer) {
         // ---------------------------------------------------------------- producer (warp-wide)
-        for (int js = min(S, nst); js < nst; ++js) {
-            const bool ok = mbar_wait(smem_u32(&ctrl->empty[pst.idx]), pst.phase ^ 1, abort, p.err, kErrProducer);
+        const int n0 = min(S, nst);  // the first S slots start out free
+        for (int js = 1; js < n0; ++js) produce_rec(js);
+        grid_dependency_wait();  // x may be the previous grid's output
+        for (int js = 0; js < n0; ++js) produce_x(js, js);
+        for (int js = n0; js < nst; ++js) {
+            const int s = pst.idx;
+            const bool ok = mbar_wait(smem_u32(&ctrl->empty[s]), pst.phase ^ 1, abort, p.err, kErrProducer);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            produce(js);
+            produce_rec(js);
+            produce_x(js, s);
         }
     } else if (warp == kWarpMma || (warp == kWarpMma2 && RPS == 2)) {
         // ---------------------------------------------------------------- MMA issuers (warp-wide)
@@ -247,23 +292,24 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         int js_next = 0;  // ring position of st: the slot of this issuer's next record
         int jseg = 0;
         bool ok = true;
-        for (int64_t seg_start = r0; ok && seg_start < r1; ++jseg) {
-            const int64_t seg_end = min(r1, (seg_start / kt64 + 1) * kt64);
+        for (int seg_start = r0; ok && seg_start < r1; ++jseg) {
+            const int seg_end = min(r1, (seg_start / KT + 1) * KT);
             const int b = (p.nacc == 2) ? (jseg & 1) : 0;
             const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
             // this issuer's records r in [seg_start, seg_end) have (r - r0) % RPS == mq
-            int64_t r = seg_start + ((seg_start - r0 - mq) & (RPS - 1));
-            const int64_t first = r;
+            int r = seg_start + ((seg_start - r0 - mq) & (RPS - 1));
+            const int first = r;
             const bool oka = mbar_wait(smem_u32(&ctrl->accempty[b]), phb ^ 1, abort, p.err, kErrMma);
             if (!__all_sync(0xFFFFFFFFu, oka)) break;
             tc_fence_after();
             const uint32_t d = tmem + (mq * p.nacc + b) * p.npad;
             for (; r < seg_end; r += RPS) {
-                const int js = static_cast<int>((r - r0) / RPS);
+                const int js = (r - r0) >> (RPS - 1);  // RPS is 1 or 2
                 st.advance(js - js_next, S);
                 js_next = js;
                 const int s = st.idx;
-                const bool okw = mbar_wait(smem_u32(&ctrl->afull[s]), st.phase, abort, p.err, kErrMma);
+                const bool okw = mbar_wait(smem_u32(&ctrl->afull[s]), st.phase, abort, p.err, kErrMma) &&
+                                 mbar_wait(smem_u32(&ctrl->xfull[s]), st.phase, abort, p.err, kErrMma);
                 if (!__all_sync(0xFFFFFFFFu, okw)) {
                     ok = false;
                     break;
@@ -289,13 +335,8 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
     } else if (warp == kWarpEscape) {
         // ---------------------------------------------------------------- escape feeder (warp-wide)
         if (!kQView) {
-            // lane l holds rec_esc_off[r0 + base + l] (cur) and [r0 + base + 32 + l] (nxt)
             int base = 0;
-            auto load = [&](int b0) -> uint32_t {
-                const int64_t i = r0 + b0 + lane;
-                return (i <= R) ? __ldg(p.rec_esc_off + i) : 0u;
-            };
-            uint32_t cur = load(0), nxt = load(32);
+            uint32_t cur = esc_cur, nxt = esc_nxt;
             auto off_of = [&](int i) -> uint32_t {  // requires i - base in [0, 64)
                 const int dd = i - base;
                 const uint32_t a = __shfl_sync(0xFFFFFFFFu, cur, dd & 31);
@@ -309,7 +350,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 if (first >= base + 32) {
                     base += 32;
                     cur = nxt;
-                    nxt = load(base + 32);
+                    nxt = esc_load(base + 32);
                 }
                 const uint32_t lo = off_of(first);
                 const uint32_t mid = off_of(first + 1);
@@ -342,9 +383,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         const int qw = warp & 3;
         const int nl = 32 * qw + lane;
         const uint32_t m3 = p.m3, m15 = p.m15;
-        int64_t cur_tile = -1;
+        int cur_tile = -1;
         uint32_t cur_base2 = 0;
-        auto base2_for = [&](int64_t tile) -> uint32_t {
+        auto base2_for = [&](int tile) -> uint32_t {
             if (tile != cur_tile) {
                 cur_tile = tile;
                 cur_base2 = base2_of(__ldg(p.base_exp + tile * kTileN + nl));
@@ -403,11 +444,22 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         int js = g;
         Ring st;
         st.advance(js, S);
-        int64_t tile = (r0 + static_cast<int64_t>(js) * RPS) / kt64;  // tile and k tile of the
-        int kt = static_cast<int>((r0 + static_cast<int64_t>(js) * RPS) % kt64);  // slot's first record
+        int tile = (r0 + js * RPS) / KT;  // tile and k tile of the slot's first record
+        int kt = (r0 + js * RPS) % KT;
         uint32_t wa[32], wb[32];
+        // A parity wait cannot tell phase u from phase u - 2. When G divides S, a slot's uses all
+        // fall to one group, which has seen use u - 1 complete before it waits for use u. When it
+        // does not, the previous use belongs to another group and its copies may land after this
+        // group's last slot: wait until that use was decoded (afull phase u - 1; afull cannot
+        // lag further, since the in-order MMA issuer consumed use u - 2 before the producer
+        // issued anything this group has decoded) so the full wait below sees phase u itself.
+        const bool shared_slots = (S % kDecGroups) != 0;
         for (; js < nst; js += kDecGroups) {
             const int s = st.idx;
+            if (shared_slots) {
+                const bool ok_prev = mbar_wait(smem_u32(&ctrl->afull[s]), st.phase ^ 1, abort, p.err, kErrDecode);
+                if (!__all_sync(0xFFFFFFFFu, ok_prev)) break;
+            }
             const bool ok_full = mbar_wait(smem_u32(&ctrl->full[s]), st.phase, abort, p.err, kErrDecode);
             if (!__all_sync(0xFFFFFFFFu, ok_full)) break;
             const int nr = min(RPS, nrec - js * RPS);
@@ -417,7 +469,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             tc_fence_after();
             tmem_st_32x32b_x32(a_slot(s, 0) + (static_cast<uint32_t>(32 * qw) << 16), wa);
             if (nr == 2) {
-                const int64_t tile1 = (kt + 1 == p.k_tiles) ? tile + 1 : tile;
+                const int tile1 = (kt + 1 == p.k_tiles) ? tile + 1 : tile;
                 decode_record(s, 1, base2_for(tile1), wb);
                 tmem_st_32x32b_x32(a_slot(s, 1) + (static_cast<uint32_t>(32 * qw) << 16), wb);
             }
@@ -448,8 +500,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         const int et = threadIdx.x - kWarpEpi0 * 32;  // 0..127
         const int M = p.M;
         bool dead = false;
+        grid_dependency_wait();  // the workspace and y may still be in use by the previous grid
         int jseg = 0;
-        int64_t r = r0;
+        int r = r0;
         auto store_y = [&](int m, int n, float f) {
             if (p.y_bf16)
                 reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(f);
@@ -467,29 +520,47 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 store_y(m, n, f);
             }
         };
-        auto partial_of = [&](int64_t cc, int64_t tile, int m) {  // block cc's partial of tile
-            const int sl = (range_start(cc, R, G) / kt64 == tile) ? 0 : 1;
+        auto partial_of = [&](int cc, int tile, int m) {  // block cc's partial of tile
+            const int sl = (block_start(cc) / KT == tile) ? 0 : 1;
             return p.partials + ((static_cast<size_t>(cc) * 2 + sl) * M + m) * kTileN + nl;
         };
         while (r < r1) {
-            const int64_t tile = r / kt64;
-            const int64_t seg_start = r, seg_end = min(r1, (tile + 1) * kt64);
+            const int tile = r / KT;
+            const int seg_start = r, seg_end = min(r1, (tile + 1) * KT);
             r = seg_end;
-            const bool full = seg_start == tile * kt64 && seg_end == (tile + 1) * kt64;
+            const bool full = seg_start == tile * KT && seg_end == (tile + 1) * KT;
             const int par = jseg & 1;
             const int slot = (jseg == 0) ? 0 : 1;
             const int b = (p.nacc == 2) ? (jseg & 1) : 0;
             const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
             ++jseg;
             const int n = static_cast<int>(tile) * kTileN + nl;
+            const int c_lo = full ? c : owner(tile * KT);
+            const int c_hi = full ? c : owner((tile + 1) * KT - 1);
+            // 0: whole tile here; 1: publish a partial; 2: sum here from the published partials
+            int mode = 0;
+            // A block's last segment ends the kernel for it. When its tile has one other block
+            // and that block has already published (the usual case: the other block had the
+            // tile at the start of its range), fetch that partial now, while this segment's MMAs
+            // still run, instead of after them. Rows <= 32 only: the partial lives in registers.
+            float pf[32];
+            const bool pre_ok = !full && !dead && seg_end == r1 && c_hi - c_lo == 1 && M <= 32;
+            if (pre_ok) {  // once per block: ctrl->pre is written only here
+                if (et == 0) ctrl->pre = (ld_acquire_gpu(&p.tile_cnt[tile]) == 1u) ? 2 : 0;
+                named_bar_sync(kEpiBar, 128);
+                mode = ctrl->pre;
+                if (mode == 2) {
+                    fence_acq_rel_gpu();
+                    const float *src = partial_of(c == c_lo ? c_hi : c_lo, tile, 0);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) pf[i] = (i < M) ? __ldcg(src + static_cast<size_t>(i) * kTileN) : 0.f;
+                }
+            }
             bool ok = !dead && mbar_wait(smem_u32(&ctrl->accfull[b]), phb, abort, p.err, kErrEpilogue);
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) dead = true;
-            const int64_t c_lo = full ? c : owner_of(tile * kt64, R, G);
-            const int64_t c_hi = full ? c : owner_of((tile + 1) * kt64 - 1, R, G);
-            // 0: whole tile here; 1: publish a partial; 2: sum here from the published partials
-            int mode = 0;
-            if (!full) {
+            const bool pre = mode == 2;  // the other block's partial is in pf
+            if (!full && mode == 0) {
                 if (et == 0)
                     ctrl->mode[par] = (ld_acquire_gpu(&p.tile_cnt[tile]) == static_cast<uint32_t>(c_hi - c_lo)) ? 2 : 1;
                 named_bar_sync(kEpiBar, 128);
@@ -506,7 +577,36 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 const bool has1 = RPS == 2 && (((seg_start - r0) & 1) == 1 || seg_end - seg_start >= 2);
                 const uint32_t t0 = tmem + lanes + (0 * p.nacc + b) * p.npad;
                 const uint32_t t1 = tmem + lanes + (1 * p.nacc + b) * p.npad;
-                for (int m0 = 0; m0 < M; m0 += 16) {
+                if (pre) {
+                    // two blocks: own + other is the same sum, bit for bit, in either order
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int m0 = 16 * h;
+                        if (m0 >= M) break;
+                        float f[16];
+                        uint32_t v[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[i] = 0.f;
+                        if (has0) {
+                            tmem_ld_32x32b_x16(t0 + m0, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                        }
+                        if (has1) {
+                            tmem_ld_32x32b_x16(t1 + m0, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) f[i] = has0 ? f[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            if (m0 + i >= M) break;
+                            emit(m0 + i, n, f[i] + pf[16 * h + i]);
+                        }
+                    }
+                }
+                for (int m0 = 0; !pre && m0 < M; m0 += 16) {
                     float f[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) f[i] = 0.f;
@@ -527,7 +627,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                         float acc[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-                        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+                        for (int cc = c_lo; cc <= c_hi; ++cc) {
                             if (cc == c) {
 #pragma unroll
                                 for (int i = 0; i < 16; ++i) acc[i] += f[i];
@@ -571,7 +671,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                         float f[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) f[i] = 0.f;
-                        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+                        for (int cc = c_lo; cc <= c_hi; ++cc) {
                             const float *src = partial_of(cc, tile, m0);
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
@@ -617,7 +717,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 for (int m = et; m < M; m += 128) {
                     float v1 = -INFINITY, v2 = -INFINITY;
                     int i1 = 0x7FFFFFFF;
-                    for (int64_t cc = 0; cc < G; ++cc) {
+                    for (int cc = 0; cc < G; ++cc) {
                         const float4 o = __ldcg(p.cta_top + static_cast<size_t>(cc) * M + m);
                         top2_merge(v1, i1, v2, o.x, __float_as_int(o.y), o.z);
                     }
@@ -636,6 +736,8 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         // let copies still in flight land before the block's shared memory is released
         for (int js = (issued > S ? issued - S : 0); js < issued; ++js)  // cold path
             if (!mbar_wait_drain(smem_u32(&ctrl->full[js % S]), (js / S) & 1)) atomicOr(p.err, kErrDrain);
+        for (int js = (xissued > S ? xissued - S : 0); js < xissued; ++js)
+            if (!mbar_wait_drain(smem_u32(&ctrl->xfull[js % S]), (js / S) & 1)) atomicOr(p.err, kErrDrain);
     }
     if ((warp == kWarpMma || (warp == kWarpMma2 && RPS == 2)) && issued > 0) {
         const int mq = (warp == kWarpMma) ? 0 : 1;
@@ -669,7 +771,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 struct Layout {
-    int npad, stages, rps, nacc, acc_cols, grid, smem;
+    int npad, stages, rps, nacc, acc_cols, grid, unit, smem;
     int64_t R;
     size_t ws_bytes, off_err, off_tile, off_done, off_part, off_top;
 };
@@ -694,11 +796,24 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     L->acc_cols = L->rps * L->nacc * L->npad;
     const int tmem_stages = (kTmemCols - L->acc_cols) / (L->rps * kACols);
     if (stages > tmem_stages) stages = tmem_stages;
-    if (stages < 2) return W12_ERR_UNSUPPORTED_SHAPE;
+    // every decode group needs a slot of its own (the slot-ordering argument in the decode loop)
+    if (stages < 2 || stages < kDecGroups) return W12_ERR_UNSUPPORTED_SHAPE;
     L->stages = stages;
     L->smem = 1024 + stages * sbytes + ctrl;
     if (L->smem < kSmemFloor) L->smem = kSmemFloor;
-    L->grid = static_cast<int>(L->R < sms ? L->R : sms);
+    // Work split. Whole tiles per block when that balances within kTileSplitSlack: no tile is
+    // then shared, so no partial sums and no cross-block fix-up at the end of the launch.
+    // Otherwise stream-K: equal contiguous record ranges over one block per SM.
+    const int T = t->n_tiles;
+    const int per = (T + sms - 1) / sms;      // tiles of the busiest block
+    const int gt = (T + per - 1) / per;       // blocks needed at that load
+    if (static_cast<double>(per) * sms <= kTileSplitSlack * T) {
+        L->grid = gt;
+        L->unit = t->k_tiles;
+    } else {
+        L->grid = static_cast<int>(L->R < sms ? L->R : sms);
+        L->unit = 1;
+    }
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -715,17 +830,30 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
 }
 
 template <bool kQ, bool kA>
-w12_status launch_variant(const CUtensorMap &map, const Params &p, const Layout &L, cudaStream_t st) {
+w12_status launch_variant(const CUtensorMap &map, const Params &p, const Layout &L, bool overlap,
+                          cudaStream_t st) {
     auto kern = w12_gemm_kernel<kQ, kA>;
     W12_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem));
-    kern<<<L.grid, kThreads, L.smem, st>>>(map, p);
-    W12_CUDA(cudaGetLastError());
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(L.smem);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = overlap ? 1 : 0;
+    W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, p));
     return W12_OK;
 }
 
 w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, int y_dtype,
-               int32_t *idx, float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream) {
+               int32_t *idx, float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream,
+               unsigned flags = 0) {
     W12_TRY(check_tensor(t));
+    if (flags & ~static_cast<unsigned>(W12_LAUNCH_OVERLAP)) return W12_ERR_INVALID_ARG;
+    const bool overlap = (flags & W12_LAUNCH_OVERLAP) != 0;
     if (!x || !aligned16(x) || !ws) return W12_ERR_INVALID_ARG;
     Layout L{};
     W12_TRY(plan(t, M, op, &L));
@@ -766,7 +894,8 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.nacc = L.nacc;
     p.acc_cols = L.acc_cols;
     p.grid = L.grid;
-    p.R = L.R;
+    p.unit = L.unit;
+    p.R = static_cast<int>(L.R);
     p.y = y;
     p.y_bf16 = (y_dtype == W12_OUT_BF16);
     p.err = reinterpret_cast<int *>(w + L.off_err);
@@ -778,8 +907,11 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.val = val;
     p.gap = gap;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (q) return argmax ? launch_variant<true, true>(map, p, L, st) : launch_variant<true, false>(map, p, L, st);
-    return argmax ? launch_variant<false, true>(map, p, L, st) : launch_variant<false, false>(map, p, L, st);
+    if (q)
+        return argmax ? launch_variant<true, true>(map, p, L, overlap, st)
+                      : launch_variant<true, false>(map, p, L, overlap, st);
+    return argmax ? launch_variant<false, true>(map, p, L, overlap, st)
+                  : launch_variant<false, false>(map, p, L, overlap, st);
 }
 
 }  // namespace
@@ -825,6 +957,16 @@ extern "C" w12_status w12_lmhead_argmax(const w12_tensor *t, const uint16_t *x, 
                                         size_t workspace_bytes, w12_stream_t stream) {
     return w12::run(t, x, M, qview ? W12_OP_QVIEW_ARGMAX : W12_OP_ARGMAX, nullptr, W12_OUT_F32, idx,
                     val, gap, workspace, workspace_bytes, stream);
+}
+
+extern "C" w12_status w12_gemm_ex(const w12_tensor *t, const uint16_t *x, int M, int op, void *y,
+                                  int y_dtype, int32_t *idx, float *val, float *gap, unsigned flags,
+                                  void *workspace, size_t workspace_bytes, w12_stream_t stream) {
+    if (op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) return W12_ERR_INVALID_ARG;
+    const bool argmax = (op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX);
+    if (argmax && y) return W12_ERR_INVALID_ARG;
+    if (!argmax && (idx || val || gap)) return W12_ERR_INVALID_ARG;
+    return w12::run(t, x, M, op, y, y_dtype, idx, val, gap, workspace, workspace_bytes, stream, flags);
 }
 
 // ------------------------------------------------------------------------------------------

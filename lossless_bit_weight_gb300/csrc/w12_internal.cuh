@@ -163,6 +163,13 @@ __device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap *map,
         : "memory");
 }
 
+// Programmatic dependent launch (sm_90+). wait: block until the grids this launch depends on
+// have completed and their memory is visible (returns at once when there are none).
+// launch_dependents: let the grid launched after this one on the stream begin; it still waits
+// for this grid's completion before reading anything this grid produced.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }

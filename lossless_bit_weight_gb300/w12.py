@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libw12.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_MISMATCH, ERR_TIMEOUT, \
     ERR_DEVICE = range(8)
 OUT_F32, OUT_BF16 = 0, 1
+LAUNCH_OVERLAP = 1
 OP_GEMM, OP_QVIEW_GEMM, OP_ARGMAX, OP_QVIEW_ARGMAX = range(4)
 TILE_N, TILE_K, RECORD_BYTES, VIEW_BYTES, MAX_M = 128, 64, 12288, 8192, 256
 
@@ -69,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "w12_lmhead_argmax": ([T, P, i32, P, P, P, i32, P, sz, P], i32),
             "w12_check": ([P, sz, P], i32),
             "w12_gemm_noalloc": ([T, P, i32, P, i32, P], i32),
+            "w12_gemm_ex": ([T, P, i32, i32, P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
             "w12_gemm_config": ([T, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32)], i32),
         }
@@ -219,8 +221,12 @@ def verify(t: W12Tensor, w_ref: torch.Tensor, stream=None) -> int:
 
 
 def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = False,
-         out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """y = x @ W^T over the exact weights (or the 8-bit view when ``qview``)."""
+         out: torch.Tensor | None = None, stream=None, overlap: bool = False) -> torch.Tensor:
+    """y = x @ W^T over the exact weights (or the 8-bit view when ``qview``).
+
+    ``overlap`` launches with ``W12_LAUNCH_OVERLAP`` (``w12_gemm_ex``): the kernel may start, and
+    fetch and decode its weights, while the previous kernel on the stream finishes; t's buffers
+    must not be written by that kernel."""
     _bits(x)
     M = x.shape[0]
     if x.shape[1] != t.K:
@@ -228,21 +234,31 @@ def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = F
     ydt = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
     if out is None:
         out = torch.empty((M, t.N), dtype=out_dtype, device=x.device)
-    ws, nb = t.workspace(M, OP_QVIEW_GEMM if qview else OP_GEMM)
+    op = OP_QVIEW_GEMM if qview else OP_GEMM
+    ws, nb = t.workspace(M, op)
+    if overlap:
+        _check(lib().w12_gemm_ex(ctypes.byref(t.c), _ptr(x), M, op, _ptr(out), ydt, None, None, None,
+                                 LAUNCH_OVERLAP, _ptr(ws), nb, _stream(stream)), "w12_gemm_ex")
+        return out
     fn = lib().w12_qview_gemm if qview else lib().w12_gemm
     _check(fn(ctypes.byref(t.c), _ptr(x), M, _ptr(out), ydt, _ptr(ws), nb, _stream(stream)),
            "w12_qview_gemm" if qview else "w12_gemm")
     return out
 
 
-def lmhead_argmax(t: W12Tensor, x: torch.Tensor, qview: bool = False, stream=None):
+def lmhead_argmax(t: W12Tensor, x: torch.Tensor, qview: bool = False, stream=None, overlap: bool = False):
     """(idx int32[M], val f32[M], gap f32[M]) of y = x @ W^T without materialising y."""
     _bits(x)
     M = x.shape[0]
     idx = torch.empty(M, dtype=torch.int32, device=x.device)
     val = torch.empty(M, dtype=torch.float32, device=x.device)
     gap = torch.empty(M, dtype=torch.float32, device=x.device)
-    ws, nb = t.workspace(M, OP_QVIEW_ARGMAX if qview else OP_ARGMAX)
+    op = OP_QVIEW_ARGMAX if qview else OP_ARGMAX
+    ws, nb = t.workspace(M, op)
+    if overlap:
+        _check(lib().w12_gemm_ex(ctypes.byref(t.c), _ptr(x), M, op, None, OUT_F32, _ptr(idx), _ptr(val),
+                                 _ptr(gap), LAUNCH_OVERLAP, _ptr(ws), nb, _stream(stream)), "w12_gemm_ex")
+        return idx, val, gap
     _check(lib().w12_lmhead_argmax(ctypes.byref(t.c), _ptr(x), M, _ptr(idx), _ptr(val), _ptr(gap),
                                    1 if qview else 0, _ptr(ws), nb, _stream(stream)), "w12_lmhead_argmax")
     return idx, val, gap

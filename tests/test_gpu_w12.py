@@ -176,6 +176,25 @@ def test_gemm_bitwise_reproducible(w12):
     assert torch.equal(ia, ib) and torch.equal(va.view(torch.int32), vb.view(torch.int32))
 
 
+@pytest.mark.parametrize("M", [1, 32, 48, 64, 96, 192, 256])
+@pytest.mark.parametrize("qview", [False, True])
+def test_gemm_repeat_stress(w12, M, qview):
+    """Thirty launches on weights larger than L2, every result bitwise equal to the first. Covers
+    the ring configurations where the pipeline's stage count is not a multiple of the decode
+    groups (slots shared between groups) as well as those where it is."""
+    w = synth.weights(17408, 5120, synth.PROJ, seed=13, device="cuda")
+    t = w12.encode(w)
+    del w
+    copies = [t] + [t.clone_records() for _ in range(2)]
+    x = synth.activations(M, 5120, seed=14 + M, device="cuda")
+    first = w12.gemm(copies[0], x, qview=qview)
+    for i in range(1, 30):
+        y = w12.gemm(copies[i % 3], x, qview=qview)
+        assert torch.equal(y.view(torch.int32), first.view(torch.int32)), i
+    for c in copies:
+        w12.check(c)
+
+
 def test_workspace_counters_left_zeroed(w12):
     """Counters and the error word (the head of the workspace) are back at zero after a call, so
     the next call can reuse the workspace without clearing it; partial sums need no clearing."""
@@ -220,3 +239,31 @@ def test_lmhead_argmax(w12, N, K, M, qview):
     for m in range(M):
         if int(idx[m]) == ridx[m]:
             assert abs(g[m] - rgap[m]) <= 2 * (2e-3 * ad[m].max() + 1e-6)
+
+
+def test_overlap_launch_chain_matches_plain(w12):
+    """W12_LAUNCH_OVERLAP: each GEMM reads the previous GEMM's output as its x, with
+    the programmatic dependent launch. The results equal those of plain launches bit for bit, the
+    argmax included. The same tensor and workspace are reused back to back."""
+    w1 = synth.weights(1024, 2048, synth.PROJ, seed=21, device="cuda")
+    w2 = synth.weights(2048, 1024, synth.PROJ, seed=22, device="cuda")
+    t1, t2 = w12.encode(w1), w12.encode(w2)
+    x = synth.activations(16, 2048, seed=23, device="cuda")
+
+    def chain(overlap):
+        outs = []
+        h = x
+        for _ in range(6):
+            a = w12.gemm(t1, h, out_dtype=torch.bfloat16, overlap=overlap)
+            h = w12.gemm(t2, a, out_dtype=torch.bfloat16, overlap=overlap)
+            outs.append(h)
+        outs.append(w12.lmhead_argmax(t1, h, overlap=overlap)[0])
+        return outs
+
+    plain = chain(False)
+    over = chain(True)
+    torch.cuda.synchronize()
+    for a, b in zip(plain, over):
+        assert torch.equal(a, b)
+    w12.check(t1)
+    w12.check(t2)
