@@ -4,7 +4,10 @@
 Workload: the MLP projection of a 27B-class dense layer, K=5120, N=17408, weights and activations
 drawn by the seeded synthetic recipe; one step = one W12 GEMM per verification-row count
 M in {1, 4, 8, 16, 32} (fp32 output). Metric: achieved HBM GB/s of the encoded (12-bit) weight
-stream. Weight copies rotate so that no call finds its weights in L2 (inputs larger than L2).
+stream, over back-to-back steps bracketed by CUDA events. Weight copies rotate so that no call
+finds its weights in L2 (inputs larger than L2). Launches use W12_LAUNCH_OVERLAP by default, as a
+serving loop over static weights would (`--launch plain` for stream-ordered launches; both modes
+are also reported on the same line).
 
 Also reported on the same line: per-M times against a bf16 cuBLAS GEMM of the same shape, the
 LM-head fused argmax (K=5120, N=151936, M=32) in rows/s, the Q-view and M=192 GEMMs, encode and
@@ -221,6 +224,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="w12", choices=["w12", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip the LM-head/encode/verify/cuBLAS lines")
+    ap.add_argument("--launch", default="overlap", choices=["overlap", "plain"],
+                    help="overlap: W12_LAUNCH_OVERLAP (each GEMM may start while the previous one "
+                         "finishes; weights are static); plain: ordinary stream-ordered launches")
     ap.add_argument("--profile-gemm", type=int, default=0, metavar="M",
                     help="only run `--steps` W12 GEMM launches at M rows on the projection (for ncu)")
     ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax"])
@@ -232,6 +238,7 @@ def main():
 
     from lossless_bit_weight_gb300 import build, w12
 
+    overlap = args.launch == "overlap"
     ws, rank, local = dist_env()
     dist = None
     if ws > 1:
@@ -261,7 +268,7 @@ def main():
             c = copies[(it * len(MS) + j) % n_copies]
             if ev is not None:
                 ev[j][0].record(stream)
-            w12.gemm(c, xs[m], out=ys[m])
+            w12.gemm(c, xs[m], out=ys[m], overlap=overlap)
             if ev is not None:
                 ev[j][1].record(stream)
 
@@ -272,16 +279,12 @@ def main():
     if dist:
         dist.barrier()
 
-    ev_every = max(1, args.steps // 400)  # per-launch events on every ev_every-th step
-    ev_steps = list(range(0, args.steps, ev_every))
-    evs = {i: [[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in MS]
-           for i in ev_steps}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with Clocks(local) as clk:
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            step(args.warmup + i, evs.get(i))
+            step(args.warmup + i)
         stop.record(stream)
         torch.cuda.synchronize()
     if dist:
@@ -290,16 +293,26 @@ def main():
     for c in copies:
         w12.check(c)
     elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
-    per_m_us = {m: statistics.median(evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in ev_steps)
-                for j, m in enumerate(MS)}
-    all_launch_us = [evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in ev_steps for j in range(len(MS))]
     value = job_gbs(bytes_per_call * len(MS) * args.steps, ws, elapsed_ms)
 
-    # algorithmic bytes per launch (roofline): encoded weights + x + y, averaged over the sweep
+    # roofline of the GEMM kernel, the only kernel in the timed region: algorithmic bytes per
+    # launch (encoded weights + x + y, averaged over the sweep) over the average launch duration
+    # (the timed region's events / launches; with overlapped launches consecutive kernels share
+    # their start-up and drain, which this average includes once)
     alg = [bytes_per_call + 2 * m * K_HID + 4 * m * N_MLP for m in MS]
     avg_alg = sum(alg) / len(alg)
-    avg_launch_s = statistics.mean(all_launch_us) * 1e-6
+    avg_launch_s = elapsed_ms * 1e-3 / (args.steps * len(MS))
     achieved = avg_alg / avg_launch_s / 1e9
+
+    # per-M duration of one isolated launch (events around each; a diagnostic, after the timed
+    # region): an event between two launches keeps them from overlapping
+    nm = min(200, max(20, args.steps // 10))
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in MS] for _ in range(nm)]
+    for i in range(nm):
+        step(i, evs[i])
+    torch.cuda.synchronize()
+    per_m_us = {m: statistics.median(evs[i][j][0].elapsed_time(evs[i][j][1]) * 1e3 for i in range(nm))
+                for j, m in enumerate(MS)}
     traffic = profile_traffic()
 
     # ---- end to end through the C ABI with host buffers (pinned), one sweep per step
@@ -316,7 +329,7 @@ def main():
         for j, m in enumerate(MS):
             c = copies[(i * len(MS) + j) % n_copies]
             xd[m].copy_(xh[m], non_blocking=True)
-            w12.gemm(c, xd[m], out=ys[m])
+            w12.gemm(c, xd[m], out=ys[m], overlap=overlap)
             yh[m].copy_(ys[m], non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -330,6 +343,9 @@ def main():
         "warmup": args.warmup, "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "K": K_HID, "N": N_MLP, "M": list(MS), "out": "fp32",
+                   "launch": ("programmatic dependent launch (W12_LAUNCH_OVERLAP)" if overlap
+                              else "stream-ordered"),
+                   "weights": "escape fraction %.2e (SpecPilot Fig. 5/App. E range)" % (t0.n_esc / (N_MLP * K_HID)),
                    "l2": f"inputs larger than L2: {n_copies} rotating weight copies of {t0.nbytes/1e6:.1f} MB "
                          f"(L2 {l2/1e6:.0f} MB)", "parallelism": f"replicas x{ws}",
                    "w12_bytes_per_call": bytes_per_call, "escapes": t0.n_esc},
@@ -341,7 +357,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                      "frac": round(achieved / hbm_peak, 4), "traffic": traffic,
                      "kernel": "w12_gemm_kernel<exact>", "peak_kind": peak_kind,
-                     "alg_bytes_per_launch": round(avg_alg)},
+                     "alg_bytes_per_launch": round(avg_alg), "avg_launch_us": round(avg_launch_s * 1e6, 2)},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * len(MS),
     }
@@ -409,10 +425,43 @@ def _time(fn, reps=10, warm=3, flush=None):
     return statistics.median(ts)
 
 
+def sweep_gbs(copies, xs, overlap, steps=100):
+    """Encoded GB/s of back-to-back sweeps over M in MS, rotating the weight copies."""
+    from lossless_bit_weight_gb300 import w12
+
+    n = len(copies)
+    ys = {m: torch.empty((m, copies[0].N), dtype=torch.float32, device=xs[m].device) for m in MS}
+    for i in range(3 * len(MS)):
+        w12.gemm(copies[i % n], xs[MS[i % len(MS)]], out=ys[MS[i % len(MS)]], overlap=overlap)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for i in range(steps):
+        for j, m in enumerate(MS):
+            w12.gemm(copies[(i * len(MS) + j) % n], xs[m], out=ys[m], overlap=overlap)
+    b.record()
+    b.synchronize()
+    for c in copies:
+        w12.check(c)
+    return copies[0].gemm_bytes() * len(MS) * steps / (a.elapsed_time(b) * 1e-3) / 1e9
+
+
 def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
     from lossless_bit_weight_gb300 import w12
 
     out = {}
+    # the sweep in both launch modes, and on weights with 0.1% exact zeros (ten times the pages'
+    # escape fraction)
+    out["launch_modes_gbs"] = {"plain": round(sweep_gbs(copies, xs, False), 1),
+                               "overlap": round(sweep_gbs(copies, xs, True), 1)}
+    wz = synth.weights(N_MLP, K_HID, synth.ZERO_HEAVY, seed=synth.seed_for(1, 7), device=dev)
+    tz = w12.encode(wz)
+    del wz
+    zc = [tz] + [tz.clone_records() for _ in range(len(copies) - 1)]
+    out["zero_heavy"] = {"escapes_per_record": round(tz.n_esc / (tz.n_tiles * tz.k_tiles), 2),
+                         "plain_gbs": round(sweep_gbs(zc, xs, False), 1),
+                         "overlap_gbs": round(sweep_gbs(zc, xs, True), 1)}
+    del zc, tz
     flush = torch.empty(int(2 * l2) // 4, dtype=torch.float32, device=dev)
     # cuBLAS bf16 on the same shapes, same cold-L2 treatment (rotating copies)
     wcopies = [w] + [w.clone() for _ in range(2)]

@@ -87,6 +87,7 @@ struct Params {
     const uint32_t *rec_esc;
     int N, K, M, n_tiles, k_tiles, npad, stages, rps, nacc, acc_cols, grid;
     int unit;  // records per unit of the work split: 1 (stream-K) or k_tiles (whole tiles)
+    int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
     uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
     int R;  // records: n_tiles * k_tiles (< 2^22)
     void *y;
@@ -268,10 +269,23 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
 
     if (warp == kWarpProducer) {
         // ---------------------------------------------------------------- producer (warp-wide)
+        // The copy engine serves requests in order, so a slot's activation tiles queued behind
+        // the records of every later slot would hold its MMAs back by several microseconds.
+        // Plain launch: each slot's records, then its tiles. Overlapped launch: the records of
+        // every free slot first (they may load while the previous grid finishes), then the tiles
+        // once it has (by then those record copies have drained).
         const int n0 = min(S, nst);  // the first S slots start out free
-        for (int js = 1; js < n0; ++js) produce_rec(js);
-        grid_dependency_wait();  // x may be the previous grid's output
-        for (int js = 0; js < n0; ++js) produce_x(js, js);
+        if (p.overlap) {
+            for (int js = 1; js < n0; ++js) produce_rec(js);
+            grid_dependency_wait();  // x may be the previous grid's output
+            for (int js = 0; js < n0; ++js) produce_x(js, js);
+        } else {
+            if (n0 > 0) produce_x(0, 0);
+            for (int js = 1; js < n0; ++js) {
+                produce_rec(js);
+                produce_x(js, js);
+            }
+        }
         for (int js = n0; js < nst; ++js) {
             const int s = pst.idx;
             const bool ok = mbar_wait(smem_u32(&ctrl->empty[s]), pst.phase ^ 1, abort, p.err, kErrProducer);
@@ -895,6 +909,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.acc_cols = L.acc_cols;
     p.grid = L.grid;
     p.unit = L.unit;
+    p.overlap = overlap ? 1 : 0;
     p.R = static_cast<int>(L.R);
     p.y = y;
     p.y_bf16 = (y_dtype == W12_OUT_BF16);
