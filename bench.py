@@ -100,10 +100,6 @@ class Clocks:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def flush_l2(buf):
-    buf.add_(1)
-
-
 def max_over_ranks(x: float, dist=None, device="cpu") -> float:
     """The largest of every rank's x (the whole job ends when its slowest rank ends)."""
     if dist is None:
@@ -408,21 +404,21 @@ def profile_gemm(args):
                       "bytes": t.gemm_bytes(args.profile_op == "qview")}))
 
 
-def _time(fn, reps=10, warm=3, flush=None):
+def _time(fn, reps=20, warm=3):
+    """Mean device time of back-to-back calls fn(0..reps-1), between two events on the current
+    stream (no host gap between calls: the queue stays ahead of the GPU). Callers rotate inputs
+    larger than L2 through i."""
     st = torch.cuda.current_stream()
-    for _ in range(warm):
-        fn(0)
-    ts = []
-    for i in range(reps):
-        if flush is not None:
-            flush_l2(flush)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(st)
+    for i in range(warm):
         fn(i)
-        b.record(st)
-        b.synchronize()
-        ts.append(a.elapsed_time(b) * 1e3)
-    return statistics.median(ts)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(reps):
+        fn(i)
+    b.record(st)
+    b.synchronize()
+    return a.elapsed_time(b) * 1e3 / reps
 
 
 def sweep_gbs(copies, xs, overlap, steps=100):
@@ -462,7 +458,6 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
                          "plain_gbs": round(sweep_gbs(zc, xs, False), 1),
                          "overlap_gbs": round(sweep_gbs(zc, xs, True), 1)}
     del zc, tz
-    flush = torch.empty(int(2 * l2) // 4, dtype=torch.float32, device=dev)
     # cuBLAS bf16 on the same shapes, same cold-L2 treatment (rotating copies)
     wcopies = [w] + [w.clone() for _ in range(2)]
     cub = {}
@@ -471,6 +466,10 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
         cub[str(m)] = round(us, 2)
     out["cublas_bf16_us"] = cub
     del wcopies
+    n = len(copies)
+    # the W12 GEMM timed the same way (back-to-back calls, rotating copies), both launch modes
+    out["w12_us"] = {mode: {str(m): round(_time(lambda i, m=m: w12.gemm(copies[i % n], xs[m], overlap=(mode == "overlap")),
+                                                reps=15), 2) for m in MS} for mode in ("plain", "overlap")}
     # Q view and M = 192 rows (the batched tree budget)
     x192 = synth.activations(192, K_HID, seed=synth.seed_for(4, 192), device=dev)
     n = len(copies)
@@ -492,8 +491,9 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
     wh = synth.weights(VOCAB, K_HID, synth.HEAD, seed=synth.seed_for(2, 0), device=dev)
     th = w12.encode(wh)
     xh = synth.activations(32, K_HID, seed=synth.seed_for(2, 1), device=dev)
-    a_us = _time(lambda i: w12.lmhead_argmax(th, xh), reps=10, flush=flush)
-    c_us = _time(lambda i: torch.argmax(torch.nn.functional.linear(xh, wh), dim=1), reps=10, flush=flush)
+    # the head (1.17 GB encoded, 1.56 GB bf16) is far larger than L2: no rotation needed
+    a_us = _time(lambda i: w12.lmhead_argmax(th, xh), reps=10)
+    c_us = _time(lambda i: torch.argmax(torch.nn.functional.linear(xh, wh), dim=1), reps=10)
     w12.check(th)
     out["lmhead"] = {"M": 32, "us": round(a_us, 1), "rows_per_s": round(32 / (a_us * 1e-6), 1),
                      "weight_gbs": round(th.gemm_bytes() / (a_us * 1e-6) / 1e9, 1),

@@ -534,6 +534,62 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 store_y(m, n, f);
             }
         };
+        // Rows m0..m0+15 of this thread's column leave for y (or the argmax) or for this block's
+        // partial. One value per row per thread would take 16 narrow stores a thread, which
+        // drain slowly at the end of the launch; instead the chunk is staged in shared memory
+        // (the argmax scratch, unused by the GEMM variants) and leaves as 16-byte stores, a
+        // warp writing one 512-byte tile row per instruction. Called by all 128 threads.
+        constexpr int kStg = 132;  // staging row stride in floats: 16-byte rows, no bank conflicts
+        float *stg = reinterpret_cast<float *>(&ctrl->wtop[0][0]);
+        const bool y_vec = (p.N % 4 == 0) &&
+                           (reinterpret_cast<uintptr_t>(p.y) & (p.y_bf16 ? 7u : 15u)) == 0;
+        auto put_rows = [&](int m0, int tile, const float (&f)[16], float *part) {
+          if constexpr (kArgmax) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (m0 + i >= M) break;
+                if (part)
+                    part[static_cast<size_t>(m0 + i) * kTileN + nl] = f[i];
+                else
+                    emit(m0 + i, tile * kTileN + nl, f[i]);
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) stg[i * kStg + nl] = f[i];
+            named_bar_sync(kEpiBar, 128);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int q = et + 128 * j;  // float4 q of the 16 x 32 chunk
+                const int row = q >> 5, c4 = (q & 31) * 4;
+                const int m = m0 + row;
+                if (m >= M) continue;
+                const float4 v = *reinterpret_cast<const float4 *>(stg + row * kStg + c4);
+                if (part) {
+                    *reinterpret_cast<float4 *>(part + static_cast<size_t>(m) * kTileN + c4) = v;
+                    continue;
+                }
+                const int n0 = tile * kTileN + c4;
+                const size_t o = static_cast<size_t>(m) * p.N + n0;
+                if (y_vec && n0 + 3 < p.N) {
+                    if (p.y_bf16) {
+                        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+                        uint2 u;
+                        u.x = *reinterpret_cast<uint32_t *>(&lo);
+                        u.y = *reinterpret_cast<uint32_t *>(&hi);
+                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.y) + o) = u;
+                    } else {
+                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + o) = v;
+                    }
+                } else {
+                    const float e4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (n0 + e < p.N) store_y(m, n0 + e, e4[e]);
+                }
+            }
+            named_bar_sync(kEpiBar, 128);  // the staging area is free again
+          }
+        };
         auto partial_of = [&](int cc, int tile, int m) {  // block cc's partial of tile
             const int sl = (block_start(cc) / KT == tile) ? 0 : 1;
             return p.partials + ((static_cast<size_t>(cc) * 2 + sl) * M + m) * kTileN + nl;
@@ -548,7 +604,6 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             const int b = (p.nacc == 2) ? (jseg & 1) : 0;
             const uint32_t phb = (p.nacc == 2) ? ((jseg >> 1) & 1) : (jseg & 1);
             ++jseg;
-            const int n = static_cast<int>(tile) * kTileN + nl;
             const int c_lo = full ? c : owner(tile * KT);
             const int c_hi = full ? c : owner((tile + 1) * KT - 1);
             // 0: whole tile here; 1: publish a partial; 2: sum here from the published partials
@@ -570,9 +625,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                     for (int i = 0; i < 32; ++i) pf[i] = (i < M) ? __ldcg(src + static_cast<size_t>(i) * kTileN) : 0.f;
                 }
             }
-            bool ok = !dead && mbar_wait(smem_u32(&ctrl->accfull[b]), phb, abort, p.err, kErrEpilogue);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok) dead = true;
+            const bool ok = !dead && mbar_wait(smem_u32(&ctrl->accfull[b]), phb, abort, p.err, kErrEpilogue);
+            // uniform over the four warps: every barrier below is taken by all of them or none
+            dead = named_bar_or(kEpiBar, 128, !ok);
             const bool pre = mode == 2;  // the other block's partial is in pf
             if (!full && mode == 0) {
                 if (et == 0)
@@ -614,10 +669,8 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                             for (int i = 0; i < 16; ++i) f[i] = has0 ? f[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
                         }
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (m0 + i >= M) break;
-                            emit(m0 + i, n, f[i] + pf[16 * h + i]);
-                        }
+                        for (int i = 0; i < 16; ++i) f[i] += pf[16 * h + i];
+                        put_rows(m0, tile, f, nullptr);
                     }
                 }
                 for (int m0 = 0; !pre && m0 < M; m0 += 16) {
@@ -655,15 +708,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) f[i] = acc[i];
                     }
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int m = m0 + i;
-                        if (m >= M) break;
-                        if (mode == 1)
-                            part[static_cast<size_t>(m) * kTileN + nl] = f[i];
-                        else
-                            emit(m, n, f[i]);
-                    }
+                    put_rows(m0, tile, f, mode == 1 ? part : nullptr);
                 }
                 tc_fence_before();
             }
@@ -691,11 +736,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                             for (int i = 0; i < 16; ++i)
                                 if (m0 + i < M) f[i] += __ldcg(src + static_cast<size_t>(i) * kTileN);
                         }
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            if (m0 + i >= M) break;
-                            emit(m0 + i, n, f[i]);
-                        }
+                        put_rows(m0, tile, f, nullptr);
                     }
                 }
             }
