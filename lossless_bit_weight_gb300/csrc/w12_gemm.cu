@@ -67,9 +67,10 @@ struct Ctrl {
     uint64_t full[kMaxStages], afull[kMaxStages], empty[kMaxStages], xfull[kMaxStages];
     uint64_t accfull[2], accempty[2];
     uint64_t done[2];
-    uint32_t esc_cnt[kMaxStages];    // entries of the slot (bit 31: too many, read from global)
-    uint32_t esc_split[kMaxStages];  // entries that belong to the slot's first record
-    uint32_t esc_src[kMaxStages];    // index of the slot's first entry in the global index
+    // per slot: x = index words of the slot (bit 31: too many to stage, read from global),
+    // y = words that belong to the slot's first record; one 8-byte load for the decode warps
+    uint2 esc_info[kMaxStages];
+    uint32_t esc_src[kMaxStages];    // index of the slot's first word in the global index
     uint32_t tmem_base;
     int abort;
     int fix;          // block-wide flag of the final argmax merge
@@ -375,8 +376,8 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 const uint32_t fb = smem_u32(&ctrl->full[s]);
                 const uint32_t cnt = hi - lo;
                 if (lane == 0) {
-                    ctrl->esc_split[s] = (nr == 2) ? mid - lo : cnt;
-                    ctrl->esc_cnt[s] = (cnt <= static_cast<uint32_t>(kEscCap)) ? cnt : (cnt | 0x80000000u);
+                    ctrl->esc_info[s] = make_uint2((cnt <= static_cast<uint32_t>(kEscCap)) ? cnt : (cnt | 0x80000000u),
+                                                   (nr == 2) ? mid - lo : cnt);
                     ctrl->esc_src[s] = lo;
                 }
                 __syncwarp();  // the header stores come before the arrive that publishes them
@@ -434,10 +435,10 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
         // few instructions each; the typical warp has 0-3). The segment header gives the
         // warp's entry range directly; every lane reads the same entry (a broadcast), so the
         // control flow is warp-uniform.
-        auto patch_record = [&](int s, int q) {
-            const uint32_t hdr = ctrl->esc_cnt[s];
+        auto patch_record = [&](int s, int q, uint2 ei) {
+            const uint32_t hdr = ei.x;
             const uint32_t total = hdr & 0x7FFFFFFFu;
-            const uint32_t split = ctrl->esc_split[s];
+            const uint32_t split = ei.y;
             const uint32_t sg0 = (q == 0) ? 0u : split, sg1 = (q == 0) ? split : total;
             if (sg1 <= sg0) return;
             const uint32_t *seg = ((hdr >> 31) ? p.rec_esc + ctrl->esc_src[s]
@@ -489,8 +490,11 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             }
             tmem_wait_st();
             if (!kQView) {
-                patch_record(s, 0);
-                if (nr == 2) patch_record(s, 1);
+                const uint2 ei = ctrl->esc_info[s];
+                if (ei.x != 0) {  // the slot has index words
+                    patch_record(s, 0, ei);
+                    if (nr == 2) patch_record(s, 1, ei);
+                }
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&ctrl->afull[s]));

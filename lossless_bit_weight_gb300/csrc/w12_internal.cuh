@@ -397,11 +397,18 @@ __device__ __forceinline__ uint4 lds128(const void *p) {
 template <bool kQView>
 __device__ __forceinline__ uint32_t decode_pair(uint32_t x, uint32_t bs, uint32_t base2, uint32_t m3,
                                                 uint32_t m15) {
-    const uint32_t t = x * m3 + base2;
-    const uint32_t u = x * m15;
-    const uint32_t r1 = (u & 0x80008000u) | (t & 0x7FFF7FFFu);
-    if (kQView) return (r1 & 0xFFF0FFF0u) | 0x00080008u;  // low mantissa := 1000b
-    return (bs & 0x000F000Fu) | (r1 & 0xFFF0FFF0u);
+    // Written as PTX so that each bit-field select stays one lop3 (select LUT 0xCA: a ? b : c);
+    // from the C++ form the compiler emitted two logic ops for one of them.
+    uint32_t t, u, r1, out;
+    asm("mad.lo.u32 %0, %1, %2, %3;" : "=r"(t) : "r"(x), "r"(m3), "r"(base2));
+    asm("mul.lo.u32 %0, %1, %2;" : "=r"(u) : "r"(x), "r"(m15));
+    asm("lop3.b32 %0, %1, %2, %3, 0xCA;" : "=r"(r1) : "r"(0x80008000u), "r"(u), "r"(t));  // sign | rest
+    if (kQView) {  // low mantissa := 1000b: (r1 & 0xFFF0FFF0) | 0x00080008 (LUT 0xEA)
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(out) : "r"(r1), "r"(0xFFF0FFF0u), "r"(0x00080008u));
+        return out;
+    }
+    asm("lop3.b32 %0, %1, %2, %3, 0xCA;" : "=r"(out) : "r"(0x000F000Fu), "r"(bs), "r"(r1));  // B nibbles
+    return out;
 }
 
 // Sixteen weights k_l = 16c .. 16c+15 of one channel row -> 8 bf16x2 words.
