@@ -61,7 +61,10 @@ constexpr int kEpiBar = 1;               // named barrier of the 128 epilogue th
 // Whole tiles per block are used when the busiest block then has at most this factor of the
 // average work: up to 15% imbalance costs less than splitting tiles and summing the partials
 // at the end (measured on the 136-tile MLP projection on 152 SMs).
-constexpr double kTileSplitSlack = 1.15;
+#ifndef W12_TILE_SPLIT_SLACK
+#define W12_TILE_SPLIT_SLACK 1.15
+#endif
+constexpr double kTileSplitSlack = W12_TILE_SPLIT_SLACK;
 
 struct Ctrl {
     uint64_t full[kMaxStages], afull[kMaxStages], empty[kMaxStages], xfull[kMaxStages];
@@ -539,16 +542,10 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             }
         };
         // Rows m0..m0+15 of this thread's column leave for y (or the argmax) or for this block's
-        // partial. One value per row per thread would take 16 narrow stores a thread, which
-        // drain slowly at the end of the launch; instead the chunk is staged in shared memory
-        // (the argmax scratch, unused by the GEMM variants) and leaves as 16-byte stores, a
-        // warp writing one 512-byte tile row per instruction. Called by all 128 threads.
-        constexpr int kStg = 132;  // staging row stride in floats: 16-byte rows, no bank conflicts
-        float *stg = reinterpret_cast<float *>(&ctrl->wtop[0][0]);
-        const bool y_vec = (p.N % 4 == 0) &&
-                           (reinterpret_cast<uintptr_t>(p.y) & (p.y_bf16 ? 7u : 15u)) == 0;
+        // partial, one value per row (a warp writes 128 contiguous bytes per row). Staging the
+        // chunk in shared memory for 16-byte stores was measured: no faster with whole tiles, and
+        // much slower with split tiles, where its two barriers per chunk serialise the warps.
         auto put_rows = [&](int m0, int tile, const float (&f)[16], float *part) {
-          if constexpr (kArgmax) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 if (m0 + i >= M) break;
@@ -557,42 +554,6 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 else
                     emit(m0 + i, tile * kTileN + nl, f[i]);
             }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) stg[i * kStg + nl] = f[i];
-            named_bar_sync(kEpiBar, 128);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int q = et + 128 * j;  // float4 q of the 16 x 32 chunk
-                const int row = q >> 5, c4 = (q & 31) * 4;
-                const int m = m0 + row;
-                if (m >= M) continue;
-                const float4 v = *reinterpret_cast<const float4 *>(stg + row * kStg + c4);
-                if (part) {
-                    *reinterpret_cast<float4 *>(part + static_cast<size_t>(m) * kTileN + c4) = v;
-                    continue;
-                }
-                const int n0 = tile * kTileN + c4;
-                const size_t o = static_cast<size_t>(m) * p.N + n0;
-                if (y_vec && n0 + 3 < p.N) {
-                    if (p.y_bf16) {
-                        __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-                        uint2 u;
-                        u.x = *reinterpret_cast<uint32_t *>(&lo);
-                        u.y = *reinterpret_cast<uint32_t *>(&hi);
-                        *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.y) + o) = u;
-                    } else {
-                        *reinterpret_cast<float4 *>(reinterpret_cast<float *>(p.y) + o) = v;
-                    }
-                } else {
-                    const float e4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if (n0 + e < p.N) store_y(m, n0 + e, e4[e]);
-                }
-            }
-            named_bar_sync(kEpiBar, 128);  // the staging area is free again
-          }
         };
         auto partial_of = [&](int cc, int tile, int m) {  // block cc's partial of tile
             const int sl = (block_start(cc) / KT == tile) ? 0 : 1;
