@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <cstddef>
 #include <mutex>
 
 #include "w12_internal.cuh"
@@ -80,9 +81,13 @@ struct Ctrl {
     int mode[2];      // how a split tile ends (by segment parity)
     int last[2];      // this block published last and sums the tile (by segment parity)
     int pre;          // the last segment's other block had published before its MMAs completed
-    float4 wtop[4][kMaxM];  // per-warp top-2 of the current tile (argmax)
+    // per-warp top-2 of the current tile (argmax); in the GEMM variants the staging buffers of
+    // the epilogue's tensor stores, whose shared-memory source must be 128-byte aligned
+    alignas(128) float4 wtop[4][kMaxM];
     float4 ctop[kMaxM];     // running top-2 of this block (argmax)
 };
+
+static_assert(offsetof(Ctrl, wtop) % 128 == 0, "tensor-store staging must be 128-byte aligned");
 
 struct Params {
     const uint8_t *records;
@@ -92,6 +97,7 @@ struct Params {
     int N, K, M, n_tiles, k_tiles, npad, stages, rps, nacc, acc_cols, grid;
     int unit;  // records per unit of the work split: 1 (stream-K) or k_tiles (whole tiles)
     int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
+    int y_tma;    // y is written by tiled tensor stores through ymap
     uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
     int R;  // records: n_tiles * k_tiles (< 2^22)
     void *y;
@@ -155,7 +161,8 @@ __device__ __forceinline__ void warp_top2(float &v1, int &i1, float &v2) {
 
 template <bool kQView, bool kArgmax>
 __global__ void __launch_bounds__(kThreads, 1)
-w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
+w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
+                const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -542,10 +549,38 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
             }
         };
         // Rows m0..m0+15 of this thread's column leave for y (or the argmax) or for this block's
-        // partial, one value per row (a warp writes 128 contiguous bytes per row). Staging the
-        // chunk in shared memory for 16-byte stores was measured: no faster with whole tiles, and
-        // much slower with split tiles, where its two barriers per chunk serialise the warps.
+        // partial. y goes out through the copy engine when the tensor map allows it (p.y_tma):
+        // each warp stages its 16 x 32 block in shared memory (two buffers, the argmax scratch
+        // area) and one lane issues a tiled tensor store, which writes only the elements inside
+        // y. The warps then need not wait for the stores to drain, which under the weight stream
+        // of the blocks still running takes microseconds per chunk. Partial sums, read back by
+        // another block, are stored directly, one value per row.
+        int ybuf = 0;
         auto put_rows = [&](int m0, int tile, const float (&f)[16], float *part) {
+          if constexpr (!kArgmax) {
+            if (!part && p.y_tma) {
+                const int esz = p.y_bf16 ? 2 : 4;
+                uint8_t *stg = reinterpret_cast<uint8_t *>(&ctrl->wtop[0][0]) + (qw * 2 + ybuf) * 16 * 32 * esz;
+                ybuf ^= 1;
+                if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (p.y_bf16)
+                        reinterpret_cast<__nv_bfloat16 *>(stg)[i * 32 + lane] = __float2bfloat16_rn(f[i]);
+                    else
+                        reinterpret_cast<float *>(stg)[i * 32 + lane] = f[i];
+                }
+                fence_proxy_async_shared();
+                __syncwarp();
+                // a box that starts at or beyond column N writes nothing: not issued
+                if (lane == 0 && tile * kTileN + 32 * qw < p.N) {
+                    tma_2d_s2g(&ymap, tile * kTileN + 32 * qw, m0, smem_u32(stg));
+                    bulk_commit_group();
+                }
+                return;
+            }
+          }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 if (m0 + i >= M) break;
@@ -722,6 +757,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const Params p) {
                 named_bar_sync(kEpiBar, 128);
             }
         }
+        // the tensor stores must have read their staging buffers before the block's shared
+        // memory goes away (their writes to y complete on their own)
+        if (!kArgmax && p.y_tma && lane == 0) bulk_wait_group_read<0>();
         if (kArgmax) {
             // publish this block's top-2 per row; the last block merges all blocks in order
             for (int m = et; m < M; m += 128) p.cta_top[static_cast<size_t>(c) * M + m] = ctrl->ctop[m];
@@ -792,6 +830,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 struct Layout {
     int npad, stages, rps, nacc, acc_cols, grid, unit, smem;
+    bool whole;  // every block covers whole tiles (no partial sums)
     int64_t R;
     size_t ws_bytes, off_err, off_tile, off_done, off_part, off_top;
 };
@@ -830,9 +869,11 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     if (static_cast<double>(per) * sms <= kTileSplitSlack * T) {
         L->grid = gt;
         L->unit = t->k_tiles;
+        L->whole = true;
     } else {
         L->grid = static_cast<int>(L->R < sms ? L->R : sms);
         L->unit = 1;
+        L->whole = false;
     }
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -850,8 +891,8 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
 }
 
 template <bool kQ, bool kA>
-w12_status launch_variant(const CUtensorMap &map, const Params &p, const Layout &L, bool overlap,
-                          cudaStream_t st) {
+w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &ymap, const Params &p, const Layout &L,
+                          bool overlap, cudaStream_t st) {
     auto kern = w12_gemm_kernel<kQ, kA>;
     W12_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem));
     cudaLaunchConfig_t cfg{};
@@ -864,7 +905,7 @@ w12_status launch_variant(const CUtensorMap &map, const Params &p, const Layout 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, p));
+    W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, ymap, p));
     return W12_OK;
 }
 
@@ -894,6 +935,20 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return W12_ERR_INVALID_ARG;
+    // y as a 2-D tensor for the epilogue's tiled stores (boxes of 32 columns x 16 rows); plain
+    // stores are used where the tensor map's alignment rules do not hold
+    CUtensorMap ymap = map;
+    bool y_tma = false;
+    if (!argmax) {
+        const cuuint64_t esz = (y_dtype == W12_OUT_BF16) ? 2 : 4;
+        const cuuint64_t ydims[2] = {static_cast<cuuint64_t>(t->N), static_cast<cuuint64_t>(M)};
+        const cuuint64_t ystrides[1] = {static_cast<cuuint64_t>(t->N) * esz};
+        const cuuint32_t ybox[2] = {32, 16};
+        if (aligned16(y) && (ystrides[0] % 16) == 0)
+            y_tma = enc(&ymap, esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, y,
+                        ydims, ystrides, ybox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
 
     uint8_t *w = static_cast<uint8_t *>(ws);
     Params p{};
@@ -916,6 +971,9 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.grid = L.grid;
     p.unit = L.unit;
     p.overlap = overlap ? 1 : 0;
+    // Tensor stores pay off when the blocks finish together (whole tiles); with split tiles
+    // (stream-K) plain stores measured faster, so they are kept there.
+    p.y_tma = (y_tma && L.whole) ? 1 : 0;
     p.R = static_cast<int>(L.R);
     p.y = y;
     p.y_bf16 = (y_dtype == W12_OUT_BF16);
@@ -929,10 +987,10 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.gap = gap;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (q)
-        return argmax ? launch_variant<true, true>(map, p, L, overlap, st)
-                      : launch_variant<true, false>(map, p, L, overlap, st);
-    return argmax ? launch_variant<false, true>(map, p, L, overlap, st)
-                  : launch_variant<false, false>(map, p, L, overlap, st);
+        return argmax ? launch_variant<true, true>(map, ymap, p, L, overlap, st)
+                      : launch_variant<true, false>(map, ymap, p, L, overlap, st);
+    return argmax ? launch_variant<false, true>(map, ymap, p, L, overlap, st)
+                  : launch_variant<false, false>(map, ymap, p, L, overlap, st);
 }
 
 }  // namespace

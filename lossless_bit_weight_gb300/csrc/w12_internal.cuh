@@ -163,6 +163,25 @@ __device__ __forceinline__ void tma_2d_g2s(uint32_t dst, const CUtensorMap *map,
         : "memory");
 }
 
+// 2-D tiled tensor copy shared -> global (bulk async-group of the executing thread); elements
+// of the box outside the tensor are not written
+__device__ __forceinline__ void tma_2d_s2g(const CUtensorMap *map, int c0, int c1, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+        ::"l"(map), "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until at most N of this thread's bulk groups still have to read their shared memory
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+// order this thread's generic-proxy shared-memory writes before later async-proxy reads
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // Programmatic dependent launch (sm_90+). wait: block until the grids this launch depends on
 // have completed and their memory is visible (returns at once when there are none).
 // launch_dependents: let the grid launched after this one on the stream begin; it still waits
