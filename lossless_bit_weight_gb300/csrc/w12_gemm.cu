@@ -613,7 +613,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             // tile at the start of its range), fetch that partial now, while this segment's MMAs
             // still run, instead of after them. Rows <= 32 only: the partial lives in registers.
             float pf[32];
-            const bool pre_ok = !full && !dead && seg_end == r1 && c_hi - c_lo == 1 && M <= 32;
+            // the GEMM variants leave split tiles to w12_reduce_kernel: they only publish
+            constexpr bool kFix = kArgmax;
+            const bool pre_ok = kFix && !full && !dead && seg_end == r1 && c_hi - c_lo == 1 && M <= 32;
             if (pre_ok) {  // once per block: ctrl->pre is written only here
                 if (et == 0) ctrl->pre = (ld_acquire_gpu(&p.tile_cnt[tile]) == 1u) ? 2 : 0;
                 named_bar_sync(kEpiBar, 128);
@@ -630,11 +632,15 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             dead = named_bar_or(kEpiBar, 128, !ok);
             const bool pre = mode == 2;  // the other block's partial is in pf
             if (!full && mode == 0) {
-                if (et == 0)
-                    ctrl->mode[par] = (ld_acquire_gpu(&p.tile_cnt[tile]) == static_cast<uint32_t>(c_hi - c_lo)) ? 2 : 1;
-                named_bar_sync(kEpiBar, 128);
-                mode = ctrl->mode[par];
-                if (mode == 2) fence_acq_rel_gpu();
+                if (kFix) {
+                    if (et == 0)
+                        ctrl->mode[par] = (ld_acquire_gpu(&p.tile_cnt[tile]) == static_cast<uint32_t>(c_hi - c_lo)) ? 2 : 1;
+                    named_bar_sync(kEpiBar, 128);
+                    mode = ctrl->mode[par];
+                    if (mode == 2) fence_acq_rel_gpu();
+                } else {
+                    mode = 1;  // publish; the reduce kernel sums the tile
+                }
             }
             float *part = p.partials + (static_cast<size_t>(c) * 2 + slot) * M * kTileN;
             if (!dead) {
@@ -715,7 +721,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             mbar_arrive(smem_u32(&ctrl->accempty[b]));
 
             bool emitted = (mode != 1);
-            if (mode == 1) {
+            if (kFix && mode == 1) {
                 fence_acq_rel_gpu();  // this thread's partial stores come before the count
                 named_bar_sync(kEpiBar, 128);
                 if (et == 0) {
@@ -807,6 +813,47 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// Split tiles of the GEMM variants (stream-K): y[m, n] = sum over the tile's blocks, in
+// increasing block order, of their published fp32 partials. One block per (tile, row m), one
+// thread per column of the tile; tiles covered by a single block were written by the GEMM.
+// Launched right after the GEMM as a programmatic dependent launch: it waits for the GEMM's
+// completion before reading the partials.
+__global__ void __launch_bounds__(kTileN)
+w12_reduce_kernel(const Params p) {
+    grid_launch_dependents();
+    const int tile = blockIdx.x, m = blockIdx.y, nl = threadIdx.x;
+    const int R = p.R, G = p.grid, KT = p.k_tiles, U = p.unit, M = p.M;
+    auto block_start = [&](int cc) { return U * range_start(cc, R / U, G); };
+    const int c_lo = owner_of((tile * KT) / U, R / U, G);
+    const int c_hi = owner_of(((tile + 1) * KT - 1) / U, R / U, G);
+    if (c_lo == c_hi) return;
+    grid_dependency_wait();
+    const int n = tile * kTileN + nl;
+    float acc = 0.f;
+    constexpr int kBatch = 8;  // loads in flight per thread; the sum keeps block order
+    for (int c0 = c_lo; c0 <= c_hi; c0 += kBatch) {
+        float v[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            const int cc = c0 + j;
+            v[j] = 0.f;
+            if (cc <= c_hi) {
+                const int sl = (block_start(cc) / KT == tile) ? 0 : 1;
+                v[j] = __ldcg(p.partials + ((static_cast<size_t>(cc) * 2 + sl) * M + m) * kTileN + nl);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (c0 + j <= c_hi) acc += v[j];
+    }
+    if (n < p.N) {
+        if (p.y_bf16)
+            reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(acc);
+        else
+            reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] = acc;
     }
 }
 
@@ -906,6 +953,15 @@ w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &ymap, const
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
     W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, ymap, p));
+    if (!kA && !L.whole && L.grid > 1) {
+        cudaLaunchConfig_t rc{};
+        rc.gridDim = dim3(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(p.M));
+        rc.blockDim = dim3(kTileN);
+        rc.stream = st;
+        rc.attrs = attr;
+        rc.numAttrs = 1;  // starts while the GEMM drains; waits for it before reading
+        W12_CUDA(cudaLaunchKernelEx(&rc, w12_reduce_kernel, p));
+    }
     return W12_OK;
 }
 
