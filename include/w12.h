@@ -109,8 +109,11 @@ w12_status w12_encode_sizes(const uint16_t *w, int N, int K, void *scratch, size
                             int64_t *n_esc, int64_t *n_rec_esc, w12_stream_t stream);
 
 /* Encodes w (device bf16 [N, K]) into the caller's buffers in *t (t->N, t->K, t->n_esc and
- * t->n_rec_esc must match w12_encode_sizes). Writes never exceed the stated buffer sizes.
- * SYNCHRONISES `stream` and returns W12_ERR_INVALID_ARG if the counts found differ from t's. */
+ * t->n_rec_esc must match w12_encode_sizes). `scratch` must be the buffer that
+ * w12_encode_sizes filled for this same w, N and K, unchanged since. This call reuses the window
+ * bases, escape counts and offsets left there and runs only the writing pass. Writes never exceed
+ * the stated buffer sizes. SYNCHRONISES `stream` and returns W12_ERR_INVALID_ARG if the counts
+ * written differ from t's. */
 w12_status w12_encode(const uint16_t *w, int N, int K, void *scratch, size_t scratch_bytes,
                       const w12_tensor *t, w12_stream_t stream);
 

@@ -12,8 +12,11 @@
 //   pack     one block per 128x64 record: planes and escape flags of 8192 weights; counting
 //            mode writes per-(channel, k-tile) and per-record escape counts, writing mode writes
 //            the record bytes, the per-record index and the per-channel list
-//   rowscan  one thread per channel: exclusive prefix of its per-k-tile counts
-//   scan     one block: exclusive prefix over channels / records -> list offsets
+//   rowscan  one warp per channel: exclusive prefix of its per-k-tile counts
+//   scan     two blocks in one launch: exclusive prefixes over channels and over records ->
+//            the offsets of both escape lists
+// w12_encode_sizes runs window, pack (counting), rowscan and scan; w12_encode reuses their
+// results from the scratch and runs pack (writing) only.
 #include "w12_internal.cuh"
 
 namespace w12 {
@@ -195,20 +198,20 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
                                           a.ct[static_cast<size_t>(n) * a.k_tiles + kt] +
                                           (half ? partner : 0)
                                     : 0;
+    // escapes are rare (about one per record): their patterns are read again (from L2) rather
+    // than keeping the 32 loaded patterns live across the block scan, which cost occupancy
     uint32_t seen = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        if (mask & (1u << j)) {
-            const uint32_t bits = (u[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-            const int64_t ri = rbase + seen, ci = cbase + seen;
-            if (ri < a.rec_cap)
-                a.rec_esc[ri] = static_cast<uint32_t>(nl * kTileK + 32 * half + j) | (bits << 16);
-            if (ci < a.esc_cap) {
-                a.esc_k[ci] = static_cast<uint32_t>(k0 + j);
-                a.esc_bits[ci] = static_cast<uint16_t>(bits);
-            }
-            ++seen;
+    for (uint32_t m = mask; m != 0; m &= m - 1) {
+        const int j = __ffs(m) - 1;
+        const uint32_t bits = __ldg(a.w + static_cast<size_t>(n) * a.K + k0 + j);
+        const int64_t ri = rbase + seen, ci = cbase + seen;
+        if (ri < a.rec_cap)
+            a.rec_esc[ri] = static_cast<uint32_t>(nl * kTileK + 32 * half + j) | (bits << 16);
+        if (ci < a.esc_cap) {
+            a.esc_k[ci] = static_cast<uint32_t>(k0 + j);
+            a.esc_bits[ci] = static_cast<uint16_t>(bits);
         }
+        ++seen;
     }
     if (threadIdx.x == 255 && total > 0) {
         const int64_t end = a.rec_off[r + 1];
@@ -217,17 +220,25 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
     }
 }
 
-__global__ void rowscan_kernel(uint32_t *ct, int n_pad, int k_tiles, uint32_t *chan_cnt) {
-    const int n = blockIdx.x * blockDim.x + threadIdx.x;
+// one warp per channel: exclusive prefix of its per-k-tile counts, in place, and the total
+__global__ void __launch_bounds__(256) rowscan_kernel(uint32_t *ct, int n_pad, int k_tiles, uint32_t *chan_cnt) {
+    const int n = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
     if (n >= n_pad) return;
     uint32_t *row = ct + static_cast<size_t>(n) * k_tiles;
     uint32_t run = 0;
-    for (int kt = 0; kt < k_tiles; ++kt) {
-        const uint32_t c = row[kt];
-        row[kt] = run;
-        run += c;
+    for (int k0 = 0; k0 < k_tiles; k0 += 32) {
+        const int kt = k0 + lane;
+        const uint32_t c = (kt < k_tiles) ? row[kt] : 0u;
+        uint32_t incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (kt < k_tiles) row[kt] = run + incl - c;
+        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
     }
-    chan_cnt[n] = run;
+    if (lane == 0) chan_cnt[n] = run;
 }
 
 // words of a record's index segment with c escapes: none, or a 4-word header + c entries
@@ -235,8 +246,20 @@ __global__ void rowscan_kernel(uint32_t *ct, int n_pad, int k_tiles, uint32_t *c
 __device__ __forceinline__ uint32_t segment_words(uint32_t c) { return c ? 4u + ((c + 3u) & ~3u) : 0u; }
 
 // out[i] = sum_{j<i} in'[j], out[count] = total, with in' = in, or segment_words(in) if seg
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const uint32_t *in, int64_t count,
-                                                            uint32_t *out, int seg) {
+struct ScanJob {
+    const uint32_t *in;
+    int64_t count;
+    uint32_t *out;
+    int seg;
+};
+
+// block b runs job b (the channel scan and the record scan share one launch)
+__global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanJob j0, ScanJob j1) {
+    const ScanJob &job = blockIdx.x == 0 ? j0 : j1;
+    const uint32_t *in = job.in;
+    const int64_t count = job.count;
+    uint32_t *out = job.out;
+    const int seg = job.seg;
     __shared__ uint32_t warp_sums[kScanThreads / 32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int64_t chunk = (count + kScanThreads - 1) / kScanThreads;
@@ -323,11 +346,9 @@ w12_status count_pass(const uint16_t *w, int N, int K, const Scratch &s, uint8_t
     a.rec_cnt = s.rec_cnt;
     pack_kernel<false><<<R, 256, 0, st>>>(a);
     W12_CUDA(cudaGetLastError());
-    rowscan_kernel<<<static_cast<int>(ceil_div(n_pad, 256)), 256, 0, st>>>(s.ct, n_pad, k_tiles, s.chan_cnt);
+    rowscan_kernel<<<static_cast<int>(ceil_div(n_pad, 8)), 256, 0, st>>>(s.ct, n_pad, k_tiles, s.chan_cnt);
     W12_CUDA(cudaGetLastError());
-    scan_kernel<<<1, kScanThreads, 0, st>>>(s.chan_cnt, N, esc_off, 0);
-    W12_CUDA(cudaGetLastError());
-    scan_kernel<<<1, kScanThreads, 0, st>>>(s.rec_cnt, R, rec_off, 1);
+    scan_kernel<<<2, kScanThreads, 0, st>>>(ScanJob{s.chan_cnt, N, esc_off, 0}, ScanJob{s.rec_cnt, R, rec_off, 1});
     W12_CUDA(cudaGetLastError());
     return W12_OK;
 }
@@ -377,8 +398,15 @@ extern "C" w12_status w12_encode(const uint16_t *w, int N, int K, void *scratch,
     const Scratch s = carve(scratch, N, K);
     if (scratch_bytes < s.bytes) return W12_ERR_WORKSPACE;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    W12_TRY(count_pass(w, N, K, s, t->base_exp, t->esc_off, t->rec_esc_off, st));
     const int R = t->n_tiles * t->k_tiles;
+    // the window bases, per-(channel, k tile) prefixes and both offset lists are those that
+    // w12_encode_sizes left in the scratch for this w: copy the three outputs into place
+    const size_t n_pad = static_cast<size_t>(t->n_tiles) * kTileN;
+    W12_CUDA(cudaMemcpyAsync(t->base_exp, s.base_tmp, n_pad, cudaMemcpyDeviceToDevice, st));
+    W12_CUDA(cudaMemcpyAsync(t->esc_off, s.off_chan, sizeof(uint32_t) * (static_cast<size_t>(N) + 1),
+                             cudaMemcpyDeviceToDevice, st));
+    W12_CUDA(cudaMemcpyAsync(t->rec_esc_off, s.off_rec, sizeof(uint32_t) * (static_cast<size_t>(R) + 1),
+                             cudaMemcpyDeviceToDevice, st));
     PackArgs a{};
     a.w = w;
     a.N = N;

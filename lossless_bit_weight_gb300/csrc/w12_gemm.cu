@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstddef>
 #include <mutex>
 
@@ -941,7 +942,15 @@ template <bool kQ, bool kA>
 w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &ymap, const Params &p, const Layout &L,
                           bool overlap, cudaStream_t st) {
     auto kern = w12_gemm_kernel<kQ, kA>;
-    W12_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L.smem));
+    // the opt-in shared-memory limit is set once per device (to the maximum any plan uses)
+    static std::atomic<uint64_t> smem_set{0};
+    int dev = 0;
+    W12_CUDA(cudaGetDevice(&dev));
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(smem_set.load(std::memory_order_acquire) & bit)) {
+        W12_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit));
+        smem_set.fetch_or(bit, std::memory_order_acq_rel);
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
     cfg.blockDim = dim3(kThreads);
