@@ -54,20 +54,9 @@ decode_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ b
     }
 }
 
-__device__ __forceinline__ uint32_t block_sum256(uint32_t v) {
-    __shared__ uint32_t s[8];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
-    if ((threadIdx.x & 31) == 0) s[threadIdx.x >> 5] = v;
-    __syncthreads();
-    uint32_t t = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) t += s[i];
-    __syncthreads();
-    return t;
-}
-
-// counters[0] += differing weights/entries, counters[1] += real per-record index entries
+// counters[0] += differing weights/entries, counters[1] += real per-record index entries.
+// The record's planes and the reference row chunks are loaded first: they do not depend on the
+// escape pass, so their latency overlaps it. Two block barriers; counts are summed per warp.
 __global__ void __launch_bounds__(256)
 verify_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ base_exp,
               const uint32_t *__restrict__ rec_off, const uint32_t *__restrict__ rec_esc, int N,
@@ -77,11 +66,26 @@ verify_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ b
     __shared__ uint32_t quarter_cnt[4];
     const int r = blockIdx.x;
     const int nt = r / k_tiles, kt = r % k_tiles;
-    for (int i = threadIdx.x; i < kRecordWeights / 32; i += blockDim.x) esc_map[i] = 0;
+    const int nl = threadIdx.x >> 1, half = threadIdx.x & 1;
+    const int n = nt * kTileN + nl;
+    const int k0 = kt * kTileK + 32 * half;
+    const uint8_t *rec = records + static_cast<size_t>(r) * kRecordBytes;
+    const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(rec + 2048 * (2 * half) + 16 * nl));
+    const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(rec + 2048 * (2 * half + 1) + 16 * nl));
+    const uint4 bq = __ldg(reinterpret_cast<const uint4 *>(rec + kViewBytes + 2048 * half + 16 * nl));
+    const int En = base_exp[n];
+    uint4 ref[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+        ref[g] = (n < N && k0 + 8 * g < K)
+                     ? __ldg(reinterpret_cast<const uint4 *>(w_ref + static_cast<size_t>(n) * K + k0 + 8 * g))
+                     : make_uint4(0, 0, 0, 0);
+    const uint32_t seg_lo = rec_off[r], seg_hi = rec_off[r + 1];
+
+    esc_map[threadIdx.x] = 0;  // 256 words, one per thread
     if (threadIdx.x < 4) quarter_cnt[threadIdx.x] = 0;
     __syncthreads();
     uint32_t bad = 0, entries = 0;
-    const uint32_t seg_lo = rec_off[r], seg_hi = rec_off[r + 1];
     const uint32_t first = seg_lo + (seg_hi > seg_lo ? 4u : 0u);
     for (uint32_t i = first + threadIdx.x; i < seg_hi; i += blockDim.x) {
         const uint32_t e = rec_esc[i];
@@ -107,19 +111,16 @@ verify_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ b
             if (rec_esc[seg_lo + q] != run) ++bad;
         }
     }
-    __syncthreads();
-    const int nl = threadIdx.x >> 1, half = threadIdx.x & 1;
-    const int n = nt * kTileN + nl;
-    const int k0 = kt * kTileK + 32 * half;
     uint32_t out[16];
-    decode_half_row(records + static_cast<size_t>(r) * kRecordBytes, nl, half, base_exp[n], out);
+    const uint32_t base2 = base2_of(En);
+    decode_chunk16<false, 0>(v0, bq, base2, out);
+    decode_chunk16<false, 1>(v1, bq, base2, out + 8);
     if (n < N) {
         const uint32_t emask = esc_map[(nl * kTileK + 32 * half) >> 5];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
             if (k0 + 8 * g >= K) continue;
-            const uint4 ref = __ldg(reinterpret_cast<const uint4 *>(w_ref + static_cast<size_t>(n) * K + k0 + 8 * g));
-            const uint32_t rw[4] = {ref.x, ref.y, ref.z, ref.w};
+            const uint32_t rw[4] = {ref[g].x, ref[g].y, ref[g].z, ref[g].w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 const uint32_t diff = out[4 * g + q] ^ rw[q];
@@ -129,9 +130,12 @@ verify_kernel(const uint8_t *__restrict__ records, const uint8_t *__restrict__ b
             }
         }
     }
-    bad = block_sum256(bad);
-    entries = block_sum256(entries);
-    if (threadIdx.x == 0) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        bad += __shfl_xor_sync(0xFFFFFFFFu, bad, off);
+        entries += __shfl_xor_sync(0xFFFFFFFFu, entries, off);
+    }
+    if ((threadIdx.x & 31) == 0) {
         if (bad) atomicAdd(&counters[0], static_cast<unsigned long long>(bad));
         if (entries) atomicAdd(&counters[1], static_cast<unsigned long long>(entries));
     }
