@@ -182,11 +182,15 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     const int xbytes = p.npad * 128;
     constexpr int rbytes = kQView ? kViewBytes : kRecordBytes;
     constexpr int ebytes = kQView ? 0 : kEscCap * 4;
-    const int sbytes = RPS * (xbytes + rbytes) + ebytes;
+    // a slot's records are copied as one contiguous range: whole records, or for the Q view
+    // from the first record's view to the end of the last record's view (the B planes between
+    // them come along: one copy instead of one per record)
+    const int recs_bytes = (RPS - 1) * kRecordBytes + rbytes;
+    const int sbytes = RPS * xbytes + recs_bytes + ebytes;
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + S * sbytes);
     auto stage_x = [&](int s, int q) { return smem + s * sbytes + q * xbytes; };
-    auto stage_rec = [&](int s, int q) { return smem + s * sbytes + RPS * xbytes + q * rbytes; };
-    auto stage_esc = [&](int s) { return smem + s * sbytes + RPS * (xbytes + rbytes); };
+    auto stage_rec = [&](int s, int q) { return smem + s * sbytes + RPS * xbytes + q * kRecordBytes; };
+    auto stage_esc = [&](int s) { return smem + s * sbytes + RPS * xbytes + recs_bytes; };
 
     const int c = blockIdx.x;
     const int R = p.R, G = p.grid, KT = p.k_tiles, U = p.unit;
@@ -211,13 +215,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         const int s = pst.idx;
         const int nr = min(RPS, nrec - js * RPS);
         const uint32_t fb = smem_u32(&ctrl->full[s]);
-        mbar_arrive_expect_tx_elect(fb, nr * rbytes);
-        if (kQView) {  // the 8-bit views only: the B planes between them stay in memory
-            for (int q = 0; q < nr; ++q)
-                bulk_g2s_elect(smem_u32(stage_rec(s, q)), psrc + q * kRecordBytes, rbytes, fb);
-        } else {       // consecutive records are contiguous: one copy
-            bulk_g2s_elect(smem_u32(stage_rec(s, 0)), psrc, nr * rbytes, fb);
-        }
+        const uint32_t bytes = (nr - 1) * kRecordBytes + rbytes;  // consecutive records are contiguous
+        mbar_arrive_expect_tx_elect(fb, bytes);
+        bulk_g2s_elect(smem_u32(stage_rec(s, 0)), psrc, bytes, fb);
         psrc += nr * kRecordBytes;
         issued = js + 1;
         pst.advance(1, S);
@@ -900,7 +900,8 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     L->npad = (M + 15) / 16 * 16;
     // two records per ring slot while the activation tiles are small
     L->rps = (L->npad <= 64) ? 2 : 1;
-    const int sbytes = L->rps * (L->npad * 128 + (q ? kViewBytes : kRecordBytes)) + (q ? 0 : kEscCap * 4);
+    const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * kRecordBytes + (q ? kViewBytes : kRecordBytes) +
+                       (q ? 0 : kEscCap * 4);
     const int ctrl = static_cast<int>(align_up(sizeof(Ctrl), 1024));
     int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
     if (stages > kMaxStages) stages = kMaxStages;
