@@ -106,6 +106,7 @@ struct Params {
     int unit;  // records per unit of the work split: 1 (stream-K) or k_tiles (whole tiles)
     int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
     int y_tma;    // y is written by tiled tensor stores through ymap
+    int x_pair;   // xmap2 loads the k-slices of two consecutive records in one copy
     uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
     int R;  // records: n_tiles * k_tiles (< 2^22)
     void *y;
@@ -169,8 +170,8 @@ __device__ __forceinline__ void warp_top2(float &v1, int &i1, float &v2) {
 
 template <bool kQView, bool kArgmax>
 __global__ void __launch_bounds__(kThreads, 1)
-w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap ymap,
-                const Params p) {
+w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap2,
+                const __grid_constant__ CUtensorMap ymap, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -226,9 +227,16 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         const int nr = min(RPS, nrec - js * RPS);
         const uint32_t xb = smem_u32(&ctrl->xfull[s]);
         mbar_arrive_expect_tx_elect(xb, nr * xbytes);
-        for (int q = 0; q < nr; ++q) {
-            tma_2d_g2s_elect(smem_u32(stage_x(s, q)), &xmap, pkt * kTileK, 0, xb);
-            if (++pkt == p.k_tiles) pkt = 0;
+        if (p.x_pair && nr == 2 && pkt + 1 < p.k_tiles) {
+            // both records in one k tile pair: slices pkt and pkt+1 land as two adjacent tiles
+            tma_3d_g2s_elect(smem_u32(stage_x(s, 0)), &xmap2, 0, 0, pkt, xb);
+            pkt += 2;
+            if (pkt == p.k_tiles) pkt = 0;
+        } else {
+            for (int q = 0; q < nr; ++q) {
+                tma_2d_g2s_elect(smem_u32(stage_x(s, q)), &xmap, pkt * kTileK, 0, xb);
+                if (++pkt == p.k_tiles) pkt = 0;
+            }
         }
         xissued = js + 1;
     };
@@ -255,6 +263,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             ctrl->fix = 0;
             fence_barrier_init();
             prefetch_tensormap(&xmap);
+            prefetch_tensormap(&xmap2);
         }
         __syncwarp();
         pkt = r0 % KT;
@@ -951,8 +960,8 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
 }
 
 template <bool kQ, bool kA>
-w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &ymap, const Params &p, const Layout &L,
-                          bool overlap, cudaStream_t st) {
+w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const CUtensorMap &ymap, const Params &p,
+                          const Layout &L, bool overlap, cudaStream_t st) {
     auto kern = w12_gemm_kernel<kQ, kA>;
     // the opt-in shared-memory limit is set once per device (to the maximum any plan uses)
     static std::atomic<uint64_t> smem_set{0};
@@ -973,7 +982,7 @@ w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &ymap, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, ymap, p));
+    W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, map2, ymap, p));
     if (!kA && !L.whole && L.grid > 1) {
         cudaLaunchConfig_t rc{};
         rc.gridDim = dim3(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(p.M));
@@ -1012,6 +1021,22 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return W12_ERR_INVALID_ARG;
+    // x as (k within a slice, row, slice): one copy brings the slices of two consecutive records
+    // as two adjacent 128B-swizzled tiles. Needs whole slices (K % 64 == 0); the single-slice
+    // map above serves the other cases.
+    CUtensorMap map2 = map;
+    bool x_pair = false;
+    if (L.rps == 2 && t->K % kTileK == 0) {
+        const cuuint64_t dims3[3] = {static_cast<cuuint64_t>(kTileK), static_cast<cuuint64_t>(M),
+                                     static_cast<cuuint64_t>(t->K / kTileK)};
+        const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(t->K) * 2, static_cast<cuuint64_t>(kTileK) * 2};
+        const cuuint32_t box3[3] = {kTileK, static_cast<cuuint32_t>(L.npad), 2};
+        const cuuint32_t estr3[3] = {1, 1, 1};
+        x_pair = enc(&map2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(x), dims3, strides3, box3,
+                     estr3, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        if (!x_pair) map2 = map;
+    }
     // y as a 2-D tensor for the epilogue's tiled stores (boxes of 32 columns x 16 rows); plain
     // stores are used where the tensor map's alignment rules do not hold
     CUtensorMap ymap = map;
@@ -1051,6 +1076,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     // Tensor stores pay off when the blocks finish together (whole tiles); with split tiles
     // (stream-K) plain stores measured faster, so they are kept there.
     p.y_tma = (y_tma && L.whole) ? 1 : 0;
+    p.x_pair = x_pair ? 1 : 0;
     p.R = static_cast<int>(L.R);
     p.y = y;
     p.y_bf16 = (y_dtype == W12_OUT_BF16);
@@ -1064,10 +1090,10 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.gap = gap;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (q)
-        return argmax ? launch_variant<true, true>(map, ymap, p, L, overlap, st)
-                      : launch_variant<true, false>(map, ymap, p, L, overlap, st);
-    return argmax ? launch_variant<false, true>(map, ymap, p, L, overlap, st)
-                  : launch_variant<false, false>(map, ymap, p, L, overlap, st);
+        return argmax ? launch_variant<true, true>(map, map2, ymap, p, L, overlap, st)
+                      : launch_variant<true, false>(map, map2, ymap, p, L, overlap, st);
+    return argmax ? launch_variant<false, true>(map, map2, ymap, p, L, overlap, st)
+                  : launch_variant<false, false>(map, map2, ymap, p, L, overlap, st);
 }
 
 }  // namespace

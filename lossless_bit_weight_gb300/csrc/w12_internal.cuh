@@ -223,6 +223,16 @@ __device__ __forceinline__ void bulk_g2s_elect(uint32_t dst, const void *src, ui
         : "memory");
 }
 
+__device__ __forceinline__ void tma_3d_g2s_elect(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                                 uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
+        "@P cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];\n\t}"
+        ::"r"(dst), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_2d_g2s_elect(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\t"
