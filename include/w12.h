@@ -57,7 +57,7 @@ enum {
 };
 
 enum { W12_OUT_F32 = 0, W12_OUT_BF16 = 1 };          /* y element type */
-enum { W12_LAUNCH_OVERLAP = 1 };                     /* w12_gemm_ex flags */
+enum { W12_LAUNCH_OVERLAP = 1, W12_LAUNCH_TEST_STALL = 2 };  /* w12_gemm_ex flags */
 enum { W12_OP_GEMM = 0, W12_OP_QVIEW_GEMM = 1, W12_OP_ARGMAX = 2, W12_OP_QVIEW_ARGMAX = 3 };
 
 /*
@@ -180,6 +180,10 @@ w12_status w12_lmhead_argmax(const w12_tensor *t, const uint16_t *x, int M, int3
  * wait for this one before using its results, as kernels launched with this flag do.
  * The kernel's bounded waits give up after about a second, so the preceding kernel must not run
  * much longer than that after this launch begins.
+ * flags = W12_LAUNCH_TEST_STALL is a test hook for the failure path. Each block's producer fills
+ * only its first pipeline slot, so the block's bounded waits run out after about a second. Every
+ * block then stops, the call's outputs are invalid, and w12_check reports W12_ERR_TIMEOUT; the
+ * workspace must then be zero-filled again. Nothing else in the library sets it.
  * Asynchronous. */
 w12_status w12_gemm_ex(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, int y_dtype,
                        int32_t *idx, float *val, float *gap, unsigned flags, void *workspace,

@@ -107,6 +107,7 @@ struct Params {
     int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
     int y_tma;    // y is written by tiled tensor stores through ymap
     int x_pair;   // xmap2 loads the k-slices of two consecutive records in one copy
+    int test_stall;  // W12_LAUNCH_TEST_STALL: the producer fills only the first slot
     uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
     int R;  // records: n_tiles * k_tiles (< 2^22)
     void *y;
@@ -302,7 +303,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // Plain launch: each slot's records, then its tiles. Overlapped launch: the records of
         // every free slot first (they may load while the previous grid finishes), then the tiles
         // once it has (by then those record copies have drained).
-        const int n0 = min(S, nst);  // the first S slots start out free
+        // the first S slots start out free; under the test hook only the first is filled, so
+        // the block's bounded waits run out
+        const int n0 = p.test_stall ? min(1, nst) : min(S, nst);
         if (p.overlap) {
             for (int js = 1; js < n0; ++js) produce_rec(js);
             grid_dependency_wait();  // x may be the previous grid's output
@@ -314,7 +317,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                 produce_x(js, js);
             }
         }
-        for (int js = n0; js < nst; ++js) {
+        for (int js = n0; !p.test_stall && js < nst; ++js) {
             const int s = pst.idx;
             const bool ok = mbar_wait(smem_u32(&ctrl->empty[s]), pst.phase ^ 1, abort, p.err, kErrProducer);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
@@ -999,7 +1002,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
                int32_t *idx, float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream,
                unsigned flags = 0) {
     W12_TRY(check_tensor(t));
-    if (flags & ~static_cast<unsigned>(W12_LAUNCH_OVERLAP)) return W12_ERR_INVALID_ARG;
+    if (flags & ~static_cast<unsigned>(W12_LAUNCH_OVERLAP | W12_LAUNCH_TEST_STALL)) return W12_ERR_INVALID_ARG;
     const bool overlap = (flags & W12_LAUNCH_OVERLAP) != 0;
     if (!x || !aligned16(x) || !ws) return W12_ERR_INVALID_ARG;
     Layout L{};
@@ -1077,6 +1080,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     // (stream-K) plain stores measured faster, so they are kept there.
     p.y_tma = (y_tma && L.whole) ? 1 : 0;
     p.x_pair = x_pair ? 1 : 0;
+    p.test_stall = (flags & W12_LAUNCH_TEST_STALL) ? 1 : 0;
     p.R = static_cast<int>(L.R);
     p.y = y;
     p.y_bf16 = (y_dtype == W12_OUT_BF16);

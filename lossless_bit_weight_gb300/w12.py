@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libw12.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_MISMATCH, ERR_TIMEOUT, \
     ERR_DEVICE = range(8)
 OUT_F32, OUT_BF16 = 0, 1
-LAUNCH_OVERLAP = 1
+LAUNCH_OVERLAP, LAUNCH_TEST_STALL = 1, 2
 OP_GEMM, OP_QVIEW_GEMM, OP_ARGMAX, OP_QVIEW_ARGMAX = range(4)
 TILE_N, TILE_K, RECORD_BYTES, VIEW_BYTES, MAX_M = 128, 64, 12288, 8192, 256
 
@@ -221,12 +221,14 @@ def verify(t: W12Tensor, w_ref: torch.Tensor, stream=None) -> int:
 
 
 def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = False,
-         out: torch.Tensor | None = None, stream=None, overlap: bool = False) -> torch.Tensor:
+         out: torch.Tensor | None = None, stream=None, overlap: bool = False,
+         test_stall: bool = False) -> torch.Tensor:
     """y = x @ W^T over the exact weights (or the 8-bit view when ``qview``).
 
     ``overlap`` launches with ``W12_LAUNCH_OVERLAP`` (``w12_gemm_ex``): the kernel may start, and
     fetch and decode its weights, while the previous kernel on the stream finishes; t's buffers
-    must not be written by that kernel."""
+    must not be written by that kernel. ``test_stall`` sets the ``W12_LAUNCH_TEST_STALL`` test
+    hook (the bounded waits run out; ``check`` then raises)."""
     _bits(x)
     M = x.shape[0]
     if x.shape[1] != t.K:
@@ -236,9 +238,10 @@ def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = F
         out = torch.empty((M, t.N), dtype=out_dtype, device=x.device)
     op = OP_QVIEW_GEMM if qview else OP_GEMM
     ws, nb = t.workspace(M, op)
-    if overlap:
+    if overlap or test_stall:
+        flags = (LAUNCH_OVERLAP if overlap else 0) | (LAUNCH_TEST_STALL if test_stall else 0)
         _check(lib().w12_gemm_ex(ctypes.byref(t.c), _ptr(x), M, op, _ptr(out), ydt, None, None, None,
-                                 LAUNCH_OVERLAP, _ptr(ws), nb, _stream(stream)), "w12_gemm_ex")
+                                 flags, _ptr(ws), nb, _stream(stream)), "w12_gemm_ex")
         return out
     fn = lib().w12_qview_gemm if qview else lib().w12_gemm
     _check(fn(ctypes.byref(t.c), _ptr(x), M, _ptr(out), ydt, _ptr(ws), nb, _stream(stream)),

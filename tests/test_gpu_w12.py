@@ -268,3 +268,23 @@ def test_overlap_launch_chain_matches_plain(w12):
         assert torch.equal(a, b)
     w12.check(t1)
     w12.check(t2)
+
+
+def test_bounded_wait_timeout_is_reported(w12):
+    """The failure path, without a GPU fault: under the W12_LAUNCH_TEST_STALL hook each block's
+    producer fills only its first pipeline slot, the waits on the next slot give up after about a
+    second, every block stops, and w12_check reports W12_ERR_TIMEOUT. The context stays usable:
+    once the workspace is zero-filled again a normal call gives the right result."""
+    w = synth.weights(512, 256, synth.TINY, seed=31, device="cuda")
+    x = synth.activations(4, 256, seed=32, device="cuda")
+    t = w12.encode(w)
+    w12.gemm(t, x, test_stall=True)
+    with pytest.raises(w12.W12Error) as e:
+        w12.check(t)
+    assert e.value.status == w12.ERR_TIMEOUT
+    for ws, _ in t._ws.values():
+        ws.zero_()
+    y = w12.gemm(t, x)
+    y_ref, ad = oracle.gemm(to_np_u16(x), to_np_u16(w))
+    assert gemm_violations(y.cpu().numpy(), y_ref, ad) == 0
+    w12.check(t)
