@@ -311,23 +311,62 @@ def main():
                 for j, m in enumerate(MS)}
     traffic = profile_traffic()
 
-    # ---- end to end through the C ABI with host buffers (pinned), one sweep per step
+    # ---- end to end through the C ABI with host buffers (pinned), one sweep per step. Each
+    # launch's x comes from pinned host memory and its y goes back to pinned host memory. The
+    # copies run on two copy streams, double-buffered, so they overlap the GEMMs as a serving loop
+    # would. Ten steps (50 launches, 100 copies) are captured once in a CUDA graph: replaying it
+    # keeps the host's launch cost out of the way. The timed region holds whole replays.
+    nb2, cap_steps = 2, 10
     xh = {m: xs[m].cpu().pin_memory() for m in MS}
-    yh = {m: torch.empty((m, N_MLP), dtype=torch.float32).pin_memory() for m in MS}
-    xd = {m: torch.empty_like(xs[m]) for m in MS}
-    e2e_steps = max(3, min(args.steps, 400))
+    yh = {m: [torch.empty((m, N_MLP), dtype=torch.float32).pin_memory() for _ in range(nb2)] for m in MS}
+    xd = {m: [torch.empty_like(xs[m]) for _ in range(nb2)] for m in MS}
+    yd = {m: [torch.empty((m, N_MLP), dtype=torch.float32, device=dev) for _ in range(nb2)] for m in MS}
+    h2d_s, d2h_s, cap_s = (torch.cuda.Stream(device=dev) for _ in range(3))
+    n_l = cap_steps * len(MS)
+    x_ready, gemm_done, y_done = ([torch.cuda.Event() for _ in range(n_l)] for _ in range(3))
+
+    def pipeline():
+        cur = torch.cuda.current_stream()
+        h2d_s.wait_stream(cur)
+        d2h_s.wait_stream(cur)
+        for g in range(n_l):
+            m, b = MS[g % len(MS)], (g // len(MS)) % nb2
+            c = copies[g % n_copies]
+            with torch.cuda.stream(h2d_s):
+                if g >= len(MS) * nb2:
+                    h2d_s.wait_event(gemm_done[g - len(MS) * nb2])  # the GEMM that last read xd[m][b]
+                xd[m][b].copy_(xh[m], non_blocking=True)
+                x_ready[g].record(h2d_s)
+            cur.wait_event(x_ready[g])
+            if g >= len(MS) * nb2:
+                cur.wait_event(y_done[g - len(MS) * nb2])  # the copy that last read yd[m][b]
+            w12.gemm(c, xd[m][b], out=yd[m][b], overlap=overlap)
+            gemm_done[g].record(cur)
+            with torch.cuda.stream(d2h_s):
+                d2h_s.wait_event(gemm_done[g])
+                yh[m][b].copy_(yd[m][b], non_blocking=True)
+                y_done[g].record(d2h_s)
+        cur.wait_stream(h2d_s)
+        cur.wait_stream(d2h_s)
+
+    with torch.cuda.stream(cap_s):
+        pipeline()  # eager once: workspaces, kernel attributes
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap_s):
+            pipeline()
+    reps = max(2, min(args.steps, 400) // cap_steps)
+    e2e_steps = reps * cap_steps
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        for j, m in enumerate(MS):
-            c = copies[(i * len(MS) + j) % n_copies]
-            xd[m].copy_(xh[m], non_blocking=True)
-            w12.gemm(c, xd[m], out=ys[m], overlap=overlap)
-            yh[m].copy_(ys[m], non_blocking=True)
-    e1.record(stream)
+    with torch.cuda.stream(cap_s):
+        graph.replay()  # warm
+        e0.record(cap_s)
+        for _ in range(reps):
+            graph.replay()
+        e1.record(cap_s)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     e2e_value = job_gbs(bytes_per_call * len(MS) * e2e_steps, ws, e2e_ms)
@@ -346,7 +385,7 @@ def main():
                          f"(L2 {l2/1e6:.0f} MB)", "parallelism": f"replicas x{ws}",
                    "w12_bytes_per_call": bytes_per_call, "escapes": t0.n_esc},
         "frac_of_peak": round(value / ws / hbm_peak, 4), "peak_gbs": hbm_peak, "peak_kind": peak_kind,
-        "per_m": {str(m): {"us": round(per_m_us[m], 2),
+        "per_m_isolated": {str(m): {"us": round(per_m_us[m], 2),
                            "weight_gbs": round(bytes_per_call / (per_m_us[m] * 1e-6) / 1e9, 1),
                            "tflops": round(2 * m * N_MLP * K_HID / (per_m_us[m] * 1e-6) / 1e12, 2)}
                   for m in MS},

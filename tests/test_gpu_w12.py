@@ -288,3 +288,36 @@ def test_bounded_wait_timeout_is_reported(w12):
     y_ref, ad = oracle.gemm(to_np_u16(x), to_np_u16(w))
     assert gemm_violations(y.cpu().numpy(), y_ref, ad) == 0
     w12.check(t)
+
+
+def test_overlap_chain_in_cuda_graph(w12):
+    """GEMMs launched with W12_LAUNCH_OVERLAP inside a captured CUDA graph: a chain in which each
+    GEMM reads the previous one's output, stream-K shapes included (their reduce kernels become
+    graph nodes too). Replays give the eager plain-launch results bit for bit."""
+    w1 = synth.weights(1024, 2048, synth.PROJ, seed=41, device="cuda")  # stream-K: 8 tiles
+    w2 = synth.weights(2048, 1024, synth.PROJ, seed=42, device="cuda")
+    t1, t2 = w12.encode(w1), w12.encode(w2)
+    x = synth.activations(32, 2048, seed=43, device="cuda")
+
+    def chain(overlap):
+        a = w12.gemm(t1, x, out_dtype=torch.bfloat16, overlap=overlap)
+        b = w12.gemm(t2, a, out_dtype=torch.bfloat16, overlap=overlap)
+        c = w12.gemm(t1, b, overlap=overlap)
+        return c, w12.lmhead_argmax(t1, b, overlap=overlap)[0]
+
+    ref_y, ref_i = chain(False)
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        chain(True)  # workspaces and kernel attributes before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            gy, gi = chain(True)
+        for _ in range(3):
+            g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(gy.view(torch.int32), ref_y.view(torch.int32))
+    assert torch.equal(gi, ref_i)
+    w12.check(t1)
+    w12.check(t2)
