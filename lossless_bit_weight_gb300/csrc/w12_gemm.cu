@@ -38,6 +38,7 @@
 
 #include "w12_internal.cuh"
 
+
 namespace w12 {
 namespace {
 
@@ -106,6 +107,7 @@ struct Params {
     int unit;  // records per unit of the work split: 1 (stream-K) or k_tiles (whole tiles)
     int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
     int y_tma;    // y is written by tiled tensor stores through ymap
+    int v_tma;    // Q view: a slot's two record views arrive by one tiled copy through vmap
     int x_pair;   // xmap2 loads the k-slices of two consecutive records in one copy
     int test_stall;  // W12_LAUNCH_TEST_STALL: the producer fills only the first slot
     uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
@@ -172,7 +174,7 @@ __device__ __forceinline__ void warp_top2(float &v1, int &i1, float &v2) {
 template <bool kQView, bool kArgmax>
 __global__ void __launch_bounds__(kThreads, 1)
 w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap2,
-                const __grid_constant__ CUtensorMap ymap, const Params p) {
+                const __grid_constant__ CUtensorMap ymap, const __grid_constant__ CUtensorMap vmap, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,14 +186,16 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     const int xbytes = p.npad * 128;
     constexpr int rbytes = kQView ? kViewBytes : kRecordBytes;
     constexpr int ebytes = kQView ? 0 : kEscCap * 4;
-    // a slot's records are copied as one contiguous range: whole records, or for the Q view
-    // from the first record's view to the end of the last record's view (the B planes between
-    // them come along: one copy instead of one per record)
-    const int recs_bytes = (RPS - 1) * kRecordBytes + rbytes;
+    // A slot's records arrive by one copy: whole records as one contiguous range; for the Q view
+    // the two records' views by one tiled copy that skips the B planes between them (vmap), else
+    // the range from the first record's view to the end of the last one's.
+    const bool vtma = kQView && p.v_tma;
+    const int rstride = vtma ? kViewBytes : kRecordBytes;  // shared-memory distance between records
+    const int recs_bytes = (RPS - 1) * rstride + rbytes;
     const int sbytes = RPS * xbytes + recs_bytes + ebytes;
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + S * sbytes);
     auto stage_x = [&](int s, int q) { return smem + s * sbytes + q * xbytes; };
-    auto stage_rec = [&](int s, int q) { return smem + s * sbytes + RPS * xbytes + q * kRecordBytes; };
+    auto stage_rec = [&](int s, int q) { return smem + s * sbytes + RPS * xbytes + q * rstride; };
     auto stage_esc = [&](int s) { return smem + s * sbytes + RPS * xbytes + recs_bytes; };
 
     const int c = blockIdx.x;
@@ -217,9 +221,16 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         const int s = pst.idx;
         const int nr = min(RPS, nrec - js * RPS);
         const uint32_t fb = smem_u32(&ctrl->full[s]);
-        const uint32_t bytes = (nr - 1) * kRecordBytes + rbytes;  // consecutive records are contiguous
-        mbar_arrive_expect_tx_elect(fb, bytes);
-        bulk_g2s_elect(smem_u32(stage_rec(s, 0)), psrc, bytes, fb);
+        if (vtma) {
+            // the box always spans two records; past the last record it reads zeros, and a
+            // record past this block's range is read but not decoded
+            mbar_arrive_expect_tx_elect(fb, 2 * kViewBytes);
+            tma_3d_g2s_elect(smem_u32(stage_rec(s, 0)), &vmap, 0, 0, r0 + js * 2, fb);
+        } else {
+            const uint32_t bytes = (nr - 1) * kRecordBytes + rbytes;  // consecutive records are contiguous
+            mbar_arrive_expect_tx_elect(fb, bytes);
+            bulk_g2s_elect(smem_u32(stage_rec(s, 0)), psrc, bytes, fb);
+        }
         psrc += nr * kRecordBytes;
         issued = js + 1;
         pst.advance(1, S);
@@ -265,6 +276,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             fence_barrier_init();
             prefetch_tensormap(&xmap);
             prefetch_tensormap(&xmap2);
+            if (vtma) prefetch_tensormap(&vmap);
         }
         __syncwarp();
         pkt = r0 % KT;
@@ -281,6 +293,18 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     if (!kQView && warp == kWarpEscape) {
         esc_cur = esc_load(0);
         esc_nxt = esc_load(32);
+    }
+    // decode threads: their row's E_n for the block's first two tiles, requested before the
+    // set-up barrier so that these loads are not queued behind the first slots' record copies
+    const int en_row = 32 * (warp & 3) + lane;
+    auto en_load = [&](int tile) -> uint32_t {
+        return (tile < p.n_tiles) ? static_cast<uint32_t>(__ldg(p.base_exp + tile * kTileN + en_row)) : 0u;
+    };
+    int en_tile = r0 / KT;
+    uint32_t en_cur = 0, en_nxt = 0;
+    if (warp >= kWarpDec0) {
+        en_cur = en_load(en_tile);
+        en_nxt = en_load(en_tile + 1);
     }
     if (kArgmax) {
         for (int m = threadIdx.x; m < p.M; m += kThreads)
@@ -428,14 +452,15 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         const int qw = warp & 3;
         const int nl = 32 * qw + lane;
         const uint32_t m3 = p.m3, m15 = p.m15;
-        int cur_tile = -1;
-        uint32_t cur_base2 = 0;
+        // this row's E_n for tile en_tile (en_cur) and the tile after it (en_nxt): moving to the
+        // next tile takes the value already loaded and starts the load of the one after
         auto base2_for = [&](int tile) -> uint32_t {
-            if (tile != cur_tile) {
-                cur_tile = tile;
-                cur_base2 = base2_of(__ldg(p.base_exp + tile * kTileN + nl));
+            while (en_tile < tile) {
+                en_cur = en_nxt;
+                ++en_tile;
+                en_nxt = en_load(en_tile + 1);
             }
-            return cur_base2;
+            return base2_of(static_cast<int>(en_cur));
         };
         // decode this thread's row of record q of slot s into w (escapes patched)
         auto decode_record = [&](int s, int q, uint32_t base2, uint32_t (&w)[32]) {
@@ -898,6 +923,7 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 struct Layout {
     int npad, stages, rps, nacc, acc_cols, grid, unit, smem;
     bool whole;  // every block covers whole tiles (no partial sums)
+    bool vtma;   // Q view with two records per slot: views copied through a tensor map
     int64_t R;
     size_t ws_bytes, off_err, off_tile, off_done, off_part, off_top;
 };
@@ -912,22 +938,6 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     L->npad = (M + 15) / 16 * 16;
     // two records per ring slot while the activation tiles are small
     L->rps = (L->npad <= 64) ? 2 : 1;
-    const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * kRecordBytes + (q ? kViewBytes : kRecordBytes) +
-                       (q ? 0 : kEscCap * 4);
-    const int ctrl = static_cast<int>(align_up(sizeof(Ctrl), 1024));
-    int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
-    if (stages > kMaxStages) stages = kMaxStages;
-    // tensor memory: nacc accumulators of npad columns, then 32 columns per record in flight
-    // one accumulator set per MMA issuer (rps issuers), double-buffered when it fits
-    L->nacc = (2 * L->rps * L->npad + 4 * L->rps * kACols <= kTmemCols) ? 2 : 1;
-    L->acc_cols = L->rps * L->nacc * L->npad;
-    const int tmem_stages = (kTmemCols - L->acc_cols) / (L->rps * kACols);
-    if (stages > tmem_stages) stages = tmem_stages;
-    // every decode group needs a slot of its own (the slot-ordering argument in the decode loop)
-    if (stages < 2 || stages < kDecGroups) return W12_ERR_UNSUPPORTED_SHAPE;
-    L->stages = stages;
-    L->smem = 1024 + stages * sbytes + ctrl;
-    if (L->smem < kSmemFloor) L->smem = kSmemFloor;
     // Work split. Whole tiles per block when that balances within kTileSplitSlack: no tile is
     // then shared, so no partial sums and no cross-block fix-up at the end of the launch.
     // Otherwise stream-K: equal contiguous record ranges over one block per SM.
@@ -947,6 +957,25 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
         L->unit = 1;
         L->whole = false;
     }
+    // the view map needs a 16-byte aligned record array (records are 12 KB apart)
+    L->vtma = q && L->rps == 2 && aligned16(t->records);
+    const int rstride = L->vtma ? kViewBytes : kRecordBytes;
+    const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * rstride + (q ? kViewBytes : kRecordBytes) +
+                       (q ? 0 : kEscCap * 4);
+    const int ctrl = static_cast<int>(align_up(sizeof(Ctrl), 1024));
+    int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
+    if (stages > kMaxStages) stages = kMaxStages;
+    // tensor memory: nacc accumulators of npad columns, then 32 columns per record in flight
+    // one accumulator set per MMA issuer (rps issuers), double-buffered when it fits
+    L->nacc = (2 * L->rps * L->npad + 4 * L->rps * kACols <= kTmemCols) ? 2 : 1;
+    L->acc_cols = L->rps * L->nacc * L->npad;
+    const int tmem_stages = (kTmemCols - L->acc_cols) / (L->rps * kACols);
+    if (stages > tmem_stages) stages = tmem_stages;
+    // every decode group needs a slot of its own (the slot-ordering argument in the decode loop)
+    if (stages < 2 || stages < kDecGroups) return W12_ERR_UNSUPPORTED_SHAPE;
+    L->stages = stages;
+    L->smem = 1024 + stages * sbytes + ctrl;
+    if (L->smem < kSmemFloor) L->smem = kSmemFloor;
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -963,8 +992,8 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
 }
 
 template <bool kQ, bool kA>
-w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const CUtensorMap &ymap, const Params &p,
-                          const Layout &L, bool overlap, cudaStream_t st) {
+w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const CUtensorMap &ymap,
+                          const CUtensorMap &vmap, const Params &p, const Layout &L, bool overlap, cudaStream_t st) {
     auto kern = w12_gemm_kernel<kQ, kA>;
     // the opt-in shared-memory limit is set once per device (to the maximum any plan uses)
     static std::atomic<uint64_t> smem_set{0};
@@ -985,7 +1014,7 @@ w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = overlap ? 1 : 0;
-    W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, map2, ymap, p));
+    W12_CUDA(cudaLaunchKernelEx(&cfg, kern, map, map2, ymap, vmap, p));
     if (!kA && !L.whole && L.grid > 1) {
         cudaLaunchConfig_t rc{};
         rc.gridDim = dim3(static_cast<unsigned>(p.n_tiles), static_cast<unsigned>(p.M));
@@ -1055,6 +1084,20 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }
 
+    // the records as (4-byte word within a 1 KB row, row of the record, record): a box of 8 rows
+    // x 2 records is two consecutive records' views, landing back to back
+    CUtensorMap vmap = map;
+    if (L.vtma) {
+        const cuuint64_t vdims[3] = {256, kRecordBytes / 1024, static_cast<cuuint64_t>(L.R)};
+        const cuuint64_t vstrides[2] = {1024, kRecordBytes};
+        const cuuint32_t vbox[3] = {256, kViewBytes / 1024, 2};
+        const cuuint32_t vestr[3] = {1, 1, 1};
+        if (enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, t->records, vdims, vstrides, vbox, vestr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return W12_ERR_CUDA;
+    }
+
     uint8_t *w = static_cast<uint8_t *>(ws);
     Params p{};
     p.records = t->records;
@@ -1080,6 +1123,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     // (stream-K) plain stores measured faster, so they are kept there.
     p.y_tma = (y_tma && L.whole) ? 1 : 0;
     p.x_pair = x_pair ? 1 : 0;
+    p.v_tma = L.vtma ? 1 : 0;
     p.test_stall = (flags & W12_LAUNCH_TEST_STALL) ? 1 : 0;
     p.R = static_cast<int>(L.R);
     p.y = y;
@@ -1094,10 +1138,10 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.gap = gap;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (q)
-        return argmax ? launch_variant<true, true>(map, map2, ymap, p, L, overlap, st)
-                      : launch_variant<true, false>(map, map2, ymap, p, L, overlap, st);
-    return argmax ? launch_variant<false, true>(map, map2, ymap, p, L, overlap, st)
-                  : launch_variant<false, false>(map, map2, ymap, p, L, overlap, st);
+        return argmax ? launch_variant<true, true>(map, map2, ymap, vmap, p, L, overlap, st)
+                      : launch_variant<true, false>(map, map2, ymap, vmap, p, L, overlap, st);
+    return argmax ? launch_variant<false, true>(map, map2, ymap, vmap, p, L, overlap, st)
+                  : launch_variant<false, false>(map, map2, ymap, vmap, p, L, overlap, st);
 }
 
 }  // namespace

@@ -218,6 +218,14 @@ def test_qview_gemm(w12, M):
     assert gemm_violations(yv, y_ref, ad) == 0
 
 
+@pytest.mark.parametrize("N,K,M", [(1000, 448, 8), (2000, 320, 32), (4000, 192, 3), (640, 1344, 17)])
+def test_qview_gemm_odd_record_counts(w12, N, K, M):
+    """Q view where blocks hold odd numbers of records and tiles an odd number of k slices: a
+    slot's view copy then spans a record the block does not decode, or one past the last."""
+    _, _, _, yv, y_ref, ad = _gemm_case(w12, N, K, M, seed=N + K + M, qview=True)
+    assert gemm_violations(yv, y_ref, ad) == 0
+
+
 @pytest.mark.parametrize("N,K,M,qview", [(3000, 512, 32, False), (1000, 256, 1, False),
                                          (3000, 512, 64, True), (129, 64, 5, False)])
 def test_lmhead_argmax(w12, N, K, M, qview):
