@@ -54,7 +54,7 @@ constexpr int kWarpEscape = 2;
 constexpr int kWarpMma2 = 3;  // second MMA issuer (the second record of each slot)
 constexpr int kWarpEpi0 = 4;
 constexpr int kWarpDec0 = 8;
-constexpr int kEscCap = 512;       // escape entries staged per slot; more -> read from global
+constexpr int kEscCap = 128;       // index words staged per slot; more -> read from global
 constexpr int kACols = 32;         // tensor-memory columns of one decoded record (64 bf16/lane)
 constexpr int kMaxStages = 8;
 constexpr int kMaxM = 256;
@@ -357,6 +357,13 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // rest, and commits (or, without a record in the segment, just arrives on) accfull.
         const int mq = (warp == kWarpMma) ? 0 : 1;
         const uint32_t idesc = idesc_bf16_f32(128, p.npad);
+        // the slot's operands: its activation tile for this issuer (B, by descriptor; the
+        // descriptor's start-address field moves by sbytes / 16 per slot) and the issuer's
+        // decoded record (A, in tensor memory)
+        const uint64_t bdesc0 = smem_desc_sw128(smem_u32(stage_x(0, mq)));
+        const uint64_t bstep = static_cast<uint64_t>(sbytes >> 4);
+        const uint32_t a0 = a_slot(0, mq);
+        const uint32_t astep = static_cast<uint32_t>(RPS * kACols);
         Ring st;
         int js_next = 0;  // ring position of st: the slot of this issuer's next record
         int jseg = 0;
@@ -384,14 +391,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                     break;
                 }
                 tc_fence_after();
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(stage_x(s, mq)));
-                const uint32_t a = a_slot(s, mq);
                 // the issuer's first MMA of a segment overwrites its accumulator; the rest add
-                mma_bf16_ts_elect(d, a, bdesc, idesc, r != first ? 1u : 0u);
-                mma_bf16_ts_acc_elect(d, a + 8, bdesc + 2, idesc);
-                mma_bf16_ts_acc_elect(d, a + 16, bdesc + 4, idesc);
-                mma_bf16_ts_acc_elect(d, a + 24, bdesc + 6, idesc);
-                mma_commit_elect(smem_u32(&ctrl->empty[s]));
+                mma4_bf16_ts_elect(d, a0 + static_cast<uint32_t>(s) * astep, bdesc0 + static_cast<uint64_t>(s) * bstep,
+                                   idesc, r != first ? 1u : 0u, smem_u32(&ctrl->empty[s]));
                 issued = js + 1;
             }
             if (!ok) break;
@@ -967,7 +969,10 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     if (stages > kMaxStages) stages = kMaxStages;
     // tensor memory: nacc accumulators of npad columns, then 32 columns per record in flight
     // one accumulator set per MMA issuer (rps issuers), double-buffered when it fits
+    // (a block of one whole tile has a single segment: nothing to double-buffer, and the
+    // columns go to the ring instead)
     L->nacc = (2 * L->rps * L->npad + 4 * L->rps * kACols <= kTmemCols) ? 2 : 1;
+    if (L->whole && per == 1) L->nacc = 1;
     L->acc_cols = L->rps * L->nacc * L->npad;
     const int tmem_stages = (kTmemCols - L->acc_cols) / (L->rps * kACols);
     if (stages > tmem_stages) stages = tmem_stages;

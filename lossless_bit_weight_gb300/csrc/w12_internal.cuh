@@ -298,6 +298,28 @@ __device__ __forceinline__ void mma_bf16_ts_acc_elect(uint32_t d_tmem, uint32_t 
         : "memory");
 }
 
+// Four MMAs of one 128 x 64 record and the commit that tracks them, from one elected lane:
+// A = 32 tensor-memory columns from a_tmem (8 per K = 16 step), B = the 128B-swizzled activation
+// tile of b_desc (32 bytes, 2 in the descriptor's address field, per step). The first MMA
+// overwrites D unless `accumulate`.
+__device__ __forceinline__ void mma4_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate, uint32_t bar) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t.reg .pred A;\n\t.reg .pred T;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "setp.ne.b32 A, %4, 0;\n\t"
+        "setp.eq.u32 T, 1, 1;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, A;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %6, %3, T;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %3, T;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], %10, %3, T;\n\t"
+        "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate),
+          "r"(a_tmem + 8), "l"(b_desc + 2), "r"(a_tmem + 16), "l"(b_desc + 4), "r"(a_tmem + 24), "l"(b_desc + 6),
+          "r"(bar)
+        : "memory");
+}
+
 // Commit from the elected lane (the lane that issued the MMAs it must track).
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(
