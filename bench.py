@@ -497,24 +497,28 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
                          "plain_gbs": round(sweep_gbs(zc, xs, False), 1),
                          "overlap_gbs": round(sweep_gbs(zc, xs, True), 1)}
     del zc, tz
-    # cuBLAS bf16 on the same shapes, same cold-L2 treatment (rotating copies)
+    # cuBLAS bf16 on the same shapes, same cold-L2 treatment (rotating copies); every call here
+    # writes into a preallocated output, so the host keeps ahead of the GPU
     wcopies = [w] + [w.clone() for _ in range(2)]
+    yb = {m: torch.empty((m, N_MLP), dtype=torch.bfloat16, device=dev) for m in MS}
+    yf = {m: torch.empty((m, N_MLP), dtype=torch.float32, device=dev) for m in MS + (192,)}
     cub = {}
     for m in MS:
-        us = _time(lambda i: torch.nn.functional.linear(xs[m], wcopies[i % 3]), reps=15)
+        us = _time(lambda i, m=m: torch.matmul(xs[m], wcopies[i % 3].t(), out=yb[m]), reps=15)
         cub[str(m)] = round(us, 2)
     out["cublas_bf16_us"] = cub
     del wcopies
     n = len(copies)
     # the W12 GEMM timed the same way (back-to-back calls, rotating copies), both launch modes
-    out["w12_us"] = {mode: {str(m): round(_time(lambda i, m=m: w12.gemm(copies[i % n], xs[m], overlap=(mode == "overlap")),
+    out["w12_us"] = {mode: {str(m): round(_time(lambda i, m=m: w12.gemm(copies[i % n], xs[m], out=yf[m],
+                                                                        overlap=(mode == "overlap")),
                                                 reps=15), 2) for m in MS} for mode in ("plain", "overlap")}
     # Q view and M = 192 rows (the batched tree budget)
     x192 = synth.activations(192, K_HID, seed=synth.seed_for(4, 192), device=dev)
     n = len(copies)
-    q_us = _time(lambda i: w12.gemm(copies[i % n], xs[32], qview=True), reps=15)
-    e192 = _time(lambda i: w12.gemm(copies[i % n], x192), reps=15)
-    q192 = _time(lambda i: w12.gemm(copies[i % n], x192, qview=True), reps=15)
+    q_us = _time(lambda i: w12.gemm(copies[i % n], xs[32], out=yf[32], qview=True), reps=15)
+    e192 = _time(lambda i: w12.gemm(copies[i % n], x192, out=yf[192]), reps=15)
+    q192 = _time(lambda i: w12.gemm(copies[i % n], x192, out=yf[192], qview=True), reps=15)
     fl = 2 * 192 * N_MLP * K_HID
     out["qview"] = {"M32_us": round(q_us, 2), "M32_view_gbs": round(t0.gemm_bytes(True) / (q_us * 1e-6) / 1e9, 1),
                     "M192_us": round(q192, 2), "M192_tflops": round(fl / (q192 * 1e-6) / 1e12, 1)}
