@@ -545,62 +545,77 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
     return out
 
 
-def model_stream(dev, th, wh, Ms=(1, 32), steps=5):
-    """The weight stream of one decoding step of the synthetic 64-layer model: every linear
-    (q, k, v, o, gate, up, down) of 64 layers and the LM-head argmax, 449 GEMMs on fixed
-    activations (no glue between them), captured once in a CUDA graph and replayed; the same
-    sequence with bf16 cuBLAS on the unencoded weights beside it."""
+def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
+    """The weight stream of one decoding step of the synthetic 64-layer model: every linear of
+    64 layers and the LM-head argmax on fixed activations (no glue between them), captured once
+    in a CUDA graph and replayed; the same sequence with bf16 cuBLAS on the unencoded weights
+    beside it. Two layouts: the seven linears of a layer as listed (q, k, v, o, gate, up, down:
+    449 GEMMs), and with the linears that share an input concatenated at load time (q|k|v and
+    gate|up, as serving engines store them: 257 GEMMs). Concatenating output channels changes
+    no record: a W12 tensor of [Wq; Wk; Wv] holds the three tensors' records one after another."""
     from lossless_bit_weight_gb300 import w12
 
-    lin = []
-    for layer in range(64):
-        for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS):
-            wb = synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device=dev)
-            lin.append((w12.encode(wb), wb))
-    w12_bytes = sum(t.gemm_bytes() for t, _ in lin) + th.gemm_bytes()
-    bf16_bytes = sum(wb.numel() * 2 for _, wb in lin) + wh.numel() * 2
-    res = {"layers": 64, "gemms_per_step": len(lin) + 1, "w12_gb_per_step": round(w12_bytes / 1e9, 2),
-           "bf16_gb_per_step": round(bf16_bytes / 1e9, 2), "by_m": {}}
+    res = {"layers": 64, "by_layout": {}}
     stream = torch.cuda.Stream(device=dev)
-    for M in Ms:
-        xs = {k: synth.activations(M, k, seed=synth.seed_for(3, 7000 + k + M), device=dev) for k in (K_HID, 6144, N_MLP)}
-        ys = {(n, dt): torch.empty((M, n), dtype=dt, device=dev)
-              for n in (6144, 1024, K_HID, N_MLP) for dt in (torch.float32, torch.bfloat16)}
+    for layout in ("separate", "fused"):
+        lin = []
+        for layer in range(64):
+            ws = {name: synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device=dev)
+                  for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS)}
+            groups = ([["q"], ["k"], ["v"], ["o"], ["gate"], ["up"], ["down"]] if layout == "separate"
+                      else [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]])
+            for g in groups:
+                wb = ws[g[0]] if len(g) == 1 else torch.cat([ws[n] for n in g], dim=0)
+                lin.append((w12.encode(wb), wb))
+            del ws
+        w12_bytes = sum(t.gemm_bytes() for t, _ in lin) + th.gemm_bytes()
+        bf16_bytes = sum(wb.numel() * 2 for _, wb in lin) + wh.numel() * 2
+        row_l = {"gemms_per_step": len(lin) + 1, "w12_gb_per_step": round(w12_bytes / 1e9, 2),
+                 "bf16_gb_per_step": round(bf16_bytes / 1e9, 2), "by_m": {}}
+        n_outs = sorted({wb.shape[0] for _, wb in lin})
+        for M in Ms:
+            xs = {k: synth.activations(M, k, seed=synth.seed_for(3, 7000 + k + M), device=dev)
+                  for k in (K_HID, 6144, N_MLP)}
+            ys = {(n, dt): torch.empty((M, n), dtype=dt, device=dev)
+                  for n in n_outs for dt in (torch.float32, torch.bfloat16)}
 
-        def w12_step():
-            for t, _ in lin:
-                w12.gemm(t, xs[t.K], out=ys[(t.N, torch.float32)], overlap=True)
-            w12.lmhead_argmax(th, xs[K_HID], overlap=True)
+            def w12_step():
+                for t, _ in lin:
+                    w12.gemm(t, xs[t.K], out=ys[(t.N, torch.float32)], overlap=True)
+                w12.lmhead_argmax(th, xs[K_HID], overlap=True)
 
-        def cublas_step():
-            for _, wb in lin:
-                torch.matmul(xs[wb.shape[1]], wb.t(), out=ys[(wb.shape[0], torch.bfloat16)])
-            torch.argmax(torch.nn.functional.linear(xs[K_HID], wh), dim=1)
+            def cublas_step():
+                for _, wb in lin:
+                    torch.matmul(xs[wb.shape[1]], wb.t(), out=ys[(wb.shape[0], torch.bfloat16)])
+                torch.argmax(torch.nn.functional.linear(xs[K_HID], wh), dim=1)
 
-        row = {}
-        for name, fn in (("w12", w12_step), ("cublas_bf16", cublas_step)):
-            with torch.cuda.stream(stream):
-                fn()  # warm-up outside capture: workspaces, kernel attributes
-                torch.cuda.synchronize()
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=stream):
-                    fn()
-            with torch.cuda.stream(stream):  # a replay runs on the current stream
-                g.replay()
-                torch.cuda.synchronize()
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a.record(stream)
-                for _ in range(steps):
+            row = {}
+            for name, fn in (("w12", w12_step), ("cublas_bf16", cublas_step)):
+                with torch.cuda.stream(stream):
+                    fn()  # warm-up outside capture: workspaces, kernel attributes
+                    torch.cuda.synchronize()
+                    g = torch.cuda.CUDAGraph()
+                    with torch.cuda.graph(g, stream=stream):
+                        fn()
+                with torch.cuda.stream(stream):  # a replay runs on the current stream
                     g.replay()
-                b.record(stream)
-                b.synchronize()
-            ms = a.elapsed_time(b) / steps
-            nbytes = w12_bytes if name == "w12" else bf16_bytes
-            row[name] = {"ms_per_step": round(ms, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
-            del g
-        for t, _ in lin[:7]:
-            w12.check(t)
-        res["by_m"][str(M)] = row
+                    torch.cuda.synchronize()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(steps):
+                        g.replay()
+                    b.record(stream)
+                    b.synchronize()
+                ms = a.elapsed_time(b) / steps
+                nbytes = w12_bytes if name == "w12" else bf16_bytes
+                row[name] = {"ms_per_step": round(ms, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+                del g
+            for t, _ in lin[:7]:
+                w12.check(t)
+            row_l["by_m"][str(M)] = row
+        res["by_layout"][layout] = row_l
+        del lin
+        torch.cuda.empty_cache()
     return res
 
 
