@@ -171,6 +171,43 @@ __device__ __forceinline__ void warp_top2(float &v1, int &i1, float &v2) {
     }
 }
 
+// One halving step of the 16-row warp top-2 below: of rows [0, K) the lane keeps the upper half
+// if (lane & O), else the lower half, merges in its partner's (lane ^ O) copy of those rows and
+// stores them compacted at [0, K/2).
+template <int K, int O>
+__device__ __forceinline__ void top2_halve(float (&v1)[16], int (&i1)[16], float (&v2)[16], int lane) {
+    const bool up = (lane & O) != 0;
+#pragma unroll
+    for (int j = 0; j < K / 2; ++j) {
+        float kv1 = up ? v1[j + K / 2] : v1[j], kv2 = up ? v2[j + K / 2] : v2[j];
+        int ki1 = up ? i1[j + K / 2] : i1[j];
+        const float gv1 = up ? v1[j] : v1[j + K / 2], gv2 = up ? v2[j] : v2[j + K / 2];
+        const int gi1 = up ? i1[j] : i1[j + K / 2];
+        const float rv1 = __shfl_xor_sync(0xFFFFFFFFu, gv1, O);
+        const int ri1 = __shfl_xor_sync(0xFFFFFFFFu, gi1, O);
+        const float rv2 = __shfl_xor_sync(0xFFFFFFFFu, gv2, O);
+        top2_merge(kv1, ki1, kv2, rv1, ri1, rv2);
+        v1[j] = kv1;
+        i1[j] = ki1;
+        v2[j] = kv2;
+    }
+}
+
+// Top-2 over the warp's 32 columns of each of 16 rows, lane l holding column l of every row
+// (v1 = value, i1 = its index, v2 = -inf on entry). Recursive halving: after the steps on lane
+// bits 4..1 lane l holds row l >> 1 over the 16 lanes that share those bits; one exchange with
+// lane l ^ 1 completes it. 15 row exchanges instead of 16 five-step reductions.
+__device__ __forceinline__ void warp_top2_rows16(float (&v1)[16], int (&i1)[16], float (&v2)[16], int lane) {
+    top2_halve<16, 16>(v1, i1, v2, lane);
+    top2_halve<8, 8>(v1, i1, v2, lane);
+    top2_halve<4, 4>(v1, i1, v2, lane);
+    top2_halve<2, 2>(v1, i1, v2, lane);
+    const float rv1 = __shfl_xor_sync(0xFFFFFFFFu, v1[0], 1);
+    const int ri1 = __shfl_xor_sync(0xFFFFFFFFu, i1[0], 1);
+    const float rv2 = __shfl_xor_sync(0xFFFFFFFFu, v2[0], 1);
+    top2_merge(v1[0], i1[0], v2[0], rv1, ri1, rv2);
+}
+
 template <bool kQView, bool kArgmax>
 __global__ void __launch_bounds__(kThreads, 1)
 w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap2,
@@ -628,6 +665,24 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                 return;
             }
           }
+          if constexpr (kArgmax) {
+            if (!part) {
+                // this warp's top-2 of each of the 16 rows, into wtop[qw][m]
+                const int n = tile * kTileN + nl;
+                float v1[16], v2[16];
+                int i1[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    v1[i] = (n < p.N && !isnan(f[i])) ? f[i] : -INFINITY;
+                    i1[i] = n;
+                    v2[i] = -INFINITY;
+                }
+                warp_top2_rows16(v1, i1, v2, lane);
+                const int m = m0 + (lane >> 1);
+                if ((lane & 1) == 0 && m < M) ctrl->wtop[qw][m] = make_float4(v1[0], __int_as_float(i1[0]), v2[0], 0.f);
+                return;
+            }
+          }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 if (m0 + i >= M) break;
@@ -824,17 +879,32 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             }
             named_bar_sync(kEpiBar, 128);
             if (ctrl->fix) {
+                // The last block merges every block's top-2 of each row. Warp qw takes rows qw,
+                // qw + 4, ...; its lanes load the blocks' top-2s 32 apart, kPer at a time with all
+                // loads in flight together, and a shuffle tree merges the lanes. The top-2 of a
+                // set does not depend on the merge order (equal values go to the smaller index).
                 __threadfence();
-                for (int m = et; m < M; m += 128) {
+                constexpr int kPer = 8;
+                for (int m = qw; m < M; m += 4) {
                     float v1 = -INFINITY, v2 = -INFINITY;
                     int i1 = 0x7FFFFFFF;
-                    for (int cc = 0; cc < G; ++cc) {
-                        const float4 o = __ldcg(p.cta_top + static_cast<size_t>(cc) * M + m);
-                        top2_merge(v1, i1, v2, o.x, __float_as_int(o.y), o.z);
+                    for (int c0 = 0; c0 < G; c0 += 32 * kPer) {
+                        float4 o[kPer];
+#pragma unroll
+                        for (int k = 0; k < kPer; ++k) {
+                            const int cc = c0 + lane + 32 * k;
+                            o[k] = (cc < G) ? __ldcg(p.cta_top + static_cast<size_t>(cc) * M + m)
+                                            : make_float4(-INFINITY, __int_as_float(0x7FFFFFFF), -INFINITY, 0.f);
+                        }
+#pragma unroll
+                        for (int k = 0; k < kPer; ++k) top2_merge(v1, i1, v2, o[k].x, __float_as_int(o[k].y), o[k].z);
                     }
-                    p.idx[m] = i1;
-                    p.val[m] = v1;
-                    p.gap[m] = v1 - v2;
+                    warp_top2(v1, i1, v2);
+                    if (lane == 0) {
+                        p.idx[m] = i1;
+                        p.val[m] = v1;
+                        p.gap[m] = v1 - v2;
+                    }
                 }
                 if (et == 0) *p.done_cnt = 0;
             }
