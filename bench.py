@@ -536,10 +536,15 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
     xh = synth.activations(32, K_HID, seed=synth.seed_for(2, 1), device=dev)
     # the head (1.17 GB encoded, 1.56 GB bf16) is far larger than L2: no rotation needed
     a_us = _time(lambda i: w12.lmhead_argmax(th, xh), reps=10)
+    ao_us = _time(lambda i: w12.lmhead_argmax(th, xh, overlap=True), reps=10)
+    q_us = _time(lambda i: w12.lmhead_argmax(th, xh, qview=True, overlap=True), reps=10)
     c_us = _time(lambda i: torch.argmax(torch.nn.functional.linear(xh, wh), dim=1), reps=10)
     w12.check(th)
     out["lmhead"] = {"M": 32, "us": round(a_us, 1), "rows_per_s": round(32 / (a_us * 1e-6), 1),
                      "weight_gbs": round(th.gemm_bytes() / (a_us * 1e-6) / 1e9, 1),
+                     "overlap_us": round(ao_us, 1), "overlap_rows_per_s": round(32 / (ao_us * 1e-6), 1),
+                     "overlap_weight_gbs": round(th.gemm_bytes() / (ao_us * 1e-6) / 1e9, 1),
+                     "qview_overlap_us": round(q_us, 1),
                      "cublas_linear_argmax_us": round(c_us, 1)}
     out["model_stream"] = model_stream(dev, th, wh)
     return out
