@@ -57,6 +57,8 @@ def _load():
         lib.w12o_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.w12o_bf16_to_double.restype = ctypes.c_double
         lib.w12o_threads.restype = i32
+        lib.w12o_head_q8.argtypes = [P, i32, i32, P, P, P, P]
+        lib.w12o_certified_argmax.argtypes = [P, i32, P, i32, i32, P, P, P, P, P, P, P]
         _lib = lib
     return _lib
 
@@ -195,3 +197,40 @@ def threads() -> int:
 
 def bf16_to_double(u: int) -> float:
     return float(_load().w12o_bf16_to_double(int(u)))
+
+
+@dataclass
+class HeadQ8:
+    """The certified head's INT8 copy (SpecPilot §4.1 "Certified LM head"), row-major."""
+
+    scale: np.ndarray  # float32 [N]: s_n
+    q: np.ndarray      # int8 [N, K]: round-half-even(w / s_n), clamped to +-127
+    resid: np.ndarray  # float64 [N]: ||w_n - s_n q_n||_2 (+inf for a row with Inf or NaN)
+    qnorm: np.ndarray  # float64 [N]: ||q_n||_2
+
+
+def head_q8(w) -> HeadQ8:
+    """Per-row INT8 quantisation of the head with its residual norms."""
+    w = _u16(w)
+    N, K = w.shape
+    scale = np.zeros(N, np.float32)
+    q = np.zeros((N, K), np.int8)
+    resid = np.zeros(N, np.float64)
+    qnorm = np.zeros(N, np.float64)
+    _load().w12o_head_q8(_p(w), N, K, _p(scale), _p(q), _p(resid), _p(qnorm))
+    return HeadQ8(scale, q, resid, qnorm)
+
+
+def certified_argmax(x, w, h: HeadQ8):
+    """The certified argmax per row, fp64 from its definition: survivors of the Cauchy-Schwarz
+    bound rescored exactly. Returns (idx int32[M], val f64[M], gap f64[M], survivors int64[M])."""
+    x, w = _u16(x), _u16(w)
+    M, K = x.shape
+    N = w.shape[0]
+    idx = np.zeros(M, np.int32)
+    val = np.zeros(M, np.float64)
+    gap = np.zeros(M, np.float64)
+    cnt = np.zeros(M, np.int64)
+    _load().w12o_certified_argmax(_p(x), M, _p(w), N, K, _p(h.scale), _p(np.ascontiguousarray(h.q)),
+                                  _p(h.resid), _p(idx), _p(val), _p(gap), _p(cnt))
+    return idx, val, gap, cnt

@@ -18,6 +18,8 @@
  *   - greedy argmax: [SP] §2.1 "Speculative Decoding".
  *   - Q view (A+E only, dropped mantissa bits at their midpoint): [SP] §4.3 "Zero-copy Q pass",
  *     Fig. 7.
+ *   - certified LM head (INT8 copy, per-row Cauchy-Schwarz bound, exact rescoring of the
+ *     survivors): [SP] §4.1 "Certified LM head".
  *
  * Physical details the pages leave open (window tie rule, placeholders, byte and nibble order,
  * per-record escape index) follow the build's written W12 specification; every function states
@@ -351,3 +353,112 @@ int w12o_threads(void) { return omp_get_max_threads(); }
 #else
 int w12o_threads(void) { return 1; }
 #endif
+
+/* ---- certified LM head: an INT8 copy with a per-row error bound -----------------------------
+ * [SP] §4.1 "Certified LM head": an INT8 copy of the head whose per-row Cauchy-Schwarz error
+ * bound discards every token that provably cannot be the argmax; the survivors are rescored
+ * exactly, and the full head runs when too many survive. The pages give no formulas; this is
+ * the plainest reading, in the build's written specification:
+ *   scale   s_n = fp32(max_k |w[n,k]| / 127)   (0 for an all-zero row)
+ *   code    q[n,k] = round-half-even(w[n,k] / s_n), clamped to [-127, 127]
+ *   residual c_n = || w[n,:] - s_n q[n,:] ||_2          (+inf if the row holds Inf or NaN)
+ *   approx  yh[m,n] = s_n sum_k x[m,k] q[n,k]
+ *   bound   |y[m,n] - yh[m,n]| <= ||x[m,:]||_2 c_n       (Cauchy-Schwarz)
+ *   L_m     = second largest of yh[m,n] - ||x_m|| c_n over n (the best lower bound's runner-up)
+ *   survivors S_m = { n : yh[m,n] + ||x_m|| c_n >= L_m }: they hold the exact top-1 and top-2
+ *   result  the exact argmax and top-1/top-2 gap of y over S_m (equal to those over all n).
+ */
+
+/* per row: scale, codes (row-major int8), residual norm c_n and code norm ||q_n|| */
+void w12o_head_q8(const uint16_t *w, int N, int K, float *scale, int8_t *q, double *resid,
+                  double *qnorm) {
+    #pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        const uint16_t *row = w + (size_t)n * K;
+        int finite = 1;
+        double amax = 0.0;
+        for (int k = 0; k < K; ++k) {
+            if (bf_exp(row[k]) == 255) finite = 0;
+            double a = fabs(w12o_bf16_to_double(row[k]));
+            if (a > amax) amax = a;
+        }
+        int8_t *qr = q + (size_t)n * K;
+        if (!finite || amax == 0.0) {
+            scale[n] = 0.0f;
+            for (int k = 0; k < K; ++k) qr[k] = 0;
+            resid[n] = finite ? 0.0 : INFINITY;
+            qnorm[n] = 0.0;
+            continue;
+        }
+        const float s = (float)(amax / 127.0);
+        const double sd = (double)s;
+        double e2 = 0.0, q2 = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double wk = w12o_bf16_to_double(row[k]);
+            double t = nearbyint(wk / sd);  /* the default rounding mode: to nearest, ties to even */
+            if (t > 127.0) t = 127.0;
+            if (t < -127.0) t = -127.0;
+            qr[k] = (int8_t)t;
+            double e = wk - sd * t;         /* exact: both terms are exact in fp64 */
+            e2 += e * e;
+            q2 += t * t;
+        }
+        scale[n] = s;
+        resid[n] = sqrt(e2);
+        qnorm[n] = sqrt(q2);
+    }
+}
+
+/* The certified argmax of each row, in fp64 from its definition above. x: bf16 [M,K]; w: bf16
+ * [N,K] (the exact head, for rescoring); scale, q, resid: from w12o_head_q8. Returns the
+ * survivor count per row; idx/val/gap are the argmax over the survivors (exact y). */
+void w12o_certified_argmax(const uint16_t *x, int M, const uint16_t *w, int N, int K,
+                           const float *scale, const int8_t *q, const double *resid,
+                           int32_t *idx, double *val, double *gap, int64_t *n_surv) {
+    double *yh = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    for (int m = 0; m < M; ++m) {
+        const uint16_t *xm = x + (size_t)m * K;
+        double xn2 = 0.0;
+        for (int k = 0; k < K; ++k) {
+            double a = w12o_bf16_to_double(xm[k]);
+            xn2 += a * a;
+        }
+        const double xn = sqrt(xn2);
+        #pragma omp parallel for schedule(static)
+        for (int n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k) acc += w12o_bf16_to_double(xm[k]) * (double)q[(size_t)n * K + k];
+            yh[n] = (double)scale[n] * acc;
+        }
+        /* the two largest lower bounds */
+        double l1 = -INFINITY, l2 = -INFINITY;
+        for (int n = 0; n < N; ++n) {
+            double lb = yh[n] - xn * resid[n];
+            if (lb > l1) { l2 = l1; l1 = lb; }
+            else if (lb > l2) l2 = lb;
+        }
+        int best = -1;
+        double bv = -INFINITY, second = -INFINITY;
+        int64_t cnt = 0;
+        for (int n = 0; n < N; ++n) {
+            if (!(yh[n] + xn * resid[n] >= l2)) continue;
+            ++cnt;
+            double y = 0.0;
+            for (int k = 0; k < K; ++k)
+                y += w12o_bf16_to_double(xm[k]) * w12o_bf16_to_double(w[(size_t)n * K + k]);
+            if (isnan(y)) y = -INFINITY;  /* the GEMM argmax's rule: a NaN logit never wins */
+            if (best < 0 || y > bv) {
+                if (best >= 0) second = bv > second ? bv : second;
+                best = n;
+                bv = y;
+            } else if (y > second) {
+                second = y;
+            }
+        }
+        idx[m] = best;
+        val[m] = bv;
+        gap[m] = bv - second;
+        n_surv[m] = cnt;
+    }
+    free(yh);
+}

@@ -7,7 +7,10 @@
 - hand-derived bytes of a small ragged tensor (tests/golden/w12_layout_fixture.txt);
 - the fp64 GEMM against exact rational sums; the argmax against Python's own max over rows;
 - the Q view (SpecPilot §4.3) against value-level properties and against a second route through
-  the encoded records.
+  the encoded records;
+- the certified LM head (SpecPilot §4.1): quantisation properties of the INT8 copy, the
+  Cauchy-Schwarz bound against the exact GEMM, and the certified argmax against the brute-force
+  argmax over the whole head (random heads, exact ties, Inf rows).
 """
 import math
 import os
@@ -308,3 +311,100 @@ def test_qview_equals_decode_of_truncated_records(orc):
     e2 = orc.Encoded(e.N, e.K, rec.reshape(-1), e.base_exp, e.esc_off, e.esc_k[:0],
                      e.esc_bits[:0], np.zeros_like(e.rec_esc_off), e.rec_esc[:0])
     assert np.array_equal(orc.decode(e2), orc.qview_weights(w))
+
+
+# ---------------------------------------------------------------- certified LM head (SpecPilot §4.1)
+
+
+def _head(N, K, seed):
+    return synth.weights(N, K, synth.HEAD, seed=seed).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_head_q8_quantisation_properties(orc):
+    """Codes lie in [-127, 127]; the largest |w| of a row codes to +-127; every in-range weight
+    is within half a step of its code; the scale is the row maximum over 127 in fp32; zero rows
+    and rows holding Inf/NaN get scale 0 (the latter with an infinite residual)."""
+    w = _head(64, 96, seed=4)
+    w[3] = 0                      # all-zero row
+    w[5, 7] = 0x7F80              # +Inf
+    w[6, 9] = 0x7FC1              # NaN
+    w[7, :] = 0x3F80              # all 1.0
+    h = orc.head_q8(w)
+    v = bf16_values(w)
+    assert np.all(np.abs(h.q.astype(np.int32)) <= 127)
+    for n in range(64):
+        if n in (5, 6):
+            assert h.scale[n] == 0 and math.isinf(h.resid[n]) and not np.any(h.q[n])
+            continue
+        amax = np.abs(v[n]).max()
+        if amax == 0:
+            assert h.scale[n] == 0 and h.resid[n] == 0 and not np.any(h.q[n])
+            continue
+        assert h.scale[n] == np.float32(amax / 127.0)
+        s = float(h.scale[n])
+        e = v[n] - s * h.q[n].astype(np.float64)
+        assert np.all(np.abs(e) <= s / 2 * (1 + 1e-12) + abs(amax - 127 * s))
+        k = int(np.argmax(np.abs(v[n])))
+        assert abs(int(h.q[n, k])) == 127
+        assert h.resid[n] == pytest.approx(float(np.sqrt(np.sum(e * e))), rel=1e-12, abs=1e-300)
+    # all 1.0: every code is 127 and the residual is the fp32 scale's own rounding error
+    s7 = float(h.scale[7])
+    assert np.all(h.q[7] == 127) and h.resid[7] == pytest.approx(math.sqrt(96) * abs(1 - 127 * s7), rel=1e-9)
+
+
+def test_certified_bound_holds(orc):
+    """|y - yh| <= ||x|| c_n for every logit: the exact fp64 GEMM on one side, s_n (x . q_n) on
+    the other (numpy), the residual norm from the oracle."""
+    w = _head(500, 256, seed=8)
+    x = synth.activations(6, 256, seed=9).view(torch.int16).numpy().view(np.uint16)
+    h = orc.head_q8(w)
+    y, _ = orc.gemm(x, w)
+    xv = bf16_values(x)
+    yh = (xv @ h.q.astype(np.float64).T) * h.scale.astype(np.float64)[None, :]
+    bound = np.linalg.norm(xv, axis=1)[:, None] * h.resid[None, :]
+    assert np.all(np.abs(y - yh) <= bound * (1 + 1e-9))
+    # and it is not vacuous: on these Gaussian rows it is under a tenth of the logits' spread
+    assert np.median(bound) < 0.1 * np.std(y) * math.sqrt(256)
+
+
+@pytest.mark.parametrize("N,K,M,seed", [(3000, 256, 8, 1), (2000, 192, 5, 2), (1, 64, 3, 3), (2, 64, 2, 4)])
+def test_certified_argmax_equals_full_argmax(orc, N, K, M, seed):
+    """The survivors always hold the exact top-1 and top-2, so the certified result equals the
+    argmax and gap over the whole head (brute force over the fp64 GEMM)."""
+    w = _head(N, K, seed=seed)
+    x = synth.activations(M, K, seed=seed + 50).view(torch.int16).numpy().view(np.uint16)
+    h = orc.head_q8(w)
+    idx, val, gap, cnt = orc.certified_argmax(x, w, h)
+    y, _ = orc.gemm(x, w)
+    ridx, rval, rgap, _ = orc.argmax(y)
+    assert np.array_equal(idx, ridx)
+    assert np.array_equal(val, rval)
+    if N > 1:
+        assert np.array_equal(gap, rgap)
+    assert np.all(cnt >= min(N, 2)) and np.all(cnt <= N)
+    if N >= 1000:
+        assert np.all(cnt < N // 10)  # the bound discards most of a Gaussian head
+
+
+def test_certified_argmax_ties_and_special_rows(orc):
+    """Duplicate rows tie exactly (the smaller index wins, gap 0); a row with +Inf wins where its
+    logit is +Inf; an all-zero row is an ordinary candidate."""
+    w = _head(400, 128, seed=11)
+    w[17] = w[250]                 # exact duplicates
+    w[30] = 0
+    w[99, 5] = 0x7F80              # +Inf weight
+    x = synth.activations(4, 128, seed=12).view(torch.int16).numpy().view(np.uint16)
+    xv = bf16_values(x)
+    # make row 250 (and 17) the winner of row 0 by aligning it with x[0]
+    w[250] = np.where(xv[0] > 0, 0x3C00, 0xBC00).astype(np.uint16)  # +-2^-7
+    w[17] = w[250]
+    h = orc.head_q8(w)
+    idx, val, gap, cnt = orc.certified_argmax(x, w, h)
+    y, _ = orc.gemm(x, w)
+    ridx, rval, rgap, _ = orc.argmax(y)
+    assert idx[0] == 17 and gap[0] == 0.0
+    for m in range(4):
+        if math.isinf(rval[m]):
+            assert idx[m] == 99 and val[m] == rval[m]
+        else:
+            assert idx[m] == ridx[m] and val[m] == rval[m] and gap[m] == rgap[m]
