@@ -216,6 +216,55 @@ w12_status w12_check(void *workspace, size_t workspace_bytes, w12_stream_t strea
 w12_status w12_gemm_config(const w12_tensor *t, int M, int op, int *grid, int *stages,
                            int *smem_bytes);
 
+/* ---- certified LM head (SpecPilot §4.1 "Certified LM head") ------------------------------
+ * An INT8 copy of the head whose per-row Cauchy-Schwarz bound discards every token that
+ * provably cannot be the argmax; the survivors are rescored exactly from the W12 head, and when
+ * a row has too many survivors the full W12 argmax runs instead. The argmax and the top-1/top-2
+ * gap are those of the whole head.
+ *
+ * The copy, per output row n of the bf16 head W [N, K] (the readings the pages leave open):
+ *   scale[n] = max_k |W[n,k]| / 127 rounded to fp32 (0 for an all-zero row, a padding row, or a
+ *              row holding Inf or NaN)
+ *   q[n,k]   = W[n,k] / scale[n] rounded to the nearest integer (ties to even), clamped to +-127,
+ *              stored as a sign-magnitude byte (bit 7 sign, bits 0-6 |q|) in 128 x 64 records of
+ *              8192 bytes laid out like the W12 record's 8-bit view: record r = nt * k_tiles + kt,
+ *              byte 2048 * (k_l >> 4) + 16 * n_l + (k_l & 15)
+ *   bound[n] = an fp32 upper bound on ||W[n,:] - scale[n] q[n,:]||_2 plus the fp32 evaluation
+ *              margin of scale[n] (x . q[n,:]); +inf for a row holding Inf or NaN
+ * For a row x the certified logit interval is scale[n] (x . q[n,:]) -+ ||x||_2 bound[n].
+ */
+typedef struct {
+    int32_t N, K;
+    int32_t n_tiles, k_tiles;
+    uint8_t *codes;  /* [n_tiles * k_tiles * 8192] */
+    float *scale;    /* [n_tiles * 128] */
+    float *bound;    /* [n_tiles * 128] */
+} w12_q8_head;
+
+enum { W12_Q8_RECORD_BYTES = 8192, W12_Q8_MAX_SURVIVORS = 4096 };
+
+/* Fills h->N, K, n_tiles, k_tiles and returns the byte sizes of codes and of scale / bound.
+ * Host only. */
+w12_status w12_q8_shape(int N, int K, w12_q8_head *h, size_t *codes_bytes, size_t *row_bytes);
+
+/* Builds the copy from the bf16 head w [h->N, h->K] (device, row-major, 16-byte aligned) into
+ * the caller's buffers. Asynchronous on `stream`. */
+w12_status w12_q8_build(const uint16_t *w, const w12_q8_head *h, w12_stream_t stream);
+
+/* Workspace bytes of w12_lmhead_certified for t (the W12 head), h and M rows. The workspace
+ * must be zero-filled once; every call leaves it zeroed. Host only. */
+w12_status w12_certified_workspace_size(const w12_tensor *t, const w12_q8_head *h, int M, size_t *bytes);
+
+/* idx / val / gap (device, [M]) as w12_lmhead_argmax returns them, through the certified head;
+ * survivors (device, [M], may be NULL) receives each row's survivor count. t and h must
+ * describe the same head (same N, K). M in [1, W12_MAX_M]. If a row has more than
+ * W12_Q8_MAX_SURVIVORS survivors, the full W12 argmax produces every row's result.
+ * Asynchronous on `stream`: four kernels, then the full argmax, which does nothing unless a row
+ * overflowed. */
+w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_head *h, const uint16_t *x, int M,
+                                int32_t *idx, float *val, float *gap, int32_t *survivors, void *workspace,
+                                size_t workspace_bytes, w12_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -108,6 +108,8 @@ struct Params {
     int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
     int y_tma;    // y is written by tiled tensor stores through ymap
     int v_tma;    // Q view: a slot's two record views arrive by one tiled copy through vmap
+    const float *row_scale;  // INT8 copy: per-channel scale, [n_tiles * 128]
+    int *run_flag;           // if set, the launch does nothing unless *run_flag != 0 (then clears it)
     int x_pair;   // xmap2 loads the k-slices of two consecutive records in one copy
     int test_stall;  // W12_LAUNCH_TEST_STALL: the producer fills only the first slot
     uint32_t m3, m15;  // 8 and 32768: decode multipliers, given at run time (see decode_pair)
@@ -208,26 +210,34 @@ __device__ __forceinline__ void warp_top2_rows16(float (&v1)[16], int (&i1)[16],
     top2_merge(v1[0], i1[0], v2[0], rv1, ri1, rv2);
 }
 
-template <bool kQView, bool kArgmax>
+// kQ8: the certified head's INT8 copy (8 KB records of sign-magnitude codes, no escapes; each
+// output channel's accumulator is multiplied by its row scale)
+template <bool kQView, bool kArgmax, bool kQ8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap2,
                 const __grid_constant__ CUtensorMap ymap, const __grid_constant__ CUtensorMap vmap, const Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a conditional launch (the certified head's fallback) that is not needed ends here, before
+    // any barrier, copy or tensor memory is touched; the flag was written by an earlier kernel
+    // on the stream, which has completed (this launch is stream-ordered)
+    if (p.run_flag && *reinterpret_cast<volatile int *>(p.run_flag) == 0) return;
     // the next grid on the stream may start as soon as SMs free up; it waits for this grid's
     // completion itself before it reads activations or its workspace
     grid_launch_dependents();
 
     const int S = p.stages, RPS = p.rps;
     const int xbytes = p.npad * 128;
+    static_assert(!kQ8 || (kQView && !kArgmax), "the INT8 copy is read as a plain GEMM");
     constexpr int rbytes = kQView ? kViewBytes : kRecordBytes;
     constexpr int ebytes = kQView ? 0 : kEscCap * 4;
+    constexpr int gstride = kQ8 ? kViewBytes : kRecordBytes;  // distance between records in memory
     // A slot's records arrive by one copy: whole records as one contiguous range; for the Q view
     // the two records' views by one tiled copy that skips the B planes between them (vmap), else
     // the range from the first record's view to the end of the last one's.
     const bool vtma = kQView && p.v_tma;
-    const int rstride = vtma ? kViewBytes : kRecordBytes;  // shared-memory distance between records
+    const int rstride = (vtma || kQ8) ? kViewBytes : kRecordBytes;  // shared-memory distance between records
     const int recs_bytes = (RPS - 1) * rstride + rbytes;
     const int sbytes = RPS * xbytes + recs_bytes + ebytes;
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + S * sbytes);
@@ -264,11 +274,11 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             mbar_arrive_expect_tx_elect(fb, 2 * kViewBytes);
             tma_3d_g2s_elect(smem_u32(stage_rec(s, 0)), &vmap, 0, 0, r0 + js * 2, fb);
         } else {
-            const uint32_t bytes = (nr - 1) * kRecordBytes + rbytes;  // consecutive records are contiguous
+            const uint32_t bytes = (nr - 1) * gstride + rbytes;  // consecutive records are contiguous
             mbar_arrive_expect_tx_elect(fb, bytes);
             bulk_g2s_elect(smem_u32(stage_rec(s, 0)), psrc, bytes, fb);
         }
-        psrc += nr * kRecordBytes;
+        psrc += nr * gstride;
         issued = js + 1;
         pst.advance(1, S);
     };
@@ -317,7 +327,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         }
         __syncwarp();
         pkt = r0 % KT;
-        psrc = p.records + static_cast<size_t>(r0) * kRecordBytes;
+        psrc = p.records + static_cast<size_t>(r0) * gstride;
         if (nst > 0) produce_rec(0);
     }
     // escape feeder: lane l holds rec_esc_off[r0 + base + l] (cur) and [r0 + base + 32 + l]
@@ -339,7 +349,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     };
     int en_tile = r0 / KT;
     uint32_t en_cur = 0, en_nxt = 0;
-    if (warp >= kWarpDec0) {
+    if (!kQ8 && warp >= kWarpDec0) {
         en_cur = en_load(en_tile);
         en_nxt = en_load(en_tile + 1);
     }
@@ -508,6 +518,13 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             const uint4 v1 = lds128(rec + 1 * 2048 + 16 * nl);
             const uint4 v2 = lds128(rec + 2 * 2048 + 16 * nl);
             const uint4 v3 = lds128(rec + 3 * 2048 + 16 * nl);
+            if (kQ8) {
+                decode_q8_chunk16(v0, w);
+                decode_q8_chunk16(v1, w + 8);
+                decode_q8_chunk16(v2, w + 16);
+                decode_q8_chunk16(v3, w + 24);
+                return;
+            }
             if (kQView) {
                 const uint4 z = make_uint4(0, 0, 0, 0);
                 decode_chunk16<true, 0>(v0, z, base2, w, m3, m15);
@@ -574,12 +591,12 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             const int nr = min(RPS, nrec - js * RPS);
             // the slot's tensor-memory buffers are free: the producer refilled this slot only
             // after the MMAs that last read it completed
-            decode_record(s, 0, base2_for(tile), wa);
+            decode_record(s, 0, kQ8 ? 0u : base2_for(tile), wa);
             tc_fence_after();
             tmem_st_32x32b_x32(a_slot(s, 0) + (static_cast<uint32_t>(32 * qw) << 16), wa);
             if (nr == 2) {
                 const int tile1 = (kt + 1 == p.k_tiles) ? tile + 1 : tile;
-                decode_record(s, 1, base2_for(tile1), wb);
+                decode_record(s, 1, kQ8 ? 0u : base2_for(tile1), wb);
                 tmem_st_32x32b_x32(a_slot(s, 1) + (static_cast<uint32_t>(32 * qw) << 16), wb);
             }
             tmem_wait_st();
@@ -640,7 +657,15 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // of the blocks still running takes microseconds per chunk. Partial sums, read back by
         // another block, are stored directly, one value per row.
         int ybuf = 0;
-        auto put_rows = [&](int m0, int tile, const float (&f)[16], float *part) {
+        auto put_rows = [&](int m0, int tile, const float (&fin)[16], float *part) {
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = fin[i];
+            if constexpr (kQ8) {  // this channel's row scale
+                const float sc = p.row_scale[tile * kTileN + nl];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] *= sc;
+            }
           if constexpr (!kArgmax) {
             if (!part && p.y_tma) {
                 const int esz = p.y_bf16 ? 2 : 4;
@@ -907,6 +932,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                     }
                 }
                 if (et == 0) *p.done_cnt = 0;
+                if (et == 0 && p.run_flag) *p.run_flag = 0;  // the conditional launch has run
             }
         }
     }
@@ -992,20 +1018,25 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// internal operation: the GEMM over the certified head's INT8 copy (not part of the C ABI)
+constexpr int kOpQ8 = 100;
+
 struct Layout {
     int npad, stages, rps, nacc, acc_cols, grid, unit, smem;
     bool whole;  // every block covers whole tiles (no partial sums)
     bool vtma;   // Q view with two records per slot: views copied through a tensor map
+    bool packed; // INT8 copy: 8 KB records back to back
     int64_t R;
     size_t ws_bytes, off_err, off_tile, off_done, off_part, off_top;
 };
 
 w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     if (M < 1 || M > kMaxM) return W12_ERR_UNSUPPORTED_SHAPE;
-    if (op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) return W12_ERR_INVALID_ARG;
+    if ((op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) && op != kOpQ8) return W12_ERR_INVALID_ARG;
     int sms = 0;
     W12_TRY(require_device(&sms));
-    const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX);
+    const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8);
+    L->packed = (op == kOpQ8);
     L->R = static_cast<int64_t>(t->n_tiles) * t->k_tiles;
     L->npad = (M + 15) / 16 * 16;
     // two records per ring slot while the activation tiles are small
@@ -1030,8 +1061,8 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
         L->whole = false;
     }
     // the view map needs a 16-byte aligned record array (records are 12 KB apart)
-    L->vtma = q && L->rps == 2 && aligned16(t->records);
-    const int rstride = L->vtma ? kViewBytes : kRecordBytes;
+    L->vtma = q && !L->packed && L->rps == 2 && aligned16(t->records);
+    const int rstride = (L->vtma || L->packed) ? kViewBytes : kRecordBytes;
     const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * rstride + (q ? kViewBytes : kRecordBytes) +
                        (q ? 0 : kEscCap * 4);
     const int ctrl = static_cast<int>(align_up(sizeof(Ctrl), 1024));
@@ -1066,10 +1097,10 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     return W12_OK;
 }
 
-template <bool kQ, bool kA>
+template <bool kQ, bool kA, bool kQ8 = false>
 w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const CUtensorMap &ymap,
                           const CUtensorMap &vmap, const Params &p, const Layout &L, bool overlap, cudaStream_t st) {
-    auto kern = w12_gemm_kernel<kQ, kA>;
+    auto kern = w12_gemm_kernel<kQ, kA, kQ8>;
     // the opt-in shared-memory limit is set once per device (to the maximum any plan uses)
     static std::atomic<uint64_t> smem_set{0};
     int dev = 0;
@@ -1104,8 +1135,13 @@ w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const
 
 w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, int y_dtype,
                int32_t *idx, float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream,
-               unsigned flags = 0) {
-    W12_TRY(check_tensor(t));
+               unsigned flags = 0, const float *row_scale = nullptr, int *run_flag = nullptr) {
+    if (op == kOpQ8) {
+        // the INT8 copy of the certified head: records and row scales only
+        if (!t || !t->records || !row_scale || t->N < 1 || t->K < 1) return W12_ERR_INVALID_ARG;
+    } else {
+        W12_TRY(check_tensor(t));
+    }
     if (flags & ~static_cast<unsigned>(W12_LAUNCH_OVERLAP | W12_LAUNCH_TEST_STALL)) return W12_ERR_INVALID_ARG;
     const bool overlap = (flags & W12_LAUNCH_OVERLAP) != 0;
     if (!x || !aligned16(x) || !ws) return W12_ERR_INVALID_ARG;
@@ -1199,6 +1235,9 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.y_tma = (y_tma && L.whole) ? 1 : 0;
     p.x_pair = x_pair ? 1 : 0;
     p.v_tma = L.vtma ? 1 : 0;
+    p.row_scale = row_scale;
+    p.run_flag = run_flag;
+    if (run_flag && (!argmax || overlap)) return W12_ERR_INVALID_ARG;  // stream-ordered argmax only
     p.test_stall = (flags & W12_LAUNCH_TEST_STALL) ? 1 : 0;
     p.R = static_cast<int>(L.R);
     p.y = y;
@@ -1212,6 +1251,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.val = val;
     p.gap = gap;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (op == kOpQ8) return launch_variant<true, false, true>(map, map2, ymap, vmap, p, L, overlap, st);
     if (q)
         return argmax ? launch_variant<true, true>(map, map2, ymap, vmap, p, L, overlap, st)
                       : launch_variant<true, false>(map, map2, ymap, vmap, p, L, overlap, st);
@@ -1220,6 +1260,23 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
 }
 
 }  // namespace
+
+// ---- entry points shared with the certified head (w12_certified.cu) ----
+w12_status gemm_q8_workspace(const w12_tensor *codes, int M, size_t *bytes) {
+    Layout L{};
+    W12_TRY(plan(codes, M, kOpQ8, &L));
+    *bytes = L.ws_bytes;
+    return W12_OK;
+}
+w12_status gemm_q8(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, float *y, void *ws,
+                   size_t ws_bytes, w12_stream_t stream) {
+    return run(codes, x, M, kOpQ8, y, W12_OUT_F32, nullptr, nullptr, nullptr, ws, ws_bytes, stream, 0, row_scale);
+}
+w12_status lmhead_argmax_if(const w12_tensor *t, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,
+                            int *run_flag, void *ws, size_t ws_bytes, w12_stream_t stream) {
+    return run(t, x, M, W12_OP_ARGMAX, nullptr, W12_OUT_F32, idx, val, gap, ws, ws_bytes, stream, 0, nullptr,
+               run_flag);
+}
 }  // namespace w12
 
 extern "C" w12_status w12_workspace_size(const w12_tensor *t, int M, int op, size_t *bytes) {

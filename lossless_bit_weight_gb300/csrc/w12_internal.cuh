@@ -42,6 +42,16 @@ inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 
 w12_status check_shape(int N, int K);
 w12_status check_tensor(const w12_tensor *t);
 
+// GEMM entry points shared between translation units (defined in w12_gemm.cu):
+// the GEMM over the certified head's INT8 copy (records in `codes->records`, 8 KB each; y fp32)
+w12_status gemm_q8_workspace(const w12_tensor *codes, int M, size_t *bytes);
+w12_status gemm_q8(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, float *y, void *ws,
+                   size_t ws_bytes, w12_stream_t stream);
+// the W12 head's fused argmax, launched stream-ordered; it does nothing unless *run_flag != 0
+// when it starts, and clears the flag when it has run
+w12_status lmhead_argmax_if(const w12_tensor *t, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,
+                            int *run_flag, void *ws, size_t ws_bytes, w12_stream_t stream);
+
 // ------------------------------------------------------------------------------------------
 // device side
 // ------------------------------------------------------------------------------------------
@@ -477,6 +487,29 @@ __device__ __forceinline__ void decode_chunk16(const uint4 &v, const uint4 &b, u
         const int sh = 8 * (q & 1);
         out[2 * q] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4140u), B >> sh, base2, m3, m15);
         out[2 * q + 1] = decode_pair<kQView>(__byte_perm(vw[q], 0u, 0x4342u), B >> (sh + 4), base2, m3, m15);
+    }
+}
+
+// Two sign-magnitude INT8 codes (bit 7 sign, bits 0-6 magnitude m; the certified head's copy)
+// -> one bf16x2 word of their integer values, exactly. A byte permute places code i in the low
+// byte of half i with its sign replicated through the high byte; then h = sign | 0x4300 | m is
+// +-(128 + m) and c = sign | 0x4300 is +-128, and h - c = +-m exactly.
+__device__ __forceinline__ uint32_t decode_q8_pair(uint32_t codes, uint32_t sel) {
+    uint32_t x, h, c, out;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(codes), "r"(sel));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(h) : "r"(x), "r"(0x807F807Fu), "r"(0x43004300u));
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(c) : "r"(x), "r"(0x80008000u), "r"(0x43004300u));
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(out) : "r"(h), "r"(c));
+    return out;
+}
+
+// Sixteen INT8 codes k_l = 16c .. 16c+15 of one row -> 8 bf16x2 words.
+__device__ __forceinline__ void decode_q8_chunk16(const uint4 &v, uint32_t *out) {
+    const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        out[2 * q] = decode_q8_pair(vw[q], 0x9180u);      // codes 0, 1 of the word
+        out[2 * q + 1] = decode_q8_pair(vw[q], 0xB3A2u);  // codes 2, 3
     }
 }
 

@@ -42,6 +42,16 @@ class CTensor(ctypes.Structure):
     ]
 
 
+class CQ8Head(ctypes.Structure):
+    """Mirror of ``w12_q8_head``."""
+
+    _fields_ = [
+        ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("n_tiles", ctypes.c_int32), ("k_tiles", ctypes.c_int32),
+        ("codes", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("bound", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -73,6 +83,10 @@ def lib() -> ctypes.CDLL:
             "w12_gemm_ex": ([T, P, i32, i32, P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
             "w12_gemm_config": ([T, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32)], i32),
+            "w12_q8_shape": ([i32, i32, ctypes.POINTER(CQ8Head), ctypes.POINTER(sz), ctypes.POINTER(sz)], i32),
+            "w12_q8_build": ([P, ctypes.POINTER(CQ8Head), P], i32),
+            "w12_certified_workspace_size": ([T, ctypes.POINTER(CQ8Head), i32, ctypes.POINTER(sz)], i32),
+            "w12_lmhead_certified": ([T, ctypes.POINTER(CQ8Head), P, i32, P, P, P, P, P, sz, P], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -290,3 +304,56 @@ def gemm_config(t: W12Tensor, M: int, op: int) -> dict:
     _check(lib().w12_gemm_config(ctypes.byref(t.c), M, op, ctypes.byref(g), ctypes.byref(s), ctypes.byref(m)),
            "w12_gemm_config")
     return {"grid": g.value, "stages": s.value, "smem_bytes": m.value}
+
+
+class Q8Head:
+    """The certified LM head's INT8 copy (``w12_q8_head``): codes, row scales and row bounds."""
+
+    def __init__(self, N: int, K: int, device="cuda"):
+        self.c = CQ8Head()
+        cb, rb = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().w12_q8_shape(N, K, ctypes.byref(self.c), ctypes.byref(cb), ctypes.byref(rb)), "w12_q8_shape")
+        self.N, self.K = N, K
+        self.codes = torch.empty(int(cb.value), dtype=torch.uint8, device=device)
+        self.scale = torch.empty(int(rb.value) // 4, dtype=torch.float32, device=device)
+        self.bound = torch.empty(int(rb.value) // 4, dtype=torch.float32, device=device)
+        self.c.codes, self.c.scale, self.c.bound = self.codes.data_ptr(), self.scale.data_ptr(), self.bound.data_ptr()
+        self._ws = {}
+
+    @property
+    def nbytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in (self.codes, self.scale, self.bound))
+
+    def gemm_bytes(self) -> int:
+        """Bytes the approximate pass streams: the codes and the row scales."""
+        return self.codes.numel() + self.scale.numel() * 4
+
+
+def q8_build(w: torch.Tensor, stream=None) -> Q8Head:
+    """The INT8 copy of a bf16 head [N, K] (device)."""
+    _bits(w)
+    N, K = w.shape
+    h = Q8Head(N, K, device=w.device)
+    _check(lib().w12_q8_build(_ptr(w), ctypes.byref(h.c), _stream(stream)), "w12_q8_build")
+    return h
+
+
+def lmhead_certified(t: W12Tensor, h: Q8Head, x: torch.Tensor, stream=None):
+    """(idx int32[M], val f32[M], gap f32[M], survivors int32[M]) of x @ W^T through the certified
+    head: the INT8 copy's bound discards tokens, the survivors are rescored from the W12 head t."""
+    _bits(x)
+    M = x.shape[0]
+    idx = torch.empty(M, dtype=torch.int32, device=x.device)
+    val = torch.empty(M, dtype=torch.float32, device=x.device)
+    gap = torch.empty(M, dtype=torch.float32, device=x.device)
+    surv = torch.empty(M, dtype=torch.int32, device=x.device)
+    key = (M, torch.cuda.current_device())
+    if key not in h._ws:
+        nb = ctypes.c_size_t()
+        _check(lib().w12_certified_workspace_size(ctypes.byref(t.c), ctypes.byref(h.c), M, ctypes.byref(nb)),
+               "w12_certified_workspace_size")
+        h._ws[key] = (torch.zeros(max(int(nb.value), 16), dtype=torch.uint8, device=x.device), int(nb.value))
+    ws, nb = h._ws[key]
+    _check(lib().w12_lmhead_certified(ctypes.byref(t.c), ctypes.byref(h.c), _ptr(x), M, _ptr(idx), _ptr(val),
+                                      _ptr(gap), _ptr(surv), _ptr(ws), nb, _stream(stream)), "w12_lmhead_certified")
+    return idx, val, gap, surv
