@@ -265,6 +265,15 @@ w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_head *h, const
                                 int32_t *idx, float *val, float *gap, int32_t *survivors, void *workspace,
                                 size_t workspace_bytes, w12_stream_t stream);
 
+/* The Q pass over the separate INT8 copy (SpecPilot §5.3 and App. C: an INT6/INT8 Q-pass
+ * copy next to the nested view): idx / val / gap of each row's argmax of
+ * scale[n] (x . q[n,:]), computed like w12_lmhead_argmax (fp32 accumulation, ties to the
+ * smaller index). flags: 0 or W12_LAUNCH_OVERLAP. The workspace must be zero-filled once; every
+ * call leaves it zeroed. Asynchronous. */
+w12_status w12_q8_argmax_workspace_size(const w12_q8_head *h, int M, size_t *bytes);
+w12_status w12_q8_argmax(const w12_q8_head *h, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,
+                         unsigned flags, void *workspace, size_t workspace_bytes, w12_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -515,3 +515,19 @@ extern "C" w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_hea
     // 5. the full argmax, only if a row overflowed its survivor list
     return lmhead_argmax_if(t, x, M, idx, val, gap, flag, ws + L.off_full, L.full_ws, stream);
 }
+
+extern "C" w12_status w12_q8_argmax_workspace_size(const w12_q8_head *h, int M, size_t *bytes) {
+    W12_TRY(check_q8(h));
+    if (!bytes) return W12_ERR_INVALID_ARG;
+    const w12_tensor c = codes_tensor(h);
+    return gemm_q8_argmax_workspace(&c, M, bytes);
+}
+
+extern "C" w12_status w12_q8_argmax(const w12_q8_head *h, const uint16_t *x, int M, int32_t *idx, float *val,
+                                    float *gap, unsigned flags, void *workspace, size_t workspace_bytes,
+                                    w12_stream_t stream) {
+    W12_TRY(check_q8(h));
+    if (flags & ~static_cast<unsigned>(W12_LAUNCH_OVERLAP)) return W12_ERR_INVALID_ARG;
+    const w12_tensor c = codes_tensor(h);
+    return gemm_q8_argmax(&c, h->scale, x, M, idx, val, gap, workspace, workspace_bytes, stream, flags);
+}

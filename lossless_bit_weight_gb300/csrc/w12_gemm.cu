@@ -229,7 +229,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
 
     const int S = p.stages, RPS = p.rps;
     const int xbytes = p.npad * 128;
-    static_assert(!kQ8 || (kQView && !kArgmax), "the INT8 copy is read as a plain GEMM");
+    static_assert(!kQ8 || kQView, "the INT8 copy is read like a view: no plane B, no escapes");
     constexpr int rbytes = kQView ? kViewBytes : kRecordBytes;
     constexpr int ebytes = kQView ? 0 : kEscCap * 4;
     constexpr int gstride = kQ8 ? kViewBytes : kRecordBytes;  // distance between records in memory
@@ -657,15 +657,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // of the blocks still running takes microseconds per chunk. Partial sums, read back by
         // another block, are stored directly, one value per row.
         int ybuf = 0;
-        auto put_rows = [&](int m0, int tile, const float (&fin)[16], float *part) {
-            float f[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = fin[i];
-            if constexpr (kQ8) {  // this channel's row scale
-                const float sc = p.row_scale[tile * kTileN + nl];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) f[i] *= sc;
-            }
+        auto put_rows = [&](int m0, int tile, const float (&f)[16], float *part) {
           if constexpr (!kArgmax) {
             if (!part && p.y_tma) {
                 const int esz = p.y_bf16 ? 2 : 4;
@@ -715,6 +707,15 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                     part[static_cast<size_t>(m0 + i) * kTileN + nl] = f[i];
                 else
                     emit(m0 + i, tile * kTileN + nl, f[i]);
+            }
+        };
+        // INT8 copy: a block's accumulator values are multiplied by their channel's row scale as
+        // they leave tensor memory, so partials, their sums and y all carry the scale once
+        auto scale_rows = [&](int tile, float (&f)[16]) {
+            if constexpr (kQ8) {
+                const float sc = p.row_scale[tile * kTileN + nl];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] *= sc;
             }
         };
         auto partial_of = [&](int cc, int tile, int m) {  // block cc's partial of tile
@@ -801,6 +802,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
 #pragma unroll
                             for (int i = 0; i < 16; ++i) f[i] = has0 ? f[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
                         }
+                        scale_rows(tile, f);
 #pragma unroll
                         for (int i = 0; i < 16; ++i) f[i] += pf[16 * h + i];
                         put_rows(m0, tile, f, nullptr);
@@ -823,6 +825,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
 #pragma unroll
                         for (int i = 0; i < 16; ++i) f[i] = has0 ? f[i] + __uint_as_float(v[i]) : __uint_as_float(v[i]);
                     }
+                    scale_rows(tile, f);
                     if (mode == 2) {
                         float acc[16];
 #pragma unroll
@@ -1018,8 +1021,9 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// internal operation: the GEMM over the certified head's INT8 copy (not part of the C ABI)
-constexpr int kOpQ8 = 100;
+// internal operations over the INT8 head copy (reached through the certified-head entry points)
+constexpr int kOpQ8 = 100;        // y = scale_n (x . q_n)
+constexpr int kOpQ8Argmax = 101;  // its row argmax (the Q pass over the separate copy)
 
 struct Layout {
     int npad, stages, rps, nacc, acc_cols, grid, unit, smem;
@@ -1032,11 +1036,12 @@ struct Layout {
 
 w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     if (M < 1 || M > kMaxM) return W12_ERR_UNSUPPORTED_SHAPE;
-    if ((op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) && op != kOpQ8) return W12_ERR_INVALID_ARG;
+    if ((op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) && op != kOpQ8 && op != kOpQ8Argmax)
+        return W12_ERR_INVALID_ARG;
     int sms = 0;
     W12_TRY(require_device(&sms));
-    const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8);
-    L->packed = (op == kOpQ8);
+    const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8 || op == kOpQ8Argmax);
+    L->packed = (op == kOpQ8 || op == kOpQ8Argmax);
     L->R = static_cast<int64_t>(t->n_tiles) * t->k_tiles;
     L->npad = (M + 15) / 16 * 16;
     // two records per ring slot while the activation tiles are small
@@ -1136,7 +1141,8 @@ w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const
 w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, int y_dtype,
                int32_t *idx, float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream,
                unsigned flags = 0, const float *row_scale = nullptr, int *run_flag = nullptr) {
-    if (op == kOpQ8) {
+    const bool q8 = (op == kOpQ8 || op == kOpQ8Argmax);
+    if (q8) {
         // the INT8 copy of the certified head: records and row scales only
         if (!t || !t->records || !row_scale || t->N < 1 || t->K < 1) return W12_ERR_INVALID_ARG;
     } else {
@@ -1148,7 +1154,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     Layout L{};
     W12_TRY(plan(t, M, op, &L));
     if (ws_bytes < L.ws_bytes) return W12_ERR_WORKSPACE;
-    const bool argmax = (op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX);
+    const bool argmax = (op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8Argmax);
     const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX);
     if (argmax && (!idx || !val || !gap)) return W12_ERR_INVALID_ARG;
     if (!argmax && (!y || (y_dtype != W12_OUT_F32 && y_dtype != W12_OUT_BF16))) return W12_ERR_INVALID_ARG;
@@ -1252,6 +1258,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.gap = gap;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (op == kOpQ8) return launch_variant<true, false, true>(map, map2, ymap, vmap, p, L, overlap, st);
+    if (op == kOpQ8Argmax) return launch_variant<true, true, true>(map, map2, ymap, vmap, p, L, overlap, st);
     if (q)
         return argmax ? launch_variant<true, true>(map, map2, ymap, vmap, p, L, overlap, st)
                       : launch_variant<true, false>(map, map2, ymap, vmap, p, L, overlap, st);
@@ -1271,6 +1278,17 @@ w12_status gemm_q8_workspace(const w12_tensor *codes, int M, size_t *bytes) {
 w12_status gemm_q8(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, float *y, void *ws,
                    size_t ws_bytes, w12_stream_t stream) {
     return run(codes, x, M, kOpQ8, y, W12_OUT_F32, nullptr, nullptr, nullptr, ws, ws_bytes, stream, 0, row_scale);
+}
+w12_status gemm_q8_argmax_workspace(const w12_tensor *codes, int M, size_t *bytes) {
+    Layout L{};
+    W12_TRY(plan(codes, M, kOpQ8Argmax, &L));
+    *bytes = L.ws_bytes;
+    return W12_OK;
+}
+w12_status gemm_q8_argmax(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, int32_t *idx,
+                          float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags) {
+    return run(codes, x, M, kOpQ8Argmax, nullptr, W12_OUT_F32, idx, val, gap, ws, ws_bytes, stream, flags,
+               row_scale);
 }
 w12_status lmhead_argmax_if(const w12_tensor *t, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,
                             int *run_flag, void *ws, size_t ws_bytes, w12_stream_t stream) {

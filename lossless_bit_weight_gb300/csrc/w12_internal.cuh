@@ -47,6 +47,10 @@ w12_status check_tensor(const w12_tensor *t);
 w12_status gemm_q8_workspace(const w12_tensor *codes, int M, size_t *bytes);
 w12_status gemm_q8(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, float *y, void *ws,
                    size_t ws_bytes, w12_stream_t stream);
+// the row argmax over the INT8 copy (flags: W12_LAUNCH_OVERLAP)
+w12_status gemm_q8_argmax_workspace(const w12_tensor *codes, int M, size_t *bytes);
+w12_status gemm_q8_argmax(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, int32_t *idx,
+                          float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags);
 // the W12 head's fused argmax, launched stream-ordered; it does nothing unless *run_flag != 0
 // when it starts, and clears the flag when it has run
 w12_status lmhead_argmax_if(const w12_tensor *t, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,

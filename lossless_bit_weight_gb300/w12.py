@@ -87,6 +87,8 @@ def lib() -> ctypes.CDLL:
             "w12_q8_build": ([P, ctypes.POINTER(CQ8Head), P], i32),
             "w12_certified_workspace_size": ([T, ctypes.POINTER(CQ8Head), i32, ctypes.POINTER(sz)], i32),
             "w12_lmhead_certified": ([T, ctypes.POINTER(CQ8Head), P, i32, P, P, P, P, P, sz, P], i32),
+            "w12_q8_argmax_workspace_size": ([ctypes.POINTER(CQ8Head), i32, ctypes.POINTER(sz)], i32),
+            "w12_q8_argmax": ([ctypes.POINTER(CQ8Head), P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -357,3 +359,23 @@ def lmhead_certified(t: W12Tensor, h: Q8Head, x: torch.Tensor, stream=None):
     _check(lib().w12_lmhead_certified(ctypes.byref(t.c), ctypes.byref(h.c), _ptr(x), M, _ptr(idx), _ptr(val),
                                       _ptr(gap), _ptr(surv), _ptr(ws), nb, _stream(stream)), "w12_lmhead_certified")
     return idx, val, gap, surv
+
+
+def q8_argmax(h: Q8Head, x: torch.Tensor, stream=None, overlap: bool = False):
+    """(idx int32[M], val f32[M], gap f32[M]) of the argmax over the INT8 copy alone: the Q pass
+    through the separate copy (approximate; compare lmhead_certified for the exact argmax)."""
+    _bits(x)
+    M = x.shape[0]
+    idx = torch.empty(M, dtype=torch.int32, device=x.device)
+    val = torch.empty(M, dtype=torch.float32, device=x.device)
+    gap = torch.empty(M, dtype=torch.float32, device=x.device)
+    key = ("argmax", M, torch.cuda.current_device())
+    if key not in h._ws:
+        nb = ctypes.c_size_t()
+        _check(lib().w12_q8_argmax_workspace_size(ctypes.byref(h.c), M, ctypes.byref(nb)),
+               "w12_q8_argmax_workspace_size")
+        h._ws[key] = (torch.zeros(max(int(nb.value), 16), dtype=torch.uint8, device=x.device), int(nb.value))
+    ws, nb = h._ws[key]
+    _check(lib().w12_q8_argmax(ctypes.byref(h.c), _ptr(x), M, _ptr(idx), _ptr(val), _ptr(gap),
+                               LAUNCH_OVERLAP if overlap else 0, _ptr(ws), nb, _stream(stream)), "w12_q8_argmax")
+    return idx, val, gap

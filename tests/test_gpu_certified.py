@@ -159,3 +159,24 @@ def test_certified_full_head(w12):
     assert np.allclose(val.cpu().numpy(), fval.cpu().numpy(), rtol=1e-5, atol=1e-4)
     s = surv.cpu().numpy()
     assert np.all(s >= 2) and np.all(s <= 4096)
+
+
+@pytest.mark.parametrize("N,K,M,seed", [(3000, 256, 8, 41), (20000, 192, 16, 42), (129, 64, 3, 43)])
+def test_q8_argmax_matches_oracle(w12, N, K, M, seed):
+    """The Q pass over the INT8 copy: its argmax against the oracle's argmax of s_n (x . q_n), both
+    whole-tile and split-tile (stream-K) layouts; overlapped and plain launches agree bitwise."""
+    w = synth.weights(N, K, synth.HEAD, seed=seed, device="cuda")
+    x = synth.activations(M, K, seed=seed + 1, device="cuda")
+    h = w12.q8_build(w)
+    idx, val, gap = w12.q8_argmax(h, x)
+    io, vo, go = w12.q8_argmax(h, x, overlap=True)
+    assert torch.equal(idx, io) and torch.equal(val.view(torch.int32), vo.view(torch.int32))
+    ref = oracle.head_q8(to_np_u16(w))
+    xv = (to_np_u16(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    qf = ref.q.astype(np.float64)
+    s = ref.scale.astype(np.float64)[None, :]
+    yh = (xv @ qf.T) * s
+    ad = (np.abs(xv) @ np.abs(qf).T) * s
+    checked, near, wrong, det = argmax_check(idx.cpu().numpy(), val.cpu().numpy(), gap.cpu().numpy(), yh, ad)
+    assert wrong == 0, det
+    assert checked + near == M

@@ -199,6 +199,11 @@ def test_qview_argmax_and_agreement_on_lm_head(w12):
         iq, vq, gq = w12.lmhead_argmax(t, x, qview=True)
         w12.check(t)
         rates[name] = float((ie == iq).float().mean())
+        # the separate INT8 copy's Q pass on the same rows (SpecPilot §5.3, App. C)
+        h = w12.q8_build(w)
+        i8, _, _ = w12.q8_argmax(h, x)
+        rates[name + ", INT8 copy"] = float((ie == i8).float().mean())
+        del h
         if rec is synth.HEAD:
             yq_ref, adq = oracle.gemm(to_np_u16(x[:16]), oracle.qview_weights(to_np_u16(w)))
             checked, near, wrong, det = argmax_check(iq[:16].cpu().numpy(), vq[:16].cpu().numpy(),
@@ -206,5 +211,5 @@ def test_qview_argmax_and_agreement_on_lm_head(w12):
             assert wrong == 0, det
             assert checked >= 14
         del w, t
-    print("Q-view top-1 agreement with the exact pass on the LM head at M=64: "
+    print("Q-pass top-1 agreement with the exact pass on the LM head at M=64: "
           + ", ".join(f"{k} {v:.3f}" for k, v in rates.items()))
