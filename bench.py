@@ -539,6 +539,25 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
     ao_us = _time(lambda i: w12.lmhead_argmax(th, xh, overlap=True), reps=10)
     q_us = _time(lambda i: w12.lmhead_argmax(th, xh, qview=True, overlap=True), reps=10)
     c_us = _time(lambda i: torch.argmax(torch.nn.functional.linear(xh, wh), dim=1), reps=10)
+    # the certified head (INT8 copy + bound + exact rescoring) and the copy's own Q pass
+    import time as _t
+    torch.cuda.synchronize()
+    t0 = _t.perf_counter()
+    hq = w12.q8_build(wh)
+    torch.cuda.synchronize()
+    q8_build_ms = (_t.perf_counter() - t0) * 1e3
+    cert = {}
+    for m in (1, 32):
+        xm = xh if m == 32 else xh[:1].contiguous()
+        _, _, _, sv = w12.lmhead_certified(th, hq, xm)
+        cert[str(m)] = {"us": round(_time(lambda i: w12.lmhead_certified(th, hq, xm), reps=10), 1),
+                        "fused_argmax_overlap_us": round(_time(lambda i: w12.lmhead_argmax(th, xm, overlap=True),
+                                                               reps=10), 1),
+                        "survivors_mean": round(float(sv.float().mean()), 1), "survivors_max": int(sv.max())}
+    q8_us = _time(lambda i: w12.q8_argmax(hq, xh, overlap=True), reps=10)
+    out["certified_head"] = {"q8_copy_gb": round(hq.nbytes / 1e9, 3), "q8_build_ms": round(q8_build_ms, 1),
+                             "by_m": cert, "q8_qpass_argmax_overlap_us_M32": round(q8_us, 1)}
+    del hq
     w12.check(th)
     out["lmhead"] = {"M": 32, "us": round(a_us, 1), "rows_per_s": round(32 / (a_us * 1e-6), 1),
                      "weight_gbs": round(th.gemm_bytes() / (a_us * 1e-6) / 1e9, 1),
