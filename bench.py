@@ -551,6 +551,8 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
         xm = xh if m == 32 else xh[:1].contiguous()
         _, _, _, sv = w12.lmhead_certified(th, hq, xm)
         cert[str(m)] = {"us": round(_time(lambda i: w12.lmhead_certified(th, hq, xm), reps=10), 1),
+                        "bf16_rescore_us": round(_time(lambda i: w12.lmhead_certified(th, hq, xm, w_bf16=wh),
+                                                       reps=10), 1),
                         "fused_argmax_overlap_us": round(_time(lambda i: w12.lmhead_argmax(th, xm, overlap=True),
                                                                reps=10), 1),
                         "survivors_mean": round(float(sv.float().mean()), 1), "survivors_max": int(sv.max())}

@@ -257,11 +257,15 @@ w12_status w12_certified_workspace_size(const w12_tensor *t, const w12_q8_head *
 
 /* idx / val / gap (device, [M]) as w12_lmhead_argmax returns them, through the certified head;
  * survivors (device, [M], may be NULL) receives each row's survivor count. t and h must
- * describe the same head (same N, K). M in [1, W12_MAX_M]. If a row has more than
+ * describe the same head (same N, K). w_bf16 (device, may be NULL) is the head in bf16,
+ * row-major [N, K] with K % 8 == 0 and 16-byte alignment: when given, survivors are rescored
+ * from its contiguous rows, otherwise from t's records and escapes (a gather of 16-byte pieces,
+ * no extra memory). M in [1, W12_MAX_M]. If a row has more than
  * W12_Q8_MAX_SURVIVORS survivors, the full W12 argmax produces every row's result.
  * Asynchronous on `stream`: four kernels, then the full argmax, which does nothing unless a row
  * overflowed. */
-w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_head *h, const uint16_t *x, int M,
+w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_head *h, const uint16_t *w_bf16,
+                                const uint16_t *x, int M,
                                 int32_t *idx, float *val, float *gap, int32_t *survivors, void *workspace,
                                 size_t workspace_bytes, w12_stream_t stream);
 

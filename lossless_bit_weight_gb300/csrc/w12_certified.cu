@@ -10,8 +10,9 @@
 //   3. q8_select_kernel: the survivors, tokens whose upper bound yh + ||x|| d_n reaches L (they
 //      include the exact top-1 and top-2: the top-1 is at least the best lower bound, and the
 //      top-2 at least the smaller of the two best);
-//   4. q8_rescore_kernel: each survivor's exact logit from its W12 records and escapes, and the
-//      argmax and top-1/top-2 gap over the survivors;
+//   4. q8_rescore_kernel: each survivor's exact logit, from the bf16 head's row when the caller
+//      keeps one (contiguous reads) or else from its W12 records and escapes (a gather of
+//      16-byte pieces), and the argmax and top-1/top-2 gap over the survivors;
 //   5. the W12 fused argmax, which does nothing unless a row had more survivors than the list
 //      holds.
 // All bounds are evaluated with directed rounding, and the copy's bound d_n includes the fp32
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(kBoundThreads) q8_select_kernel(const float *_
 // exact rescoring of the survivors from the W12 head
 // ------------------------------------------------------------------------------------------
 struct W12View {
+    const uint16_t *wrow;  // the bf16 head, row-major [N, K], or null (rescore from the records)
     const uint8_t *records;
     const uint8_t *base_exp;
     const uint32_t *esc_off;
@@ -299,6 +301,26 @@ __device__ float exact_logit(const W12View &h, int n, const float *xs, int lane)
     return acc;
 }
 
+// y = x . w_n from the bf16 head's row n, by one warp: lane l reads the 16-byte pieces l, l + 32,
+// ... of the row (K % 8 == 0), and the lanes' sums are added by a fixed shuffle tree
+__device__ float exact_logit_bf16(const W12View &h, int n, const float *xs, int lane) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(h.wrow + static_cast<size_t>(n) * h.K);
+    float acc = 0.f;
+    for (int c = lane; c < h.K / 8; c += 32) {
+        const uint4 v = __ldg(row + c);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int k = 8 * c + 2 * j;
+            acc = fmaf(__uint_as_float(wv[j] << 16), xs[xs_index(k)], acc);
+            acc = fmaf(__uint_as_float(wv[j] & 0xFFFF0000u), xs[xs_index(k + 1)], acc);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+    return acc;
+}
+
 __device__ __forceinline__ bool better_logit(float v, int i, float w, int j) { return v > w || (v == w && i < j); }
 __device__ __forceinline__ void top2_add(float &v1, int &i1, float &v2, float ov1, int oi1, float ov2) {
     if (better_logit(ov1, oi1, v1, i1)) {
@@ -330,7 +352,7 @@ __global__ void __launch_bounds__(kRescoreThreads) q8_rescore_kernel(W12View h, 
     if (cnt <= static_cast<uint32_t>(kCap)) {
         for (uint32_t j = b * kRescoreWarps + warp; j < cnt; j += nrb * kRescoreWarps) {
             const int n = surv[static_cast<size_t>(m) * kCap + j];
-            float y = exact_logit(h, n, xs, lane);
+            float y = h.wrow ? exact_logit_bf16(h, n, xs, lane) : exact_logit(h, n, xs, lane);
             if (isnan(y)) y = -INFINITY;  // a NaN logit never wins (as in the fused argmax)
             top2_add(v1, i1, v2, y, n, -INFINITY);
         }
@@ -466,12 +488,14 @@ extern "C" w12_status w12_certified_workspace_size(const w12_tensor *t, const w1
     return W12_OK;
 }
 
-extern "C" w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_head *h, const uint16_t *x, int M,
+extern "C" w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_head *h, const uint16_t *w_bf16,
+                                           const uint16_t *x, int M,
                                            int32_t *idx, float *val, float *gap, int32_t *survivors, void *workspace,
                                            size_t workspace_bytes, w12_stream_t stream) {
     CertLayout L{};
     W12_TRY(cert_plan(t, h, M, &L));
     if (!x || !aligned16(x) || !idx || !val || !gap || !workspace) return W12_ERR_INVALID_ARG;
+    if (w_bf16 && (!aligned16(w_bf16) || h->K % 8 != 0)) return W12_ERR_INVALID_ARG;
     if (workspace_bytes < L.bytes) return W12_ERR_WORKSPACE;
     int sms = 0;
     W12_TRY(require_device(&sms));
@@ -498,7 +522,7 @@ extern "C" w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_hea
     q8_select_kernel<<<bg, kBoundThreads, 0, st>>>(yh, h->N, h->bound, rnorm, Lrow, scnt, surv);
     W12_CUDA(cudaGetLastError());
     // 4. exact rescoring from the W12 head
-    W12View v{t->records, t->base_exp, t->esc_off, t->esc_k, t->esc_bits, t->N, t->K, t->k_tiles};
+    W12View v{w_bf16, t->records, t->base_exp, t->esc_off, t->esc_k, t->esc_bits, t->N, t->K, t->k_tiles};
     const size_t xs_bytes = sizeof(float) * static_cast<size_t>(t->k_tiles) * 65;
     static std::atomic<uint64_t> smem_set{0};
     int dev = 0;

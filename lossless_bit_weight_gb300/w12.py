@@ -86,7 +86,7 @@ def lib() -> ctypes.CDLL:
             "w12_q8_shape": ([i32, i32, ctypes.POINTER(CQ8Head), ctypes.POINTER(sz), ctypes.POINTER(sz)], i32),
             "w12_q8_build": ([P, ctypes.POINTER(CQ8Head), P], i32),
             "w12_certified_workspace_size": ([T, ctypes.POINTER(CQ8Head), i32, ctypes.POINTER(sz)], i32),
-            "w12_lmhead_certified": ([T, ctypes.POINTER(CQ8Head), P, i32, P, P, P, P, P, sz, P], i32),
+            "w12_lmhead_certified": ([T, ctypes.POINTER(CQ8Head), P, P, i32, P, P, P, P, P, sz, P], i32),
             "w12_q8_argmax_workspace_size": ([ctypes.POINTER(CQ8Head), i32, ctypes.POINTER(sz)], i32),
             "w12_q8_argmax": ([ctypes.POINTER(CQ8Head), P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
         }
@@ -340,9 +340,12 @@ def q8_build(w: torch.Tensor, stream=None) -> Q8Head:
     return h
 
 
-def lmhead_certified(t: W12Tensor, h: Q8Head, x: torch.Tensor, stream=None):
+def lmhead_certified(t: W12Tensor, h: Q8Head, x: torch.Tensor, w_bf16: torch.Tensor | None = None, stream=None):
     """(idx int32[M], val f32[M], gap f32[M], survivors int32[M]) of x @ W^T through the certified
-    head: the INT8 copy's bound discards tokens, the survivors are rescored from the W12 head t."""
+    head: the INT8 copy's bound discards tokens; the survivors are rescored from w_bf16 (the
+    bf16 head, if given) or else from the W12 head t."""
+    if w_bf16 is not None:
+        _bits(w_bf16)
     _bits(x)
     M = x.shape[0]
     idx = torch.empty(M, dtype=torch.int32, device=x.device)
@@ -356,7 +359,7 @@ def lmhead_certified(t: W12Tensor, h: Q8Head, x: torch.Tensor, stream=None):
                "w12_certified_workspace_size")
         h._ws[key] = (torch.zeros(max(int(nb.value), 16), dtype=torch.uint8, device=x.device), int(nb.value))
     ws, nb = h._ws[key]
-    _check(lib().w12_lmhead_certified(ctypes.byref(t.c), ctypes.byref(h.c), _ptr(x), M, _ptr(idx), _ptr(val),
+    _check(lib().w12_lmhead_certified(ctypes.byref(t.c), ctypes.byref(h.c), _ptr(w_bf16), _ptr(x), M, _ptr(idx), _ptr(val),
                                       _ptr(gap), _ptr(surv), _ptr(ws), nb, _stream(stream)), "w12_lmhead_certified")
     return idx, val, gap, surv
 

@@ -91,13 +91,18 @@ def test_q8_bound_covers_every_logit(w12):
     assert np.all(np.abs(y - yh) <= xn[:, None] * bound[None, :])
 
 
+@pytest.mark.parametrize("rescore", ["w12", "bf16"])
 @pytest.mark.parametrize("N,K,M,seed", [(3000, 256, 8, 1), (2000, 192, 5, 2), (1000, 320, 33, 3), (129, 64, 2, 4)])
-def test_certified_argmax_matches_oracle(w12, N, K, M, seed):
+def test_certified_argmax_matches_oracle(w12, N, K, M, seed, rescore):
     w = synth.weights(N, K, synth.HEAD, seed=seed, device="cuda")
+    if seed == 3:  # escapes in every row: a zero and a weight 2^12 times larger
+        bits = w.view(torch.int16)
+        bits[:, 5] = 0
+        bits[:, 300] = bits[:, 300] + (12 << 7)
     x = synth.activations(M, K, seed=seed + 100, device="cuda")
     t = w12.encode(w)
     h = w12.q8_build(w)
-    idx, val, gap, surv = w12.lmhead_certified(t, h, x)
+    idx, val, gap, surv = w12.lmhead_certified(t, h, x, w_bf16=w if rescore == "bf16" else None)
     w12.check(t)
     wn, xn = to_np_u16(w), to_np_u16(x)
     y_ref, ad = oracle.gemm(xn, wn)
@@ -149,10 +154,12 @@ def test_certified_full_head(w12):
     x = synth.activations(32, K, seed=synth.seed_for(2, 1), device="cuda")
     t = w12.encode(w)
     h = w12.q8_build(w)
-    del w
+    ib, vb, gb, sb = w12.lmhead_certified(t, h, x, w_bf16=w)
     idx, val, gap, surv = w12.lmhead_certified(t, h, x)
     fidx, fval, fgap = w12.lmhead_argmax(t, x)
     w12.check(t)
+    assert torch.equal(idx, ib) and torch.equal(surv, sb)
+    assert np.allclose(val.cpu().numpy(), vb.cpu().numpy(), rtol=1e-5, atol=1e-4)
     clear = fgap.cpu().numpy() > 1e-3 * fval.abs().cpu().numpy()
     assert clear.sum() >= 30
     assert np.array_equal(idx.cpu().numpy()[clear], fidx.cpu().numpy()[clear])
