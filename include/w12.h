@@ -18,7 +18,7 @@
  *     says it synchronises. Argument errors are detected on the host and returned before any
  *     work is enqueued.
  *   - Shapes: N >= 1, K >= 8 with K % 8 == 0 (rows must be 16-byte aligned for the tensor-memory
- *     copies); N and K need not be multiples of the 128x64 tile. GEMM rows: 1 <= M <= 256.
+ *     copies); N and K need not be multiples of the 128x64 tile. GEMM rows: 1 <= M <= 384.
  *   - Device: the current device must be a compute capability 10.3 GPU (GB300);
  *     otherwise W12_ERR_DEVICE.
  *   - Determinism: for a given device, shape and input, every output is bitwise reproducible.
@@ -40,7 +40,7 @@ typedef struct CUstream_st *w12_stream_t; /* the same type as cudaStream_t; NULL
 typedef enum {
     W12_OK = 0,
     W12_ERR_INVALID_ARG = 1,       /* null pointer, bad size, misaligned pointer, bad enum */
-    W12_ERR_UNSUPPORTED_SHAPE = 2, /* K % 8 != 0, M outside [1, 256], ... */
+    W12_ERR_UNSUPPORTED_SHAPE = 2, /* K % 8 != 0, M outside [1, 384], ... */
     W12_ERR_WORKSPACE = 3,         /* workspace or scratch smaller than the size query says */
     W12_ERR_CUDA = 4,              /* a CUDA runtime call failed (launch, copy, sync) */
     W12_ERR_MISMATCH = 5,          /* w12_verify found decoded weights that differ */
@@ -53,7 +53,7 @@ enum {
     W12_TILE_K = 64,         /* reduction elements per record */
     W12_RECORD_BYTES = 12288,
     W12_VIEW_BYTES = 8192,   /* the nested 8-bit A+E view: the first two thirds of a record */
-    W12_MAX_M = 256
+    W12_MAX_M = 384
 };
 
 enum { W12_OUT_F32 = 0, W12_OUT_BF16 = 1 };          /* y element type */

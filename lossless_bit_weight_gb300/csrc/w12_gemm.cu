@@ -57,7 +57,7 @@ constexpr int kWarpDec0 = 8;
 constexpr int kEscCap = 128;       // index words staged per slot; more -> read from global
 constexpr int kACols = 32;         // tensor-memory columns of one decoded record (64 bf16/lane)
 constexpr int kMaxStages = 8;
-constexpr int kMaxM = 256;
+constexpr int kMaxM = W12_MAX_M;
 constexpr int kTmemCols = 512;
 constexpr int kSmemLimit = 232448;       // opt-in maximum per block
 constexpr int kSmemFloor = 120 * 1024;   // keeps one block per SM
@@ -90,13 +90,16 @@ struct Ctrl {
     int mode[2];      // how a split tile ends (by segment parity)
     int last[2];      // this block published last and sums the tile (by segment parity)
     int pre;          // the last segment's other block had published before its MMAs completed
-    // per-warp top-2 of the current tile (argmax); in the GEMM variants the staging buffers of
-    // the epilogue's tensor stores, whose shared-memory source must be 128-byte aligned
-    alignas(128) float4 wtop[4][kMaxM];
-    float4 ctop[kMaxM];     // running top-2 of this block (argmax)
 };
 
-static_assert(offsetof(Ctrl, wtop) % 128 == 0, "tensor-store staging must be 128-byte aligned");
+// After the control block, 128-byte aligned, the epilogue's scratch: in the argmax variants the
+// per-warp top-2 of each row (4 x M float4) and the block's running top-2 (M float4); in the
+// GEMM variants the staging buffers of the tensor stores of y (4 warps x 2 x 16 x 32 words).
+constexpr size_t kCtrlBytes = (sizeof(Ctrl) + 127) / 128 * 128;
+constexpr size_t kStagingBytes = 4 * 2 * 16 * 32 * 4;
+__host__ __device__ constexpr size_t scratch_bytes(int M) {
+    return (80 * static_cast<size_t>(M) > kStagingBytes) ? 80 * static_cast<size_t>(M) : kStagingBytes;
+}
 
 struct Params {
     const uint8_t *records;
@@ -108,6 +111,7 @@ struct Params {
     int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
     int y_tma;    // y is written by tiled tensor stores through ymap
     int v_tma;    // Q view: a slot's two record views arrive by one tiled copy through vmap
+    int xhalf;    // more than 256 rows: rows per activation box and per MMA (npad / 2), else 0
     const float *row_scale;  // INT8 copy: per-channel scale, [n_tiles * 128]
     int *run_flag;           // if set, the launch does nothing unless *run_flag != 0 (then clears it)
     int x_pair;   // xmap2 loads the k-slices of two consecutive records in one copy
@@ -241,6 +245,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     const int recs_bytes = (RPS - 1) * rstride + rbytes;
     const int sbytes = RPS * xbytes + recs_bytes + ebytes;
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + S * sbytes);
+    uint8_t *scratch = reinterpret_cast<uint8_t *>(ctrl) + kCtrlBytes;
+    float4 *wtop = reinterpret_cast<float4 *>(scratch);          // [4][M]
+    float4 *ctop = reinterpret_cast<float4 *>(scratch) + 4 * p.M;  // [M]
     auto stage_x = [&](int s, int q) { return smem + s * sbytes + q * xbytes; };
     auto stage_rec = [&](int s, int q) { return smem + s * sbytes + RPS * xbytes + q * rstride; };
     auto stage_esc = [&](int s) { return smem + s * sbytes + RPS * xbytes + recs_bytes; };
@@ -294,6 +301,8 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         } else {
             for (int q = 0; q < nr; ++q) {
                 tma_2d_g2s_elect(smem_u32(stage_x(s, q)), &xmap, pkt * kTileK, 0, xb);
+                // above 256 rows the tile arrives as two boxes of xhalf rows
+                if (p.xhalf) tma_2d_g2s_elect(smem_u32(stage_x(s, q) + p.xhalf * 128), &xmap, pkt * kTileK, p.xhalf, xb);
                 if (++pkt == p.k_tiles) pkt = 0;
             }
         }
@@ -355,7 +364,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     }
     if (kArgmax) {
         for (int m = threadIdx.x; m < p.M; m += kThreads)
-            ctrl->ctop[m] = make_float4(-INFINITY, __int_as_float(0x7FFFFFFF), -INFINITY, 0.f);
+            ctop[m] = make_float4(-INFINITY, __int_as_float(0x7FFFFFFF), -INFINITY, 0.f);
     }
     if (warp == kWarpMma) {
         tmem_alloc(smem_u32(&ctrl->tmem_base), kTmemCols);
@@ -403,7 +412,8 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // Per segment each issuer overwrites its accumulator with its first record, adds the
         // rest, and commits (or, without a record in the segment, just arrives on) accfull.
         const int mq = (warp == kWarpMma) ? 0 : 1;
-        const uint32_t idesc = idesc_bf16_f32(128, p.npad);
+        const uint32_t idesc = idesc_bf16_f32(128, p.xhalf ? p.xhalf : p.npad);
+        const uint64_t bhalf = static_cast<uint64_t>((p.xhalf * 128) >> 4);  // descriptor step to row xhalf
         // the slot's operands: its activation tile for this issuer (B, by descriptor; the
         // descriptor's start-address field moves by sbytes / 16 per slot) and the issuer's
         // decoded record (A, in tensor memory)
@@ -439,8 +449,13 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                 }
                 tc_fence_after();
                 // the issuer's first MMA of a segment overwrites its accumulator; the rest add
-                mma4_bf16_ts_elect(d, a0 + static_cast<uint32_t>(s) * astep, bdesc0 + static_cast<uint64_t>(s) * bstep,
-                                   idesc, r != first ? 1u : 0u, smem_u32(&ctrl->empty[s]));
+                if (p.xhalf)
+                    mma4x2_bf16_ts_elect(d, a0 + static_cast<uint32_t>(s) * astep, bdesc0 + static_cast<uint64_t>(s) * bstep,
+                                         bhalf, static_cast<uint32_t>(p.xhalf), idesc, r != first ? 1u : 0u,
+                                         smem_u32(&ctrl->empty[s]));
+                else
+                    mma4_bf16_ts_elect(d, a0 + static_cast<uint32_t>(s) * astep, bdesc0 + static_cast<uint64_t>(s) * bstep,
+                                       idesc, r != first ? 1u : 0u, smem_u32(&ctrl->empty[s]));
                 issued = js + 1;
             }
             if (!ok) break;
@@ -644,7 +659,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                 float v1 = (n < p.N && !isnan(f)) ? f : -INFINITY, v2 = -INFINITY;
                 int i1 = n;
                 warp_top2(v1, i1, v2);
-                if (lane == 0) ctrl->wtop[qw][m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
+                if (lane == 0) wtop[qw * M + m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
             } else if (n < p.N) {
                 store_y(m, n, f);
             }
@@ -661,7 +676,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
           if constexpr (!kArgmax) {
             if (!part && p.y_tma) {
                 const int esz = p.y_bf16 ? 2 : 4;
-                uint8_t *stg = reinterpret_cast<uint8_t *>(&ctrl->wtop[0][0]) + (qw * 2 + ybuf) * 16 * 32 * esz;
+                uint8_t *stg = scratch + (qw * 2 + ybuf) * 16 * 32 * esz;
                 ybuf ^= 1;
                 if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer
                 __syncwarp();
@@ -684,7 +699,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
           }
           if constexpr (kArgmax) {
             if (!part) {
-                // this warp's top-2 of each of the 16 rows, into wtop[qw][m]
+                // this warp's top-2 of each of the 16 rows, into wtop[qw * M + m]
                 const int n = tile * kTileN + nl;
                 float v1[16], v2[16];
                 int i1[16];
@@ -696,7 +711,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                 }
                 warp_top2_rows16(v1, i1, v2, lane);
                 const int m = m0 + (lane >> 1);
-                if ((lane & 1) == 0 && m < M) ctrl->wtop[qw][m] = make_float4(v1[0], __int_as_float(i1[0]), v2[0], 0.f);
+                if ((lane & 1) == 0 && m < M) wtop[qw * M + m] = make_float4(v1[0], __int_as_float(i1[0]), v2[0], 0.f);
                 return;
             }
           }
@@ -880,15 +895,15 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             if (kArgmax && emitted) {
                 named_bar_sync(kEpiBar, 128);
                 for (int m = et; m < M; m += 128) {
-                    float4 a4 = ctrl->ctop[m];
+                    float4 a4 = ctop[m];
                     float v1 = a4.x, v2 = a4.z;
                     int i1 = __float_as_int(a4.y);
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) {
-                        const float4 o = ctrl->wtop[qq][m];
+                        const float4 o = wtop[qq * M + m];
                         top2_merge(v1, i1, v2, o.x, __float_as_int(o.y), o.z);
                     }
-                    ctrl->ctop[m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
+                    ctop[m] = make_float4(v1, __int_as_float(i1), v2, 0.f);
                 }
                 named_bar_sync(kEpiBar, 128);
             }
@@ -898,7 +913,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         if (!kArgmax && p.y_tma && lane == 0) bulk_wait_group_read<0>();
         if (kArgmax) {
             // publish this block's top-2 per row; the last block merges all blocks in order
-            for (int m = et; m < M; m += 128) p.cta_top[static_cast<size_t>(c) * M + m] = ctrl->ctop[m];
+            for (int m = et; m < M; m += 128) p.cta_top[static_cast<size_t>(c) * M + m] = ctop[m];
             __threadfence();
             named_bar_sync(kEpiBar, 128);
             if (et == 0) {
@@ -1044,6 +1059,8 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     L->packed = (op == kOpQ8 || op == kOpQ8Argmax);
     L->R = static_cast<int64_t>(t->n_tiles) * t->k_tiles;
     L->npad = (M + 15) / 16 * 16;
+    // above 256 rows the MMA's N and the activation box are split in two halves of a multiple of 16
+    if (L->npad > 256) L->npad = (M + 31) / 32 * 32;
     // two records per ring slot while the activation tiles are small
     L->rps = (L->npad <= 64) ? 2 : 1;
     // Work split. Whole tiles per block when that balances within kTileSplitSlack: no tile is
@@ -1070,7 +1087,7 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     const int rstride = (L->vtma || L->packed) ? kViewBytes : kRecordBytes;
     const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * rstride + (q ? kViewBytes : kRecordBytes) +
                        (q ? 0 : kEscCap * 4);
-    const int ctrl = static_cast<int>(align_up(sizeof(Ctrl), 1024));
+    const int ctrl = static_cast<int>(align_up(kCtrlBytes + scratch_bytes(M), 1024));
     int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
     if (stages > kMaxStages) stages = kMaxStages;
     // tensor memory: nacc accumulators of npad columns, then 32 columns per record in flight
@@ -1164,7 +1181,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(t->K), static_cast<cuuint64_t>(M)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(t->K) * 2};
-    const cuuint32_t box[2] = {kTileK, static_cast<cuuint32_t>(L.npad)};
+    const cuuint32_t box[2] = {kTileK, static_cast<cuuint32_t>(L.npad > 256 ? L.npad / 2 : L.npad)};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1241,6 +1258,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.y_tma = (y_tma && L.whole) ? 1 : 0;
     p.x_pair = x_pair ? 1 : 0;
     p.v_tma = L.vtma ? 1 : 0;
+    p.xhalf = (L.npad > 256) ? L.npad / 2 : 0;
     p.row_scale = row_scale;
     p.run_flag = run_flag;
     if (run_flag && (!argmax || overlap)) return W12_ERR_INVALID_ARG;  // stream-ordered argmax only

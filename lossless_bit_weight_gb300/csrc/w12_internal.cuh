@@ -334,6 +334,35 @@ __device__ __forceinline__ void mma4_bf16_ts_elect(uint32_t d_tmem, uint32_t a_t
         : "memory");
 }
 
+// The same for more than 256 activation rows: the MMA's N is split into two halves of nh rows
+// (nh <= 256, a multiple of 16): per K step one MMA into accumulator columns [0, nh) from the
+// tile's first nh rows and one into [nh, 2 nh) from the next nh rows (b_desc + b_half), then
+// one commit for all eight.
+__device__ __forceinline__ void mma4x2_bf16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                     uint64_t b_half, uint32_t nh, uint32_t idesc,
+                                                     uint32_t accumulate, uint32_t bar) {
+    const uint32_t d1 = d_tmem + nh;
+    const uint64_t c = b_desc + b_half;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t.reg .pred A;\n\t.reg .pred T;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "setp.ne.b32 A, %5, 0;\n\t"
+        "setp.eq.u32 T, 1, 1;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %6, A;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%1], [%2], %4, %6, A;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %8, %6, T;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%1], [%7], %9, %6, T;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], %11, %6, T;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%1], [%10], %12, %6, T;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%0], [%13], %14, %6, T;\n\t"
+        "@P tcgen05.mma.cta_group::1.kind::f16 [%1], [%13], %15, %6, T;\n\t"
+        "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%16];\n\t}"
+        ::"r"(d_tmem), "r"(d1), "r"(a_tmem), "l"(b_desc), "l"(c), "r"(accumulate), "r"(idesc),
+          "r"(a_tmem + 8), "l"(b_desc + 2), "l"(c + 2), "r"(a_tmem + 16), "l"(b_desc + 4), "l"(c + 4),
+          "r"(a_tmem + 24), "l"(b_desc + 6), "l"(c + 6), "r"(bar)
+        : "memory");
+}
+
 // Commit from the elected lane (the lane that issued the MMAs it must track).
 __device__ __forceinline__ void mma_commit_elect(uint32_t bar) {
     asm volatile(

@@ -119,7 +119,7 @@ def _gemm_case(w12, N, K, M, seed, recipe=synth.TINY, qview=False, out_dtype=tor
     return t, x, y, yv, y_ref, absdot
 
 
-@pytest.mark.parametrize("M", [1, 2, 3, 8, 16, 17, 32, 33, 64, 100, 192, 256])
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 16, 17, 32, 33, 64, 100, 192, 256, 257, 300, 384])
 def test_gemm_ragged_all_row_classes(w12, M):
     _, _, _, yv, y_ref, ad = _gemm_case(w12, 300, 200, M, seed=100 + M)
     assert gemm_violations(yv, y_ref, ad) == 0
@@ -176,7 +176,7 @@ def test_gemm_bitwise_reproducible(w12):
     assert torch.equal(ia, ib) and torch.equal(va.view(torch.int32), vb.view(torch.int32))
 
 
-@pytest.mark.parametrize("M", [1, 32, 48, 64, 96, 192, 256])
+@pytest.mark.parametrize("M", [1, 32, 48, 64, 96, 192, 256, 320, 384])
 @pytest.mark.parametrize("qview", [False, True])
 def test_gemm_repeat_stress(w12, M, qview):
     """Thirty launches on weights larger than L2 (with 0.1% zeros: many escapes), every result
@@ -212,7 +212,7 @@ def test_workspace_counters_left_zeroed(w12):
         assert int(ws[:head].count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("M", [1, 16, 64, 192])
+@pytest.mark.parametrize("M", [1, 16, 64, 192, 300])
 def test_qview_gemm(w12, M):
     _, _, _, yv, y_ref, ad = _gemm_case(w12, 300, 200, M, seed=300 + M, qview=True)
     assert gemm_violations(yv, y_ref, ad) == 0
@@ -227,7 +227,7 @@ def test_qview_gemm_odd_record_counts(w12, N, K, M):
 
 
 @pytest.mark.parametrize("N,K,M,qview", [(3000, 512, 32, False), (1000, 256, 1, False),
-                                         (3000, 512, 64, True), (129, 64, 5, False)])
+                                         (3000, 512, 64, True), (129, 64, 5, False), (2000, 256, 300, False)])
 def test_lmhead_argmax(w12, N, K, M, qview):
     w = synth.weights(N, K, synth.HEAD, seed=N + M, device="cuda")
     x = synth.activations(M, K, seed=N + M + 1, device="cuda")
@@ -241,7 +241,8 @@ def test_lmhead_argmax(w12, N, K, M, qview):
     checked, near, wrong, details = argmax_check(idx.cpu().numpy(), val.cpu().numpy(),
                                                  gap.cpu().numpy(), y_ref, ad)
     assert wrong == 0, details
-    assert checked + near == M and checked >= M - 2
+    # near-ties (gap under 1e-3 of the row's scale) are a property of the data: a few per 100 rows
+    assert checked + near == M and checked >= M - max(2, M // 25)
     # the gap is the difference of two GEMM outputs: within their summed bounds
     ridx, rval, rgap, _ = oracle.argmax(y_ref)
     g = gap.cpu().numpy().astype(np.float64)
@@ -329,3 +330,13 @@ def test_overlap_chain_in_cuda_graph(w12):
     assert torch.equal(gi, ref_i)
     w12.check(t1)
     w12.check(t2)
+
+
+def test_rows_above_limit_rejected(w12):
+    """M = 385 is outside [1, 384]: the call reports an unsupported shape and launches nothing."""
+    w = synth.weights(256, 128, synth.TINY, seed=61, device="cuda")
+    t = w12.encode(w)
+    x = synth.activations(385, 128, seed=62, device="cuda")
+    with pytest.raises(w12.W12Error) as e:
+        w12.gemm(t, x)
+    assert "shape" in str(e.value).lower()
