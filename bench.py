@@ -225,7 +225,7 @@ def main():
                          "finishes; weights are static); plain: ordinary stream-ordered launches")
     ap.add_argument("--profile-gemm", type=int, default=0, metavar="M",
                     help="only run `--steps` W12 GEMM launches at M rows on the projection (for ncu)")
-    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax"])
+    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax", "certified"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -418,10 +418,12 @@ def profile_gemm(args):
     build.build()
     dev = torch.device("cuda", 0)
     M = args.profile_gemm
-    N = VOCAB if args.profile_op == "argmax" else N_MLP
-    rec = synth.HEAD if args.profile_op == "argmax" else synth.PROJ
+    head = args.profile_op in ("argmax", "certified")
+    N = VOCAB if head else N_MLP
+    rec = synth.HEAD if head else synth.PROJ
     w = synth.weights(N, K_HID, rec, seed=synth.seed_for(1, 0), device=dev)
     t = w12.encode(w)
+    hq = w12.q8_build(w) if args.profile_op == "certified" else None
     del w
     copies = [t] + [t.clone_records() for _ in range(2 if N == N_MLP else 0)]
     x = synth.activations(M, K_HID, seed=synth.seed_for(1, 100 + M), device=dev)
@@ -432,6 +434,8 @@ def profile_gemm(args):
         a.record()
         if args.profile_op == "argmax":
             w12.lmhead_argmax(c, x)
+        elif args.profile_op == "certified":
+            w12.lmhead_certified(c, hq, x)
         else:
             w12.gemm(c, x, qview=args.profile_op == "qview")
         b.record()

@@ -30,7 +30,7 @@ namespace {
 
 constexpr int kQ8RecordBytes = W12_Q8_RECORD_BYTES;
 constexpr int kCap = W12_Q8_MAX_SURVIVORS;
-constexpr int kBoundThreads = 256;
+constexpr int kBoundThreads = 512;
 constexpr int kRescoreThreads = 256;
 constexpr int kRescoreWarps = kRescoreThreads / 32;
 constexpr int kRescoreBlocksPerRow = 8;
