@@ -33,7 +33,7 @@ constexpr int kCap = W12_Q8_MAX_SURVIVORS;
 constexpr int kBoundThreads = 512;
 constexpr int kRescoreThreads = 256;
 constexpr int kRescoreWarps = kRescoreThreads / 32;
-constexpr int kRescoreBlocksPerRow = 8;
+constexpr int kRescoreBlocksPerRow = 16;
 constexpr int kMaxRescoreK = 48 * 1024;  // x row in shared memory as fp32 (+1/64 padding): 195 KB
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
@@ -121,9 +121,16 @@ __global__ void __launch_bounds__(256) q8_build_kernel(const uint16_t *__restric
 template <int kBlock>
 __device__ float row_norm_up(const uint16_t *__restrict__ xm, int K, float *red) {
     float s = 0.f;
-    for (int k = threadIdx.x; k < K; k += kBlock) {
-        const float v = bf16_bits_to_float(xm[k]);
-        s = __fadd_ru(s, v * v);
+#pragma unroll 4
+    for (int c = threadIdx.x; c < K / 8; c += kBlock) {  // 16-byte pieces (K % 8 == 0)
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xm) + c);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = __uint_as_float(wv[j] << 16), b = __uint_as_float(wv[j] & 0xFFFF0000u);
+            s = __fadd_ru(s, a * a);
+            s = __fadd_ru(s, b * b);
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s = __fadd_ru(s, __shfl_xor_sync(0xFFFFFFFFu, s, off));
@@ -149,6 +156,7 @@ __global__ void __launch_bounds__(kBoundThreads) q8_bounds_kernel(const float *_
     const int n0 = static_cast<int>(static_cast<int64_t>(N) * b / nb);
     const int n1 = static_cast<int>(static_cast<int64_t>(N) * (b + 1) / nb);
     float l1 = -INFINITY, l2 = -INFINITY;
+#pragma unroll 4
     for (int n = n0 + threadIdx.x; n < n1; n += kBoundThreads) {
         const float lb = __fsub_rd(yh[static_cast<size_t>(m) * N + n], __fmul_ru(r, bound[n]));
         if (lb > l1) {
@@ -202,6 +210,7 @@ __global__ void __launch_bounds__(kBoundThreads) q8_select_kernel(const float *_
     const float r = rnorm[m], lm = L[m];
     const int n0 = static_cast<int>(static_cast<int64_t>(N) * b / nb);
     const int n1 = static_cast<int>(static_cast<int64_t>(N) * (b + 1) / nb);
+#pragma unroll 4
     for (int n = n0 + threadIdx.x; n < n1; n += kBoundThreads) {
         const float ub = __fadd_ru(yh[static_cast<size_t>(m) * N + n], __fmul_ru(r, bound[n]));
         if (ub >= lm) {
@@ -305,15 +314,24 @@ __device__ float exact_logit(const W12View &h, int n, const float *xs, int lane)
 // ... of the row (K % 8 == 0), and the lanes' sums are added by a fixed shuffle tree
 __device__ float exact_logit_bf16(const W12View &h, int n, const float *xs, int lane) {
     const uint4 *row = reinterpret_cast<const uint4 *>(h.wrow + static_cast<size_t>(n) * h.K);
+    const int pieces = h.K / 8;
     float acc = 0.f;
-    for (int c = lane; c < h.K / 8; c += 32) {
-        const uint4 v = __ldg(row + c);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+    // four pieces per lane in flight at a time
+    for (int c0 = lane; c0 < pieces; c0 += 128) {
+        uint4 v[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int k = 8 * c + 2 * j;
-            acc = fmaf(__uint_as_float(wv[j] << 16), xs[xs_index(k)], acc);
-            acc = fmaf(__uint_as_float(wv[j] & 0xFFFF0000u), xs[xs_index(k + 1)], acc);
+        for (int u = 0; u < 4; ++u) v[u] = (c0 + 32 * u < pieces) ? __ldg(row + c0 + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + 32 * u;
+            if (c >= pieces) break;
+            const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k = 8 * c + 2 * j;
+                acc = fmaf(__uint_as_float(wv[j] << 16), xs[xs_index(k)], acc);
+                acc = fmaf(__uint_as_float(wv[j] & 0xFFFF0000u), xs[xs_index(k + 1)], acc);
+            }
         }
     }
 #pragma unroll
@@ -343,8 +361,19 @@ __global__ void __launch_bounds__(kRescoreThreads) q8_rescore_kernel(W12View h, 
     const int m = blockIdx.y, nrb = gridDim.x, b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int kpad = h.k_tiles * 64;
-    for (int k = threadIdx.x; k < kpad; k += kRescoreThreads)
-        xs[xs_index(k)] = (k < h.K) ? bf16_bits_to_float(x[static_cast<size_t>(m) * h.K + k]) : 0.f;
+    // 16-byte pieces of the row (K % 8 == 0), several loads in flight per thread
+#pragma unroll 4
+    for (int c = threadIdx.x; c < kpad / 8; c += kRescoreThreads) {
+        const int k0 = 8 * c;
+        const uint4 v = (k0 < h.K) ? __ldg(reinterpret_cast<const uint4 *>(x + static_cast<size_t>(m) * h.K + k0))
+                                   : make_uint4(0, 0, 0, 0);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            xs[xs_index(k0 + 2 * j)] = __uint_as_float(wv[j] << 16);
+            xs[xs_index(k0 + 2 * j + 1)] = __uint_as_float(wv[j] & 0xFFFF0000u);
+        }
+    }
     __syncthreads();
     const uint32_t cnt = surv_cnt[m];
     float v1 = -INFINITY, v2 = -INFINITY;
