@@ -187,16 +187,22 @@ __global__ void __launch_bounds__(kBoundThreads) q8_bounds_kernel(const float *_
         last = atomicAdd(&row_cnt[m], 1u) == static_cast<uint32_t>(nb - 1);
     }
     __syncthreads();
-    if (last && threadIdx.x == 0) {
+    if (last && threadIdx.x < 32) {
+        // the slices' results, loaded by the lanes together (nb <= 64), merged by a shuffle tree
         __threadfence();
         float a1 = -INFINITY, a2 = -INFINITY;
-        for (int i = 0; i < nb; ++i) {
+        for (int i = threadIdx.x; i < nb; i += 32) {
             const float2 t = __ldcg(&lb_top[static_cast<size_t>(m) * nb + i]);
             merge(a1, a2, t.x, t.y);
         }
-        L[m] = a2;
-        rnorm[m] = r;
-        row_cnt[m] = 0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+            merge(a1, a2, __shfl_xor_sync(0xFFFFFFFFu, a1, off), __shfl_xor_sync(0xFFFFFFFFu, a2, off));
+        if (threadIdx.x == 0) {
+            L[m] = a2;
+            rnorm[m] = r;
+            row_cnt[m] = 0;
+        }
     }
 }
 
@@ -399,14 +405,24 @@ __global__ void __launch_bounds__(kRescoreThreads) q8_rescore_kernel(W12View h, 
         last = atomicAdd(&res_cnt[m], 1u) == static_cast<uint32_t>(nrb - 1);
     }
     __syncthreads();
-    if (last && threadIdx.x == 0) {
+    float a1 = -INFINITY, a2 = -INFINITY;
+    int ai = 0x7FFFFFFF;
+    if (last && threadIdx.x < 32) {
+        // the blocks' results, loaded by the lanes together, merged by a shuffle tree (the top-2
+        // of a set does not depend on the merge order)
         __threadfence();
-        float a1 = -INFINITY, a2 = -INFINITY;
-        int ai = 0x7FFFFFFF;
-        for (int i = 0; i < nrb; ++i) {
+        for (int i = threadIdx.x; i < nrb; i += 32) {
             const float4 t = __ldcg(&res_top[static_cast<size_t>(m) * nrb + i]);
             top2_add(a1, ai, a2, t.x, __float_as_int(t.y), t.z);
         }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float o1 = __shfl_xor_sync(0xFFFFFFFFu, a1, off), o2 = __shfl_xor_sync(0xFFFFFFFFu, a2, off);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, ai, off);
+            top2_add(a1, ai, a2, o1, oi, o2);
+        }
+    }
+    if (last && threadIdx.x == 0) {
         if (cnt <= static_cast<uint32_t>(kCap)) {
             idx[m] = ai;
             val[m] = a1;
