@@ -55,6 +55,7 @@ constexpr int kWarpMma2 = 3;  // second MMA issuer (the second record of each sl
 constexpr int kWarpEpi0 = 4;
 constexpr int kWarpDec0 = 8;
 constexpr int kEscCap = 128;       // index words staged per slot; more -> read from global
+constexpr int kStageBufs = 2;      // tensor-store staging buffers per epilogue warp
 constexpr int kACols = 32;         // tensor-memory columns of one decoded record (64 bf16/lane)
 constexpr int kMaxStages = 8;
 constexpr int kMaxM = W12_MAX_M;
@@ -96,9 +97,12 @@ struct Ctrl {
 // per-warp top-2 of each row (4 x M float4) and the block's running top-2 (M float4); in the
 // GEMM variants the staging buffers of the tensor stores of y (4 warps x 2 x 16 x 32 words).
 constexpr size_t kCtrlBytes = (sizeof(Ctrl) + 127) / 128 * 128;
-constexpr size_t kStagingBytes = 4 * 2 * 16 * 32 * 4;
-__host__ __device__ constexpr size_t scratch_bytes(int M) {
-    return (80 * static_cast<size_t>(M) > kStagingBytes) ? 80 * static_cast<size_t>(M) : kStagingBytes;
+constexpr size_t kStagingBytes = 4 * kStageBufs * 16 * 32 * 4;
+// the argmax variants need their top-2 records, the GEMM variants the tensor-store staging
+// (tensor stores of y measured faster than plain stores at every row count: at M=192 plain
+// stores and the sixth ring slot they free cost 6 us a launch)
+constexpr size_t scratch_bytes(int M, bool argmax) {
+    return argmax ? 80 * static_cast<size_t>(M) : kStagingBytes;
 }
 
 struct Params {
@@ -676,9 +680,9 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
           if constexpr (!kArgmax) {
             if (!part && p.y_tma) {
                 const int esz = p.y_bf16 ? 2 : 4;
-                uint8_t *stg = scratch + (qw * 2 + ybuf) * 16 * 32 * esz;
-                ybuf ^= 1;
-                if (lane == 0) bulk_wait_group_read<1>();  // the store that last read this buffer
+                uint8_t *stg = scratch + (qw * kStageBufs + ybuf) * 16 * 32 * esz;
+                ybuf = (ybuf + 1) % kStageBufs;
+                if (lane == 0) bulk_wait_group_read<kStageBufs - 1>();  // the store that last read this buffer
                 __syncwarp();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -1087,7 +1091,8 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     const int rstride = (L->vtma || L->packed) ? kViewBytes : kRecordBytes;
     const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * rstride + (q ? kViewBytes : kRecordBytes) +
                        (q ? 0 : kEscCap * 4);
-    const int ctrl = static_cast<int>(align_up(kCtrlBytes + scratch_bytes(M), 1024));
+    const bool am = (op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8Argmax);
+    const int ctrl = static_cast<int>(align_up(kCtrlBytes + scratch_bytes(M, am), 1024));
     int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
     if (stages > kMaxStages) stages = kMaxStages;
     // tensor memory: nacc accumulators of npad columns, then 32 columns per record in flight
