@@ -59,6 +59,9 @@ def _load():
         lib.w12o_threads.restype = i32
         lib.w12o_head_q8.argtypes = [P, i32, i32, P, P, P, P]
         lib.w12o_certified_argmax.argtypes = [P, i32, P, i32, i32, P, P, P, P, P, P, P]
+        lib.w12o_copy_q6.argtypes = [P, i32, i32, P, P]
+        lib.w12o_q6_pack.argtypes = [P, i32, i32, P]
+        lib.w12o_gemm_q6.argtypes = [P, i32, P, P, i32, i32, P]
         _lib = lib
     return _lib
 
@@ -234,3 +237,40 @@ def certified_argmax(x, w, h: HeadQ8):
     _load().w12o_certified_argmax(_p(x), M, _p(w), N, K, _p(h.scale), _p(np.ascontiguousarray(h.q)),
                                   _p(h.resid), _p(idx), _p(val), _p(gap), _p(cnt))
     return idx, val, gap, cnt
+
+
+@dataclass
+class CopyQ6:
+    """The INT6 Q-pass copy (SpecPilot §5.3, App. C): row scales and row-major codes."""
+
+    scale: np.ndarray  # float32 [N]
+    q: np.ndarray      # int8 [N, K], in [-31, 31]
+
+
+def copy_q6(w) -> CopyQ6:
+    w = _u16(w)
+    N, K = w.shape
+    scale = np.zeros(N, dtype=np.float32)
+    q = np.zeros((N, K), dtype=np.int8)
+    _load().w12o_copy_q6(_p(w), N, K, _p(scale), _p(q))
+    return CopyQ6(scale, q)
+
+
+def q6_pack(q: np.ndarray) -> np.ndarray:
+    """The INT6 copy's 6144-byte records (uint8 [n_tiles * k_tiles * 6144]) from row-major codes."""
+    q = np.ascontiguousarray(q, dtype=np.int8)
+    N, K = q.shape
+    nt, kt = (N + TILE_N - 1) // TILE_N, (K + TILE_K - 1) // TILE_K
+    rec = np.zeros(nt * kt * 6144, dtype=np.uint8)
+    _load().w12o_q6_pack(_p(q), N, K, _p(rec))
+    return rec
+
+
+def gemm_q6(x, c: CopyQ6) -> np.ndarray:
+    """yq [M, N] = s_n (x . c_n) in fp64."""
+    x = _u16(x)
+    M, K = x.shape
+    N = c.q.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    _load().w12o_gemm_q6(_p(x), M, _p(np.ascontiguousarray(c.q)), _p(c.scale), N, K, _p(y))
+    return y

@@ -20,6 +20,8 @@
  *     Fig. 7.
  *   - certified LM head (INT8 copy, per-row Cauchy-Schwarz bound, exact rescoring of the
  *     survivors): [SP] §4.1 "Certified LM head".
+ *   - INT6 Q-pass copy (per-row scale, 6-bit codes, its GEMM): [SP] §5.3 "Generality Through
+ *     Memory"; App. C.
  *
  * Physical details the pages leave open (window tie rule, placeholders, byte and nibble order,
  * per-record escape index) follow the build's written W12 specification; every function states
@@ -461,4 +463,96 @@ void w12o_certified_argmax(const uint16_t *x, int M, const uint16_t *w, int N, i
         n_surv[m] = cnt;
     }
     free(yh);
+}
+
+/* ---- INT6 Q-pass copy -------------------------------------------------------------------
+ * [SP] §5.3 ("DSpark also added the INT6 copy for the Q pass"; "an INT6/INT8 Q-pass copy") and
+ * App. C (the Q pass reads the nested 8-bit view or a separate low-precision copy). The pages
+ * give no formulas; the plainest reading, fixed in the build's written specification, is the
+ * INT8 copy's per-row symmetric quantisation with 6-bit codes:
+ *   scale   s_n = fp32(max_k |w[n,k]| / 31)  (0 for an all-zero row and for a row holding Inf
+ *                                             or NaN, whose codes are then all 0)
+ *   code    c[n,k] = round-half-even(w[n,k] / s_n), clamped to [-31, 31]
+ *   Q pass  yq[m,n] = s_n sum_k x[m,k] c[n,k]
+ */
+void w12o_copy_q6(const uint16_t *w, int N, int K, float *scale, int8_t *q) {
+    #pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        const uint16_t *row = w + (size_t)n * K;
+        int finite = 1;
+        double amax = 0.0;
+        for (int k = 0; k < K; ++k) {
+            if (bf_exp(row[k]) == 255) finite = 0;
+            double a = fabs(w12o_bf16_to_double(row[k]));
+            if (a > amax) amax = a;
+        }
+        int8_t *qr = q + (size_t)n * K;
+        if (!finite || amax == 0.0) {
+            scale[n] = 0.0f;
+            for (int k = 0; k < K; ++k) qr[k] = 0;
+            continue;
+        }
+        const float s = (float)(amax / 31.0);
+        for (int k = 0; k < K; ++k) {
+            double t = nearbyint(w12o_bf16_to_double(row[k]) / (double)s);  /* ties to even */
+            if (t > 31.0) t = 31.0;
+            if (t < -31.0) t = -31.0;
+            qr[k] = (int8_t)t;
+        }
+        scale[n] = s;
+    }
+}
+
+/* The INT6 copy's records, from row-major codes c [N,K] (build's specification). One record
+ * per 128 x 64 tile, record r = n_tile * k_tiles + k_tile, 6144 bytes, holding u = c + 32
+ * (1..63; padding rows and columns hold code 0, u = 32) as two planes of 32-bit little-endian
+ * words. For local row n_l, k_l = 16 g + 2 j + h (group g 0..3, pair j 0..7, half h 0..1):
+ *   plane L (bytes 0..4095), the low four bits of u:  word 2g + (j >> 2) of the row, where row
+ *     words 0..3 sit at byte 16 n_l + 4 i and words 4..7 at 2048 + 16 n_l + 4 (i - 4);
+ *     bits 4 (j & 3) + 16 h .. +3
+ *   plane T (bytes 4096..6143), the top two bits of u: word g of the row at byte
+ *     4096 + 16 n_l + 4 g; bits 2 j + 16 h .. +1 */
+void w12o_q6_pack(const int8_t *q, int N, int K, uint8_t *records) {
+    const int nt_n = (N + W12O_TILE_N - 1) / W12O_TILE_N, kt_n = (K + W12O_TILE_K - 1) / W12O_TILE_K;
+    #pragma omp parallel for schedule(static)
+    for (int nt = 0; nt < nt_n; ++nt) {
+        for (int kt = 0; kt < kt_n; ++kt) {
+            uint8_t *rec = records + ((size_t)nt * kt_n + kt) * 6144;
+            uint32_t words[128][12];
+            for (int nl = 0; nl < 128; ++nl)
+                for (int i = 0; i < 12; ++i) words[nl][i] = 0;
+            for (int nl = 0; nl < 128; ++nl) {
+                for (int kl = 0; kl < 64; ++kl) {
+                    const int n = nt * 128 + nl, k = kt * 64 + kl;
+                    const int c = (n < N && k < K) ? q[(size_t)n * K + k] : 0;
+                    const uint32_t u = (uint32_t)(c + 32);
+                    const int g = kl >> 4, j = (kl & 15) >> 1, h = kl & 1;
+                    words[nl][2 * g + (j >> 2)] |= (u & 15u) << (4 * (j & 3) + 16 * h);
+                    words[nl][8 + g] |= (u >> 4) << (2 * j + 16 * h);
+                }
+            }
+            for (int nl = 0; nl < 128; ++nl) {
+                for (int i = 0; i < 12; ++i) {
+                    size_t off;
+                    if (i < 4) off = (size_t)16 * nl + 4 * i;
+                    else if (i < 8) off = 2048 + (size_t)16 * nl + 4 * (i - 4);
+                    else off = 4096 + (size_t)16 * nl + 4 * (i - 8);
+                    for (int b = 0; b < 4; ++b) rec[off + b] = (uint8_t)(words[nl][i] >> (8 * b));
+                }
+            }
+        }
+    }
+}
+
+/* yq [M,N] = s_n sum_k x[m,k] c[n,k], in fp64 (each product is exact). */
+void w12o_gemm_q6(const uint16_t *x, int M, const int8_t *q, const float *scale, int N, int K, double *y) {
+    #pragma omp parallel for schedule(static)
+    for (int n = 0; n < N; ++n) {
+        for (int m = 0; m < M; ++m) {
+            double acc = 0.0;
+            for (int k = 0; k < K; ++k)
+                acc += w12o_bf16_to_double(x[(size_t)m * K + k]) * (double)q[(size_t)n * K + k];
+            y[(size_t)m * N + n] = (double)scale[n] * acc;
+        }
+    }
 }

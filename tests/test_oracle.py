@@ -10,7 +10,10 @@
   the encoded records;
 - the certified LM head (SpecPilot §4.1): quantisation properties of the INT8 copy, the
   Cauchy-Schwarz bound against the exact GEMM, and the certified argmax against the brute-force
-  argmax over the whole head (random heads, exact ties, Inf rows).
+  argmax over the whole head (random heads, exact ties, Inf rows);
+- the INT6 Q-pass copy (SpecPilot §5.3, App. C): quantisation properties, hand-derived record
+  bytes, a record reader written from the bit layout, and the lossless case of its GEMM against
+  the exact GEMM.
 """
 import math
 import os
@@ -408,3 +411,106 @@ def test_certified_argmax_ties_and_special_rows(orc):
             assert idx[m] == 99 and val[m] == rval[m]
         else:
             assert idx[m] == ridx[m] and val[m] == rval[m] and gap[m] == rgap[m]
+
+
+# ---------------------------------------------------------------- INT6 Q-pass copy
+
+def test_copy_q6_quantisation_properties(orc):
+    """Codes lie in [-31, 31]; the largest |w| of a row codes to +-31; every weight is within half
+    a step of its code; the scale is the row maximum over 31 in fp32; zero rows and rows holding
+    Inf/NaN get scale 0 and code 0."""
+    w = _head(64, 96, seed=14)
+    w[3] = 0                      # all-zero row
+    w[5, 7] = 0x7F80              # +Inf
+    w[6, 9] = 0x7FC1              # NaN
+    w[7, :] = 0x3F80              # all 1.0
+    c = orc.copy_q6(w)
+    v = bf16_values(w)
+    assert np.all(np.abs(c.q.astype(np.int32)) <= 31)
+    for n in range(64):
+        amax = np.abs(v[n]).max() if n not in (5, 6) else np.inf
+        if n in (3, 5, 6):
+            assert c.scale[n] == 0 and not np.any(c.q[n])
+            continue
+        assert c.scale[n] == np.float32(amax / 31.0)
+        s = float(c.scale[n])
+        e = v[n] - s * c.q[n].astype(np.float64)
+        assert np.all(np.abs(e) <= s / 2 * (1 + 1e-12) + abs(amax - 31 * s))
+        assert abs(int(c.q[n, int(np.argmax(np.abs(v[n])))])) == 31
+    # ties go to the even code: a row whose maximum is 7.75 = 31 * 2^-2 has scale 2^-2
+    row = np.zeros((1, 64), np.uint16)
+    row[0, 0] = 0x40F8            # 7.75 -> 31
+    row[0, 1] = 0x3F20            # 0.625 = 2.5 * 2^-2 -> 2
+    row[0, 2] = 0x3F60            # 0.875 = 3.5 * 2^-2 -> 4
+    row[0, 3] = 0xBFB0            # -1.375 = -5.5 * 2^-2 -> -6
+    row[0, 4] = 0x3FE0            # 1.75 = 7 * 2^-2 -> 7
+    c = orc.copy_q6(row)
+    assert c.scale[0] == 0.25 and list(c.q[0, :5]) == [31, 2, 4, -6, 7]
+
+
+def _q6_read_records(rec, N, K):
+    """Codes [N, K] read back from INT6 records by the stated bit layout (independent of the
+    oracle's packer): per 128-row, 64-column tile a 6144-byte record; per local row twelve 32-bit
+    little-endian words, eight of low nibbles (words 0-3 at byte 16 n_l, words 4-7 at 2048 +
+    16 n_l) and four of top bit pairs (at 4096 + 16 n_l); k_l = 16 g + 2 j + h."""
+    nt, kt = (N + 127) // 128, (K + 63) // 64
+    out = np.zeros((nt * 128, kt * 64), dtype=np.int16)
+    b = rec.reshape(nt * kt, 6144)
+    for r in range(nt * kt):
+        t, k0 = divmod(r, kt)
+        lo = np.concatenate([b[r, :2048].reshape(128, 16), b[r, 2048:4096].reshape(128, 16)], axis=1)
+        lo = lo.view("<u4")                                   # [128, 8]
+        hi = b[r, 4096:].reshape(128, 16).view("<u4")         # [128, 4]
+        for kl in range(64):
+            g, j, h = kl >> 4, (kl & 15) >> 1, kl & 1
+            low = (lo[:, 2 * g + (j >> 2)] >> (4 * (j & 3) + 16 * h)) & 15
+            top = (hi[:, g] >> (2 * j + 16 * h)) & 3
+            out[t * 128:(t + 1) * 128, k0 * 64 + kl] = (low | (top << 4)).astype(np.int16) - 32
+    return out
+
+
+def test_q6_records_hand_fixture(orc):
+    """One record whose only nonzero code is c = -3 at n_l = 5, k_l = 37. Every other position
+    holds u = 32 (low nibble 0, top bits 10b): plane L is zero and every plane-T word is
+    0xAAAAAAAA. u = 29 = 01 1101b; k_l = 37 is g 2, j 2, h 1: its low nibble 0xD goes to L word
+    4 of row 5 (byte 2048 + 80), bits 24-27, i.e. byte 2131 = 0x0D; its top bits 01 go to T word
+    2 of row 5 (byte 4096 + 80 + 8 = 4184), bits 20-21: the word becomes 0xAA9AAAAA, i.e. byte
+    4186 = 0x9A."""
+    q = np.zeros((128, 64), dtype=np.int8)
+    q[5, 37] = -3
+    rec = orc.q6_pack(q)
+    want = np.zeros(6144, dtype=np.uint8)
+    want[4096:] = 0xAA
+    want[2131] = 0x0D
+    want[4186] = 0x9A
+    assert np.array_equal(rec, want)
+
+
+@pytest.mark.parametrize("N,K", [(128, 64), (300, 200), (129, 8)])
+def test_q6_records_round_trip(orc, N, K):
+    """Random codes in [-31, 31] read back unchanged from the records, and padding holds code 0."""
+    rng = np.random.default_rng(N + K)
+    q = rng.integers(-31, 32, size=(N, K)).astype(np.int8)
+    back = _q6_read_records(orc.q6_pack(q), N, K)
+    assert np.array_equal(back[:N, :K], q)
+    assert not np.any(back[N:]) and not np.any(back[:, K:])
+
+
+def test_gemm_q6_lossless_case_is_the_exact_gemm(orc):
+    """Rows whose weights are integers times 2^-e with a maximum of 31 * 2^-e quantise without
+    loss (scale 2^-e, codes the integers), so the Q6 GEMM equals the exact fp64 GEMM bit for bit
+    (scaling by a power of two commutes with every rounding)."""
+    rng = np.random.default_rng(21)
+    N, K, M = 40, 128, 5
+    ints = rng.integers(-31, 32, size=(N, K))
+    ints[:, 0] = 31
+    e = rng.integers(2, 12, size=N)
+    wv = (ints * (2.0 ** -e)[:, None]).astype(np.float32)
+    w = (wv.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(bf16_values(w), wv.astype(np.float64))
+    x = synth.activations(M, K, seed=22).view(torch.int16).numpy().view(np.uint16)
+    c = orc.copy_q6(w)
+    assert np.array_equal(c.scale.astype(np.float64), 2.0 ** -e)
+    assert np.array_equal(c.q, ints.astype(np.int8))
+    y, _ = orc.gemm(x, w)
+    assert np.array_equal(orc.gemm_q6(x, c), y)
