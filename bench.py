@@ -225,7 +225,7 @@ def main():
                          "finishes; weights are static); plain: ordinary stream-ordered launches")
     ap.add_argument("--profile-gemm", type=int, default=0, metavar="M",
                     help="only run `--steps` W12 GEMM launches at M rows on the projection (for ncu)")
-    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax", "certified"])
+    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax", "certified", "q6"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -424,6 +424,7 @@ def profile_gemm(args):
     w = synth.weights(N, K_HID, rec, seed=synth.seed_for(1, 0), device=dev)
     t = w12.encode(w)
     hq = w12.q8_build(w) if args.profile_op == "certified" else None
+    q6 = [w12.q6_build(w) for _ in range(3)] if args.profile_op == "q6" else None
     del w
     copies = [t] + [t.clone_records() for _ in range(2 if N == N_MLP else 0)]
     x = synth.activations(M, K_HID, seed=synth.seed_for(1, 100 + M), device=dev)
@@ -436,6 +437,8 @@ def profile_gemm(args):
             w12.lmhead_argmax(c, x)
         elif args.profile_op == "certified":
             w12.lmhead_certified(c, hq, x)
+        elif args.profile_op == "q6":
+            w12.q6_gemm(q6[i % 3], x)
         else:
             w12.gemm(c, x, qview=args.profile_op == "qview")
         b.record()
@@ -528,6 +531,18 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
                     "M192_us": round(q192, 2), "M192_tflops": round(fl / (q192 * 1e-6) / 1e12, 1)}
     out["m192_exact"] = {"us": round(e192, 2), "tflops": round(fl / (e192 * 1e-6) / 1e12, 1),
                          "frac_tensor_peak": round(fl / (e192 * 1e-6) / 1e12 / tc_peak, 3)}
+    # the separate INT6 Q-pass copy of the projection (0.75 B per weight), rotating copies
+    qc = [w12.q6_build(w)]
+    qc += [w12.Q6Copy(N_MLP, K_HID, device=dev) for _ in range(3)]
+    for c in qc[1:]:
+        c.codes.copy_(qc[0].codes)
+        c.scale.copy_(qc[0].scale)
+    q6_32 = _time(lambda i: w12.q6_gemm(qc[i % 4], xs[32], out=yf[32], overlap=True), reps=15)
+    q6_192 = _time(lambda i: w12.q6_gemm(qc[i % 4], x192, out=yf[192], overlap=True), reps=15)
+    out["q6_copy"] = {"copy_mb": round(qc[0].nbytes / 1e6, 1),
+                      "M32_overlap_us": round(q6_32, 2), "M32_gbs": round(qc[0].nbytes / (q6_32 * 1e-6) / 1e9, 1),
+                      "M192_overlap_us": round(q6_192, 2), "M192_tflops": round(fl / (q6_192 * 1e-6) / 1e12, 1)}
+    del qc
     # encode and verify (load time), bf16 GB/s read
     enc_us = _time(lambda i: w12.encode(w), reps=3, warm=1)
     ver_us = _time(lambda i: w12.verify(t0, w), reps=3, warm=1)
@@ -564,6 +579,11 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
     out["certified_head"] = {"q8_copy_gb": round(hq.nbytes / 1e9, 3), "q8_build_ms": round(q8_build_ms, 1),
                              "by_m": cert, "q8_qpass_argmax_overlap_us_M32": round(q8_us, 1)}
     del hq
+    h6 = w12.q6_build(wh)
+    q6_us = _time(lambda i: w12.q6_argmax(h6, xh, overlap=True), reps=10)
+    out["q6_copy"]["lmhead_argmax_overlap_us_M32"] = round(q6_us, 1)
+    out["q6_copy"]["lmhead_copy_gb"] = round(h6.nbytes / 1e9, 3)
+    del h6
     w12.check(th)
     out["lmhead"] = {"M": 32, "us": round(a_us, 1), "rows_per_s": round(32 / (a_us * 1e-6), 1),
                      "weight_gbs": round(th.gemm_bytes() / (a_us * 1e-6) / 1e9, 1),

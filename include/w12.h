@@ -278,6 +278,59 @@ w12_status w12_q8_argmax_workspace_size(const w12_q8_head *h, int M, size_t *byt
 w12_status w12_q8_argmax(const w12_q8_head *h, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,
                          unsigned flags, void *workspace, size_t workspace_bytes, w12_stream_t stream);
 
+/* ---- INT6 Q-pass copy (SpecPilot §5.3 "Generality Through Memory": the INT6 copy added for
+ *      the Q pass, and the INT6/INT8 Q-pass copy; App. C: the Q pass reads the nested 8-bit
+ *      view or a separate low-precision copy) -------------------------------------------------
+ * A separate 6-bit copy of a weight matrix for the low-precision Q pass: 0.75 bytes per weight
+ * against the nested view's 1.0 and W12's 1.5. The pages give no formulas; the copy here is
+ * the INT8 copy's per-row symmetric quantisation with 6-bit codes. Per output row n of the bf16
+ * matrix W [N, K]:
+ *   scale[n] = max_k |W[n,k]| / 31 rounded to fp32 (0 for an all-zero row, a padding row, or a
+ *              row holding Inf or NaN; that row's codes are 0)
+ *   c[n,k]   = W[n,k] / scale[n] rounded to the nearest integer (ties to even), clamped to +-31
+ * and the Q pass computes yq[m,n] = scale[n] * sum_k x[m,k] c[n,k] with fp32 accumulation.
+ * Records: one per 128 x 64 tile (record r = nt * k_tiles + kt), 6144 bytes, holding u = c + 32
+ * (padding rows and columns hold u = 32) in 32-bit little-endian words. For local row n_l and
+ * k_l = 16 g + 2 j + h (group g 0..3, pair j 0..7, half h 0..1):
+ *   plane L, bytes [0, 4096): the low four bits of u, in row word i = 2 g + (j >> 2) at bits
+ *     4 (j & 3) + 16 h; row words 0-3 lie at byte 16 n_l + 4 i, words 4-7 at 2048 + 16 n_l + 4 (i - 4)
+ *   plane T, bytes [4096, 6144): the top two bits of u, in row word g at byte 4096 + 16 n_l + 4 g,
+ *     bits 2 j + 16 h
+ */
+typedef struct {
+    int32_t N, K;
+    int32_t n_tiles, k_tiles;
+    uint8_t *codes;  /* [n_tiles * k_tiles * 6144] */
+    float *scale;    /* [n_tiles * 128] */
+} w12_q6_copy;
+
+enum { W12_Q6_RECORD_BYTES = 6144 };
+
+/* Fills c->N, K, n_tiles, k_tiles and returns the byte sizes of codes and of scale. Host only. */
+w12_status w12_q6_shape(int N, int K, w12_q6_copy *c, size_t *codes_bytes, size_t *scale_bytes);
+
+/* Builds the copy from the bf16 matrix w [c->N, c->K] (device, row-major, 16-byte aligned) into
+ * the caller's buffers. Asynchronous. */
+w12_status w12_q6_build(const uint16_t *w, const w12_q6_copy *c, w12_stream_t stream);
+
+/* Workspace bytes of w12_q6_gemm (argmax = 0) or w12_q6_argmax (argmax != 0) at M rows. The
+ * workspace must be zero-filled once before its first use; every call leaves it zeroed. Calls
+ * that share a workspace must not overlap on the GPU. Host only. */
+w12_status w12_q6_workspace_size(const w12_q6_copy *c, int M, int argmax, size_t *bytes);
+
+/* yq = x . (scale * c)^T as above: x device bf16 [M, K] (16-byte aligned), y [M, N] fp32 or
+ * bf16 (round to nearest even) by y_dtype. flags: 0 or W12_LAUNCH_OVERLAP (as for w12_gemm_ex:
+ * the copy's buffers must hold their final contents when the preceding kernel starts).
+ * Asynchronous. */
+w12_status w12_q6_gemm(const w12_q6_copy *c, const uint16_t *x, int M, void *y, int y_dtype, unsigned flags,
+                       void *workspace, size_t workspace_bytes, w12_stream_t stream);
+
+/* The Q pass's row argmax over the copy: idx / val / gap (device, [M]) of each row of yq,
+ * computed like w12_lmhead_argmax (ties to the smaller index, NaN not ranked). flags: 0 or
+ * W12_LAUNCH_OVERLAP. Asynchronous. */
+w12_status w12_q6_argmax(const w12_q6_copy *c, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,
+                         unsigned flags, void *workspace, size_t workspace_bytes, w12_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -116,7 +116,7 @@ struct Params {
     int y_tma;    // y is written by tiled tensor stores through ymap
     int v_tma;    // Q view: a slot's two record views arrive by one tiled copy through vmap
     int xhalf;    // more than 256 rows: rows per activation box and per MMA (npad / 2), else 0
-    const float *row_scale;  // INT8 copy: per-channel scale, [n_tiles * 128]
+    const float *row_scale;  // INT8 / INT6 copy: per-channel scale, [n_tiles * 128]
     int *run_flag;           // if set, the launch does nothing unless *run_flag != 0 (then clears it)
     int x_pair;   // xmap2 loads the k-slices of two consecutive records in one copy
     int test_stall;  // W12_LAUNCH_TEST_STALL: the producer fills only the first slot
@@ -218,9 +218,10 @@ __device__ __forceinline__ void warp_top2_rows16(float (&v1)[16], int (&i1)[16],
     top2_merge(v1[0], i1[0], v2[0], rv1, ri1, rv2);
 }
 
-// kQ8: the certified head's INT8 copy (8 KB records of sign-magnitude codes, no escapes; each
-// output channel's accumulator is multiplied by its row scale)
-template <bool kQView, bool kArgmax, bool kQ8 = false>
+// kPack: 0 = W12 records; 8 = the INT8 copy (8 KB records of sign-magnitude codes); 6 = the
+// INT6 copy (6 KB records of offset codes in two planes). The copies have no escapes, and each
+// output channel's accumulator is multiplied by its row scale.
+template <bool kQView, bool kArgmax, int kPack = 0>
 __global__ void __launch_bounds__(kThreads, 1)
 w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap xmap2,
                 const __grid_constant__ CUtensorMap ymap, const __grid_constant__ CUtensorMap vmap, const Params p) {
@@ -237,15 +238,19 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
 
     const int S = p.stages, RPS = p.rps;
     const int xbytes = p.npad * 128;
-    static_assert(!kQ8 || kQView, "the INT8 copy is read like a view: no plane B, no escapes");
-    constexpr int rbytes = kQView ? kViewBytes : kRecordBytes;
+    constexpr bool kCopy = kPack != 0;  // a separate low-precision copy (INT8 or INT6)
+    static_assert(kPack == 0 || kPack == 6 || kPack == 8, "W12 records, the INT8 or the INT6 copy");
+    static_assert(!kCopy || kQView, "the copies are read like a view: no plane B, no escapes");
+    constexpr int rbytes = (kPack == 6) ? kQ6RecordBytes : (kQView ? kViewBytes : kRecordBytes);
     constexpr int ebytes = kQView ? 0 : kEscCap * 4;
-    constexpr int gstride = kQ8 ? kViewBytes : kRecordBytes;  // distance between records in memory
+    // distance between records in memory
+    constexpr int gstride = (kPack == 6) ? kQ6RecordBytes : (kCopy ? kViewBytes : kRecordBytes);
     // A slot's records arrive by one copy: whole records as one contiguous range; for the Q view
     // the two records' views by one tiled copy that skips the B planes between them (vmap), else
     // the range from the first record's view to the end of the last one's.
     const bool vtma = kQView && p.v_tma;
-    const int rstride = (vtma || kQ8) ? kViewBytes : kRecordBytes;  // shared-memory distance between records
+    // shared-memory distance between records
+    const int rstride = (kPack == 6) ? kQ6RecordBytes : ((vtma || kCopy) ? kViewBytes : kRecordBytes);
     const int recs_bytes = (RPS - 1) * rstride + rbytes;
     const int sbytes = RPS * xbytes + recs_bytes + ebytes;
     Ctrl *ctrl = reinterpret_cast<Ctrl *>(smem + S * sbytes);
@@ -362,7 +367,7 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
     };
     int en_tile = r0 / KT;
     uint32_t en_cur = 0, en_nxt = 0;
-    if (!kQ8 && warp >= kWarpDec0) {
+    if (!kCopy && warp >= kWarpDec0) {
         en_cur = en_load(en_tile);
         en_nxt = en_load(en_tile + 1);
     }
@@ -533,11 +538,22 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         // decode this thread's row of record q of slot s into w (escapes patched)
         auto decode_record = [&](int s, int q, uint32_t base2, uint32_t (&w)[32]) {
             const uint8_t *rec = stage_rec(s, q);
+            if constexpr (kPack == 6) {
+                // plane L words 0-3 (groups 0, 1) and 4-7 (groups 2, 3), then plane T words 0-3
+                const uint4 l0 = lds128(rec + 16 * nl);
+                const uint4 l1 = lds128(rec + 2048 + 16 * nl);
+                const uint4 tw = lds128(rec + 4096 + 16 * nl);
+                decode_q6_group16(l0.x, l0.y, tw.x, w);
+                decode_q6_group16(l0.z, l0.w, tw.y, w + 8);
+                decode_q6_group16(l1.x, l1.y, tw.z, w + 16);
+                decode_q6_group16(l1.z, l1.w, tw.w, w + 24);
+                return;
+            }
             const uint4 v0 = lds128(rec + 0 * 2048 + 16 * nl);
             const uint4 v1 = lds128(rec + 1 * 2048 + 16 * nl);
             const uint4 v2 = lds128(rec + 2 * 2048 + 16 * nl);
             const uint4 v3 = lds128(rec + 3 * 2048 + 16 * nl);
-            if (kQ8) {
+            if constexpr (kPack == 8) {
                 decode_q8_chunk16(v0, w);
                 decode_q8_chunk16(v1, w + 8);
                 decode_q8_chunk16(v2, w + 16);
@@ -610,12 +626,12 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             const int nr = min(RPS, nrec - js * RPS);
             // the slot's tensor-memory buffers are free: the producer refilled this slot only
             // after the MMAs that last read it completed
-            decode_record(s, 0, kQ8 ? 0u : base2_for(tile), wa);
+            decode_record(s, 0, kCopy ? 0u : base2_for(tile), wa);
             tc_fence_after();
             tmem_st_32x32b_x32(a_slot(s, 0) + (static_cast<uint32_t>(32 * qw) << 16), wa);
             if (nr == 2) {
                 const int tile1 = (kt + 1 == p.k_tiles) ? tile + 1 : tile;
-                decode_record(s, 1, kQ8 ? 0u : base2_for(tile1), wb);
+                decode_record(s, 1, kCopy ? 0u : base2_for(tile1), wb);
                 tmem_st_32x32b_x32(a_slot(s, 1) + (static_cast<uint32_t>(32 * qw) << 16), wb);
             }
             tmem_wait_st();
@@ -728,10 +744,11 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                     emit(m0 + i, tile * kTileN + nl, f[i]);
             }
         };
-        // INT8 copy: a block's accumulator values are multiplied by their channel's row scale as
-        // they leave tensor memory, so partials, their sums and y all carry the scale once
+        // the INT8 and INT6 copies: a block's accumulator values are multiplied by their channel's
+        // row scale as they leave tensor memory, so partials, their sums and y all carry the scale
+        // once
         auto scale_rows = [&](int tile, float (&f)[16]) {
-            if constexpr (kQ8) {
+            if constexpr (kCopy) {
                 const float sc = p.row_scale[tile * kTileN + nl];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) f[i] *= sc;
@@ -1043,24 +1060,31 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // internal operations over the INT8 head copy (reached through the certified-head entry points)
 constexpr int kOpQ8 = 100;        // y = scale_n (x . q_n)
 constexpr int kOpQ8Argmax = 101;  // its row argmax (the Q pass over the separate copy)
+// and over the INT6 Q-pass copy (w12_q6_gemm, w12_q6_argmax)
+constexpr int kOpQ6 = 102;
+constexpr int kOpQ6Argmax = 103;
+inline bool is_copy_op(int op) { return op == kOpQ8 || op == kOpQ8Argmax || op == kOpQ6 || op == kOpQ6Argmax; }
+inline bool is_argmax_op(int op) {
+    return op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8Argmax || op == kOpQ6Argmax;
+}
 
 struct Layout {
     int npad, stages, rps, nacc, acc_cols, grid, unit, smem;
     bool whole;  // every block covers whole tiles (no partial sums)
     bool vtma;   // Q view with two records per slot: views copied through a tensor map
-    bool packed; // INT8 copy: 8 KB records back to back
+    bool packed; // a separate copy: INT8 (8 KB) or INT6 (6 KB) records back to back
     int64_t R;
     size_t ws_bytes, off_err, off_tile, off_done, off_part, off_top;
 };
 
 w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     if (M < 1 || M > kMaxM) return W12_ERR_UNSUPPORTED_SHAPE;
-    if ((op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) && op != kOpQ8 && op != kOpQ8Argmax)
-        return W12_ERR_INVALID_ARG;
+    if ((op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) && !is_copy_op(op)) return W12_ERR_INVALID_ARG;
     int sms = 0;
     W12_TRY(require_device(&sms));
-    const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8 || op == kOpQ8Argmax);
-    L->packed = (op == kOpQ8 || op == kOpQ8Argmax);
+    const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX || is_copy_op(op));
+    L->packed = is_copy_op(op);
+    const bool q6 = (op == kOpQ6 || op == kOpQ6Argmax);
     L->R = static_cast<int64_t>(t->n_tiles) * t->k_tiles;
     L->npad = (M + 15) / 16 * 16;
     // above 256 rows the MMA's N and the activation box are split in two halves of a multiple of 16
@@ -1088,10 +1112,10 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     }
     // the view map needs a 16-byte aligned record array (records are 12 KB apart)
     L->vtma = q && !L->packed && L->rps == 2 && aligned16(t->records);
-    const int rstride = (L->vtma || L->packed) ? kViewBytes : kRecordBytes;
-    const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * rstride + (q ? kViewBytes : kRecordBytes) +
-                       (q ? 0 : kEscCap * 4);
-    const bool am = (op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8Argmax);
+    const int rstride = q6 ? kQ6RecordBytes : ((L->vtma || L->packed) ? kViewBytes : kRecordBytes);
+    const int rbytes = q6 ? kQ6RecordBytes : (q ? kViewBytes : kRecordBytes);
+    const int sbytes = L->rps * L->npad * 128 + (L->rps - 1) * rstride + rbytes + (q ? 0 : kEscCap * 4);
+    const bool am = is_argmax_op(op);
     const int ctrl = static_cast<int>(align_up(kCtrlBytes + scratch_bytes(M, am), 1024));
     int stages = (kSmemLimit - 1024 - ctrl) / sbytes;
     if (stages > kMaxStages) stages = kMaxStages;
@@ -1124,10 +1148,10 @@ w12_status plan(const w12_tensor *t, int M, int op, Layout *L) {
     return W12_OK;
 }
 
-template <bool kQ, bool kA, bool kQ8 = false>
+template <bool kQ, bool kA, int kPack = 0>
 w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const CUtensorMap &ymap,
                           const CUtensorMap &vmap, const Params &p, const Layout &L, bool overlap, cudaStream_t st) {
-    auto kern = w12_gemm_kernel<kQ, kA, kQ8>;
+    auto kern = w12_gemm_kernel<kQ, kA, kPack>;
     // the opt-in shared-memory limit is set once per device (to the maximum any plan uses)
     static std::atomic<uint64_t> smem_set{0};
     int dev = 0;
@@ -1163,9 +1187,8 @@ w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const
 w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, int y_dtype,
                int32_t *idx, float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream,
                unsigned flags = 0, const float *row_scale = nullptr, int *run_flag = nullptr) {
-    const bool q8 = (op == kOpQ8 || op == kOpQ8Argmax);
-    if (q8) {
-        // the INT8 copy of the certified head: records and row scales only
+    if (is_copy_op(op)) {
+        // a separate copy (INT8 or INT6): records and row scales only
         if (!t || !t->records || !row_scale || t->N < 1 || t->K < 1) return W12_ERR_INVALID_ARG;
     } else {
         W12_TRY(check_tensor(t));
@@ -1176,7 +1199,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     Layout L{};
     W12_TRY(plan(t, M, op, &L));
     if (ws_bytes < L.ws_bytes) return W12_ERR_WORKSPACE;
-    const bool argmax = (op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX || op == kOpQ8Argmax);
+    const bool argmax = is_argmax_op(op);
     const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX);
     if (argmax && (!idx || !val || !gap)) return W12_ERR_INVALID_ARG;
     if (!argmax && (!y || (y_dtype != W12_OUT_F32 && y_dtype != W12_OUT_BF16))) return W12_ERR_INVALID_ARG;
@@ -1280,8 +1303,10 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     p.val = val;
     p.gap = gap;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (op == kOpQ8) return launch_variant<true, false, true>(map, map2, ymap, vmap, p, L, overlap, st);
-    if (op == kOpQ8Argmax) return launch_variant<true, true, true>(map, map2, ymap, vmap, p, L, overlap, st);
+    if (op == kOpQ8) return launch_variant<true, false, 8>(map, map2, ymap, vmap, p, L, overlap, st);
+    if (op == kOpQ8Argmax) return launch_variant<true, true, 8>(map, map2, ymap, vmap, p, L, overlap, st);
+    if (op == kOpQ6) return launch_variant<true, false, 6>(map, map2, ymap, vmap, p, L, overlap, st);
+    if (op == kOpQ6Argmax) return launch_variant<true, true, 6>(map, map2, ymap, vmap, p, L, overlap, st);
     if (q)
         return argmax ? launch_variant<true, true>(map, map2, ymap, vmap, p, L, overlap, st)
                       : launch_variant<true, false>(map, map2, ymap, vmap, p, L, overlap, st);
@@ -1311,6 +1336,21 @@ w12_status gemm_q8_argmax_workspace(const w12_tensor *codes, int M, size_t *byte
 w12_status gemm_q8_argmax(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, int32_t *idx,
                           float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags) {
     return run(codes, x, M, kOpQ8Argmax, nullptr, W12_OUT_F32, idx, val, gap, ws, ws_bytes, stream, flags,
+               row_scale);
+}
+w12_status gemm_q6_workspace(const w12_tensor *codes, int M, bool argmax, size_t *bytes) {
+    Layout L{};
+    W12_TRY(plan(codes, M, argmax ? kOpQ6Argmax : kOpQ6, &L));
+    *bytes = L.ws_bytes;
+    return W12_OK;
+}
+w12_status gemm_q6(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, void *y, int y_dtype,
+                   void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags) {
+    return run(codes, x, M, kOpQ6, y, y_dtype, nullptr, nullptr, nullptr, ws, ws_bytes, stream, flags, row_scale);
+}
+w12_status gemm_q6_argmax(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, int32_t *idx,
+                          float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags) {
+    return run(codes, x, M, kOpQ6Argmax, nullptr, W12_OUT_F32, idx, val, gap, ws, ws_bytes, stream, flags,
                row_scale);
 }
 w12_status lmhead_argmax_if(const w12_tensor *t, const uint16_t *x, int M, int32_t *idx, float *val, float *gap,

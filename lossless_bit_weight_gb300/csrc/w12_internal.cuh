@@ -15,6 +15,7 @@ constexpr int kTileK = 64;
 constexpr int kRecordBytes = 12288;
 constexpr int kViewBytes = 8192;
 constexpr int kRecordWeights = kTileN * kTileK;  // 8192
+constexpr int kQ6RecordBytes = W12_Q6_RECORD_BYTES;  // 6144: the INT6 copy's record
 
 // ------------------------------------------------------------------------------------------
 // host side
@@ -50,6 +51,12 @@ w12_status gemm_q8(const w12_tensor *codes, const float *row_scale, const uint16
 // the row argmax over the INT8 copy (flags: W12_LAUNCH_OVERLAP)
 w12_status gemm_q8_argmax_workspace(const w12_tensor *codes, int M, size_t *bytes);
 w12_status gemm_q8_argmax(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, int32_t *idx,
+                          float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags);
+// the GEMM and the row argmax over the INT6 Q-pass copy (6 KB records; flags: W12_LAUNCH_OVERLAP)
+w12_status gemm_q6_workspace(const w12_tensor *codes, int M, bool argmax, size_t *bytes);
+w12_status gemm_q6(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, void *y, int y_dtype,
+                   void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags);
+w12_status gemm_q6_argmax(const w12_tensor *codes, const float *row_scale, const uint16_t *x, int M, int32_t *idx,
                           float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream, unsigned flags);
 // the W12 head's fused argmax, launched stream-ordered; it does nothing unless *run_flag != 0
 // when it starts, and clears the flag when it has run
@@ -543,6 +550,25 @@ __device__ __forceinline__ void decode_q8_chunk16(const uint4 &v, uint32_t *out)
     for (int q = 0; q < 4; ++q) {
         out[2 * q] = decode_q8_pair(vw[q], 0x9180u);      // codes 0, 1 of the word
         out[2 * q + 1] = decode_q8_pair(vw[q], 0xB3A2u);  // codes 2, 3
+    }
+}
+
+// Sixteen INT6 codes k_l = 16g .. 16g+15 of one row -> 8 bf16x2 words (word j: k_l = 16g + 2j
+// in the low half, 16g + 2j + 1 in the high half). Each code c is stored as u = c + 32 (1..63):
+// lw0 / lw1 are the row's plane-L words 2g and 2g+1 (the low four bits of pair j at bits 4(j&3)
+// and 16 + 4(j&3) of word j >> 2), tw its plane-T word g (the top two bits of pair j at bits 2j
+// and 16 + 2j). OR-ing u into the mantissa of 128.0 (bf16 0x4300, whose mantissa step is 1)
+// gives 128 + u exactly, and subtracting 160 leaves c exactly.
+__device__ __forceinline__ void decode_q6_group16(uint32_t lw0, uint32_t lw1, uint32_t tw, uint32_t *out) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t l = ((j < 4) ? lw0 : lw1) >> (4 * (j & 3));
+        const uint32_t t = (j < 2) ? (tw << (4 - 2 * j)) : (tw >> (2 * j - 4));  // bits 2j -> 4
+        uint32_t v, o;
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(l), "r"(0x000F000Fu), "r"(0x43004300u));
+        asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(v) : "r"(t), "r"(0x00300030u), "r"(v));
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(o) : "r"(v), "r"(0x43204320u));
+        out[j] = o;
     }
 }
 

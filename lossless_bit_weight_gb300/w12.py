@@ -52,6 +52,16 @@ class CQ8Head(ctypes.Structure):
     ]
 
 
+class CQ6Copy(ctypes.Structure):
+    """Mirror of ``w12_q6_copy``."""
+
+    _fields_ = [
+        ("N", ctypes.c_int32), ("K", ctypes.c_int32),
+        ("n_tiles", ctypes.c_int32), ("k_tiles", ctypes.c_int32),
+        ("codes", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -89,6 +99,11 @@ def lib() -> ctypes.CDLL:
             "w12_lmhead_certified": ([T, ctypes.POINTER(CQ8Head), P, P, i32, P, P, P, P, P, sz, P], i32),
             "w12_q8_argmax_workspace_size": ([ctypes.POINTER(CQ8Head), i32, ctypes.POINTER(sz)], i32),
             "w12_q8_argmax": ([ctypes.POINTER(CQ8Head), P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
+            "w12_q6_shape": ([i32, i32, ctypes.POINTER(CQ6Copy), ctypes.POINTER(sz), ctypes.POINTER(sz)], i32),
+            "w12_q6_build": ([P, ctypes.POINTER(CQ6Copy), P], i32),
+            "w12_q6_workspace_size": ([ctypes.POINTER(CQ6Copy), i32, i32, ctypes.POINTER(sz)], i32),
+            "w12_q6_gemm": ([ctypes.POINTER(CQ6Copy), P, i32, P, i32, ctypes.c_uint, P, sz, P], i32),
+            "w12_q6_argmax": ([ctypes.POINTER(CQ6Copy), P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -381,4 +396,67 @@ def q8_argmax(h: Q8Head, x: torch.Tensor, stream=None, overlap: bool = False):
     ws, nb = h._ws[key]
     _check(lib().w12_q8_argmax(ctypes.byref(h.c), _ptr(x), M, _ptr(idx), _ptr(val), _ptr(gap),
                                LAUNCH_OVERLAP if overlap else 0, _ptr(ws), nb, _stream(stream)), "w12_q8_argmax")
+    return idx, val, gap
+
+
+class Q6Copy:
+    """The INT6 Q-pass copy of a weight matrix (``w12_q6_copy``): 6 KB records and row scales."""
+
+    def __init__(self, N: int, K: int, device="cuda"):
+        self.c = CQ6Copy()
+        cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+        _check(lib().w12_q6_shape(N, K, ctypes.byref(self.c), ctypes.byref(cb), ctypes.byref(sb)), "w12_q6_shape")
+        self.N, self.K = N, K
+        self.codes = torch.empty(int(cb.value), dtype=torch.uint8, device=device)
+        self.scale = torch.empty(int(sb.value) // 4, dtype=torch.float32, device=device)
+        self.c.codes, self.c.scale = self.codes.data_ptr(), self.scale.data_ptr()
+        self._ws = {}
+
+    @property
+    def nbytes(self) -> int:
+        return self.codes.numel() + self.scale.numel() * 4
+
+    def workspace(self, M: int, argmax: bool, device):
+        key = (M, bool(argmax), torch.cuda.current_device())
+        if key not in self._ws:
+            nb = ctypes.c_size_t()
+            _check(lib().w12_q6_workspace_size(ctypes.byref(self.c), M, 1 if argmax else 0, ctypes.byref(nb)),
+                   "w12_q6_workspace_size")
+            self._ws[key] = (torch.zeros(max(int(nb.value), 16), dtype=torch.uint8, device=device), int(nb.value))
+        return self._ws[key]
+
+
+def q6_build(w: torch.Tensor, stream=None) -> Q6Copy:
+    """The INT6 Q-pass copy of a bf16 matrix [N, K] (device)."""
+    _bits(w)
+    N, K = w.shape
+    c = Q6Copy(N, K, device=w.device)
+    _check(lib().w12_q6_build(_ptr(w), ctypes.byref(c.c), _stream(stream)), "w12_q6_build")
+    return c
+
+
+def q6_gemm(c: Q6Copy, x: torch.Tensor, out_dtype=torch.float32, out: torch.Tensor | None = None, stream=None,
+            overlap: bool = False) -> torch.Tensor:
+    """yq = x @ (scale * codes)^T through the INT6 copy: fp32 or bf16 [M, N]."""
+    _bits(x)
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty(M, c.N, dtype=out_dtype, device=x.device)
+    ydt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
+    ws, nb = c.workspace(M, False, x.device)
+    _check(lib().w12_q6_gemm(ctypes.byref(c.c), _ptr(x), M, _ptr(out), ydt, LAUNCH_OVERLAP if overlap else 0,
+                             _ptr(ws), nb, _stream(stream)), "w12_q6_gemm")
+    return out
+
+
+def q6_argmax(c: Q6Copy, x: torch.Tensor, stream=None, overlap: bool = False):
+    """(idx int32[M], val f32[M], gap f32[M]) of each row's argmax of the INT6 Q pass."""
+    _bits(x)
+    M = x.shape[0]
+    idx = torch.empty(M, dtype=torch.int32, device=x.device)
+    val = torch.empty(M, dtype=torch.float32, device=x.device)
+    gap = torch.empty(M, dtype=torch.float32, device=x.device)
+    ws, nb = c.workspace(M, True, x.device)
+    _check(lib().w12_q6_argmax(ctypes.byref(c.c), _ptr(x), M, _ptr(idx), _ptr(val), _ptr(gap),
+                               LAUNCH_OVERLAP if overlap else 0, _ptr(ws), nb, _stream(stream)), "w12_q6_argmax")
     return idx, val, gap

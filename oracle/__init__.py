@@ -61,7 +61,7 @@ def _load():
         lib.w12o_certified_argmax.argtypes = [P, i32, P, i32, i32, P, P, P, P, P, P, P]
         lib.w12o_copy_q6.argtypes = [P, i32, i32, P, P]
         lib.w12o_q6_pack.argtypes = [P, i32, i32, P]
-        lib.w12o_gemm_q6.argtypes = [P, i32, P, P, i32, i32, P]
+        lib.w12o_gemm_q6.argtypes = [P, i32, P, P, i32, i32, P, P]
         _lib = lib
     return _lib
 
@@ -266,11 +266,12 @@ def q6_pack(q: np.ndarray) -> np.ndarray:
     return rec
 
 
-def gemm_q6(x, c: CopyQ6) -> np.ndarray:
-    """yq [M, N] = s_n (x . c_n) in fp64."""
+def gemm_q6(x, c: CopyQ6) -> tuple[np.ndarray, np.ndarray]:
+    """(yq, ad) [M, N]: yq = s_n (x . c_n) and ad = s_n sum_k |x_k c_nk|, in fp64."""
     x = _u16(x)
     M, K = x.shape
     N = c.q.shape[0]
     y = np.zeros((M, N), dtype=np.float64)
-    _load().w12o_gemm_q6(_p(x), M, _p(np.ascontiguousarray(c.q)), _p(c.scale), N, K, _p(y))
-    return y
+    ad = np.zeros((M, N), dtype=np.float64)
+    _load().w12o_gemm_q6(_p(x), M, _p(np.ascontiguousarray(c.q)), _p(c.scale), N, K, _p(y), _p(ad))
+    return y, ad

@@ -544,15 +544,21 @@ void w12o_q6_pack(const int8_t *q, int N, int K, uint8_t *records) {
     }
 }
 
-/* yq [M,N] = s_n sum_k x[m,k] c[n,k], in fp64 (each product is exact). */
-void w12o_gemm_q6(const uint16_t *x, int M, const int8_t *q, const float *scale, int N, int K, double *y) {
+/* yq [M,N] = s_n sum_k x[m,k] c[n,k] and ad [M,N] = s_n sum_k |x[m,k] c[n,k]| (the scale of
+ * the rounding error of any evaluation order), in fp64 (each product is exact). */
+void w12o_gemm_q6(const uint16_t *x, int M, const int8_t *q, const float *scale, int N, int K, double *y,
+                  double *ad) {
     #pragma omp parallel for schedule(static)
     for (int n = 0; n < N; ++n) {
         for (int m = 0; m < M; ++m) {
-            double acc = 0.0;
-            for (int k = 0; k < K; ++k)
-                acc += w12o_bf16_to_double(x[(size_t)m * K + k]) * (double)q[(size_t)n * K + k];
+            double acc = 0.0, aacc = 0.0;
+            for (int k = 0; k < K; ++k) {
+                const double p = w12o_bf16_to_double(x[(size_t)m * K + k]) * (double)q[(size_t)n * K + k];
+                acc += p;
+                aacc += fabs(p);
+            }
             y[(size_t)m * N + n] = (double)scale[n] * acc;
+            ad[(size_t)m * N + n] = (double)scale[n] * aacc;
         }
     }
 }

@@ -100,6 +100,26 @@ def test_null_tensor_is_rejected_before_device_work(w12):
     assert L.w12_encode(None, 64, 64, None, 0, None, None) == w12.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("N,K", [(151936, 5120), (17408, 5120), (1, 8), (130, 72)])
+def test_q6_copy_shape_and_argument_checks(w12, N, K):
+    """The INT6 copy's sizes (6144-byte records, one fp32 scale per padded row) and its calls'
+    argument checks, all on the host."""
+    L = w12.lib()
+    c = w12.CQ6Copy()
+    cb, sb = ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.w12_q6_shape(N, K, ctypes.byref(c), ctypes.byref(cb), ctypes.byref(sb)) == w12.OK
+    nt, kt = -(-N // 128), -(-K // 64)
+    assert (c.N, c.K, c.n_tiles, c.k_tiles) == (N, K, nt, kt)
+    assert cb.value == nt * kt * 6144 and sb.value == 4 * nt * 128
+    assert L.w12_q6_shape(N, 12, ctypes.byref(c), None, None) == w12.ERR_UNSUPPORTED_SHAPE
+    nb = ctypes.c_size_t()
+    # no buffers yet: rejected before any device work
+    assert L.w12_q6_build(None, ctypes.byref(c), None) == w12.ERR_INVALID_ARG
+    assert L.w12_q6_workspace_size(ctypes.byref(c), 1, 0, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    assert L.w12_q6_gemm(ctypes.byref(c), None, 1, None, 0, 0, None, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_q6_argmax(None, None, 1, None, None, None, 0, None, 0, None) == w12.ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_the_library(w12, monkeypatch):
     monkeypatch.setattr(w12, "_lib", None)
     monkeypatch.setattr(w12, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libw12.so"))

@@ -513,4 +513,6 @@ def test_gemm_q6_lossless_case_is_the_exact_gemm(orc):
     assert np.array_equal(c.scale.astype(np.float64), 2.0 ** -e)
     assert np.array_equal(c.q, ints.astype(np.int8))
     y, _ = orc.gemm(x, w)
-    assert np.array_equal(orc.gemm_q6(x, c), y)
+    yq, adq = orc.gemm_q6(x, c)
+    assert np.array_equal(yq, y)
+    assert np.array_equal(adq, np.abs(bf16_values(x)) @ np.abs(wv.astype(np.float64)).T)
