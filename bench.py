@@ -596,24 +596,29 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
 
 
 def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
-    """The weight stream of one decoding step of the synthetic 64-layer model: every linear of
-    64 layers and the LM-head argmax on fixed activations (no glue between them), captured once
-    in a CUDA graph and replayed; the same sequence with bf16 cuBLAS on the unencoded weights
-    beside it. Two layouts: the seven linears of a layer as listed (q, k, v, o, gate, up, down:
-    449 GEMMs), and with the linears that share an input concatenated at load time (q|k|v and
-    gate|up, as serving engines store them: 257 GEMMs). Concatenating output channels changes
-    no record: a W12 tensor of [Wq; Wk; Wv] holds the three tensors' records one after another."""
+    """One decoding step of the synthetic 64-layer model, captured once in a CUDA graph and
+    replayed; the same sequence with bf16 cuBLAS on the unencoded weights beside it. Three
+    layouts. Two stream the weights on fixed activations (no glue between the GEMMs): the seven
+    linears of a layer as listed (q, k, v, o, gate, up, down: 449 GEMMs), and with the linears
+    that share an input concatenated at load time (q|k|v and gate|up, as serving engines store
+    them: 257 GEMMs). Concatenating output channels changes no record: a W12 tensor of
+    [Wq; Wk; Wv] holds the three tensors' records one after another. The third ("carried") is
+    the step itself: M rows carried from layer to layer through the library's glue (row
+    normalisation, residual adds fused into the GEMMs, the gate-up product): 321 GEMMs and 193
+    glue kernels; its cuBLAS counterpart runs the same chain with torch glue."""
     from lossless_bit_weight_gb300 import w12
 
     res = {"layers": 64, "by_layout": {}}
     stream = torch.cuda.Stream(device=dev)
-    for layout in ("separate", "fused"):
+    for layout in ("separate", "fused", "carried"):
         lin = []
         for layer in range(64):
             ws = {name: synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device=dev)
                   for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS)}
-            groups = ([["q"], ["k"], ["v"], ["o"], ["gate"], ["up"], ["down"]] if layout == "separate"
-                      else [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]])
+            groups = {"separate": [["q"], ["k"], ["v"], ["o"], ["gate"], ["up"], ["down"]],
+                      "fused": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
+                      # carried: a is its own output (o reads it), k|v are computed and dropped
+                      "carried": [["q"], ["k", "v"], ["o"], ["gate", "up"], ["down"]]}[layout]
             for g in groups:
                 wb = ws[g[0]] if len(g) == 1 else torch.cat([ws[n] for n in g], dim=0)
                 lin.append((w12.encode(wb), wb))
@@ -639,6 +644,51 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
                     torch.matmul(xs[wb.shape[1]], wb.t(), out=ys[(wb.shape[0], torch.bfloat16)])
                 torch.argmax(torch.nn.functional.linear(xs[K_HID], wh), dim=1)
 
+            if layout == "carried":
+                # the rows carried from layer to layer: h fp32, every glue step in the library
+                h0 = synth.activations(M, K_HID, seed=synth.seed_for(3, M), device=dev).float()
+                h = torch.empty_like(h0)
+                xa = torch.empty((M, K_HID), dtype=torch.bfloat16, device=dev)
+                a_q = torch.empty((M, 6144), dtype=torch.bfloat16, device=dev)
+                kv = torch.empty((M, 2048), dtype=torch.bfloat16, device=dev)
+                gu = torch.empty((M, 2 * N_MLP), dtype=torch.float32, device=dev)
+                pz = torch.empty((M, N_MLP), dtype=torch.bfloat16, device=dev)
+
+                # the glue kernels are stream-ordered: launched early (overlapped), their blocks
+                # wait on SMs that the next GEMM's blocks need (measured: 125 us per layer at
+                # M=1 stream-ordered, 169 us overlapped); each GEMM still starts while the glue
+                # kernel before it runs
+                def w12_step():
+                    h.copy_(h0)
+                    for i in range(0, len(lin), 5):
+                        (tq, _), (tkv, _), (to, _), (tgu, _), (td, _) = lin[i:i + 5]
+                        w12.rms_bf16(h, out=xa)
+                        w12.gemm(tq, xa, out=a_q, overlap=True)
+                        w12.gemm(tkv, xa, out=kv, overlap=True)
+                        w12.gemm(to, a_q, out=h, accumulate=True, overlap=True)
+                        w12.rms_bf16(h, out=xa)
+                        w12.gemm(tgu, xa, out=gu, overlap=True)
+                        w12.mul_bf16(gu, N_MLP, out=pz)
+                        w12.gemm(td, pz, out=h, accumulate=True, overlap=True)
+                    w12.rms_bf16(h, out=xa)
+                    w12.lmhead_argmax(th, xa, overlap=True)
+
+                def cublas_step():
+                    # the same chain on bf16 weights: cuBLAS GEMMs, torch glue
+                    h.copy_(h0)
+                    for i in range(0, len(lin), 5):
+                        (_, wq), (_, wkv), (_, wo), (_, wgu), (_, wd) = lin[i:i + 5]
+                        x = (h / h.pow(2).mean(dim=1, keepdim=True).sqrt()).to(torch.bfloat16)
+                        torch.matmul(x, wq.t(), out=a_q)
+                        torch.matmul(x, wkv.t(), out=kv)
+                        h.add_(torch.matmul(a_q, wo.t()).float())
+                        x2 = (h / h.pow(2).mean(dim=1, keepdim=True).sqrt()).to(torch.bfloat16)
+                        g = torch.matmul(x2, wgu.t()).float()
+                        p = (g[:, :N_MLP] * g[:, N_MLP:]).to(torch.bfloat16)
+                        h.add_(torch.matmul(p, wd.t()).float())
+                    x = (h / h.pow(2).mean(dim=1, keepdim=True).sqrt()).to(torch.bfloat16)
+                    torch.argmax(torch.nn.functional.linear(x, wh), dim=1)
+
             row = {}
             for name, fn in (("w12", w12_step), ("cublas_bf16", cublas_step)):
                 with torch.cuda.stream(stream):
@@ -663,6 +713,9 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
             for t, _ in lin[:7]:
                 w12.check(t)
             row_l["by_m"][str(M)] = row
+        if layout == "carried":
+            row_l["glue_kernels_per_step"] = 2 * 64 + 64 + 1
+            row_l["gemms_per_step"] = len(lin) + 1
         res["by_layout"][layout] = row_l
         del lin
         torch.cuda.empty_cache()

@@ -57,7 +57,7 @@ enum {
 };
 
 enum { W12_OUT_F32 = 0, W12_OUT_BF16 = 1 };          /* y element type */
-enum { W12_LAUNCH_OVERLAP = 1, W12_LAUNCH_TEST_STALL = 2 };  /* w12_gemm_ex flags */
+enum { W12_LAUNCH_OVERLAP = 1, W12_LAUNCH_TEST_STALL = 2, W12_LAUNCH_ACCUMULATE = 4 };  /* w12_gemm_ex flags */
 enum { W12_OP_GEMM = 0, W12_OP_QVIEW_GEMM = 1, W12_OP_ARGMAX = 2, W12_OP_QVIEW_ARGMAX = 3 };
 
 /*
@@ -180,6 +180,10 @@ w12_status w12_lmhead_argmax(const w12_tensor *t, const uint16_t *x, int M, int3
  * wait for this one before using its results, as kernels launched with this flag do.
  * The kernel's bounded waits give up after about a second, so the preceding kernel must not run
  * much longer than that after this launch begins.
+ * flags with W12_LAUNCH_ACCUMULATE (GEMM ops with fp32 y only, else W12_ERR_INVALID_ARG): y += the
+ * result instead of y = the result, one fp32 addition per element (a residual add fused into the
+ * GEMM); deterministic like the plain GEMM. It combines with W12_LAUNCH_OVERLAP (y is read only
+ * after the preceding kernel has completed).
  * flags = W12_LAUNCH_TEST_STALL is a test hook for the failure path. Each block's producer fills
  * only its first pipeline slot, so the block's bounded waits run out after about a second. Every
  * block then stops, the call's outputs are invalid, and w12_check reports W12_ERR_TIMEOUT; the
@@ -205,6 +209,27 @@ w12_status w12_gemm_ex(const w12_tensor *t, const uint16_t *x, int M, int op, vo
  * reported by this call (use w12_gemm with w12_check where that matters). Asynchronous. */
 w12_status w12_gemm_noalloc(const w12_tensor *t, const uint16_t *x, int M, void *y, int y_dtype,
                             w12_stream_t stream);
+
+/* ---- glue of the synthetic layer stream (the pages give no layer dataflow) ---------------
+ * The synthetic 64-layer stream carries M rows from layer to layer (the build's reading): h fp32
+ * [M, K]; x = bf16(h / rms(h)); a = bf16(x Wq^T); h += a Wo^T (W12_LAUNCH_ACCUMULATE);
+ * x2 = bf16(h / rms(h)); p = bf16((x2 Wg^T) * (x2 Wu^T)); h += p Wd^T. These two calls are its
+ * steps between the GEMMs. flags: 0 or W12_LAUNCH_OVERLAP (the kernel may start while the
+ * previous kernel on the stream finishes and reads its input only after that kernel has
+ * completed). Both let the next kernel start early; a GEMM launched with W12_LAUNCH_OVERLAP
+ * waits for their completion before it reads x. M in [1, W12_MAX_M]. Asynchronous. */
+
+/* x[m, k] = bf16(h[m, k] * (1 / sqrt(mean_k h[m, k]^2))): the sum of squares, the reciprocal of
+ * the root (rounded once) and each product (rounded once) in fp64, then one rounding to bf16,
+ * nearest even; zeros for an all-zero row. h: device fp32 [M, K], 16-byte aligned; x: device bf16
+ * [M, K], 8-byte aligned. K % 4 != 0 returns W12_ERR_UNSUPPORTED_SHAPE. */
+w12_status w12_rms_bf16(const float *h, int M, int K, uint16_t *x, unsigned flags, w12_stream_t stream);
+
+/* p[m, n] = bf16(g[m*ld + n] * u[m*ld + n]) for n < N: the fp32 product rounded to nearest even.
+ * g, u: device fp32 with row stride ld >= N (g and u may be two halves of one [M, 2N] GEMM output,
+ * ld = 2N); p: device bf16 [M, N]. */
+w12_status w12_mul_bf16(const float *g, const float *u, int M, int N, int ld, uint16_t *p, unsigned flags,
+                        w12_stream_t stream);
 
 /* SYNCHRONISES `stream`, then reports W12_ERR_TIMEOUT if a GEMM kernel that used this
  * workspace gave up one of its bounded waits (its outputs are then invalid and the workspace

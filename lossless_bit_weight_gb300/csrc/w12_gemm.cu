@@ -114,6 +114,7 @@ struct Params {
     int unit;  // records per unit of the work split: 1 (stream-K) or k_tiles (whole tiles)
     int overlap;  // launched as a programmatic dependent launch (W12_LAUNCH_OVERLAP)
     int y_tma;    // y is written by tiled tensor stores through ymap
+    int y_accum;  // W12_LAUNCH_ACCUMULATE: y (fp32) += the result instead of y = the result
     int v_tma;    // Q view: a slot's two record views arrive by one tiled copy through vmap
     int xhalf;    // more than 256 rows: rows per activation box and per MMA (npad / 2), else 0
     const float *row_scale;  // INT8 / INT6 copy: per-channel scale, [n_tiles * 128]
@@ -670,6 +671,8 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
         auto store_y = [&](int m, int n, float f) {
             if (p.y_bf16)
                 reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(f);
+            else if (p.y_accum)  // this thread alone writes the element in this launch
+                reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] += f;
             else
                 reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] = f;
         };
@@ -711,7 +714,10 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
                 __syncwarp();
                 // a box that starts at or beyond column N writes nothing: not issued
                 if (lane == 0 && tile * kTileN + 32 * qw < p.N) {
-                    tma_2d_s2g(&ymap, tile * kTileN + 32 * qw, m0, smem_u32(stg));
+                    if (p.y_accum)  // each element of y gets exactly one addition per launch
+                        tma_2d_s2g_add(&ymap, tile * kTileN + 32 * qw, m0, smem_u32(stg));
+                    else
+                        tma_2d_s2g(&ymap, tile * kTileN + 32 * qw, m0, smem_u32(stg));
                     bulk_commit_group();
                 }
                 return;
@@ -1034,6 +1040,8 @@ w12_reduce_kernel(const Params p) {
     if (n < p.N) {
         if (p.y_bf16)
             reinterpret_cast<__nv_bfloat16 *>(p.y)[static_cast<size_t>(m) * p.N + n] = __float2bfloat16_rn(acc);
+        else if (p.y_accum)
+            reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] += acc;
         else
             reinterpret_cast<float *>(p.y)[static_cast<size_t>(m) * p.N + n] = acc;
     }
@@ -1193,7 +1201,8 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     } else {
         W12_TRY(check_tensor(t));
     }
-    if (flags & ~static_cast<unsigned>(W12_LAUNCH_OVERLAP | W12_LAUNCH_TEST_STALL)) return W12_ERR_INVALID_ARG;
+    if (flags & ~static_cast<unsigned>(W12_LAUNCH_OVERLAP | W12_LAUNCH_TEST_STALL | W12_LAUNCH_ACCUMULATE))
+        return W12_ERR_INVALID_ARG;
     const bool overlap = (flags & W12_LAUNCH_OVERLAP) != 0;
     if (!x || !aligned16(x) || !ws) return W12_ERR_INVALID_ARG;
     Layout L{};
@@ -1203,6 +1212,8 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     const bool q = (op == W12_OP_QVIEW_GEMM || op == W12_OP_QVIEW_ARGMAX);
     if (argmax && (!idx || !val || !gap)) return W12_ERR_INVALID_ARG;
     if (!argmax && (!y || (y_dtype != W12_OUT_F32 && y_dtype != W12_OUT_BF16))) return W12_ERR_INVALID_ARG;
+    const bool accum = (flags & W12_LAUNCH_ACCUMULATE) != 0;
+    if (accum && (argmax || y_dtype != W12_OUT_F32)) return W12_ERR_INVALID_ARG;
 
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return W12_ERR_CUDA;
@@ -1284,6 +1295,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     // Tensor stores pay off when the blocks finish together (whole tiles); with split tiles
     // (stream-K) plain stores measured faster, so they are kept there.
     p.y_tma = (y_tma && L.whole) ? 1 : 0;
+    p.y_accum = accum ? 1 : 0;
     p.x_pair = x_pair ? 1 : 0;
     p.v_tma = L.vtma ? 1 : 0;
     p.xhalf = (L.npad > 256) ? L.npad / 2 : 0;

@@ -192,6 +192,13 @@ __device__ __forceinline__ void tma_2d_s2g(const CUtensorMap *map, int c0, int c
         ::"l"(map), "r"(c0), "r"(c1), "r"(src)
         : "memory");
 }
+// the same box added element-wise into global memory (y += staged values; one addition each)
+__device__ __forceinline__ void tma_2d_s2g_add(const CUtensorMap *map, int c0, int c1, uint32_t src) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];"
+        ::"l"(map), "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // wait until at most N of this thread's bulk groups still have to read their shared memory
 template <int N>

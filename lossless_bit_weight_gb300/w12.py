@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libw12.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_MISMATCH, ERR_TIMEOUT, \
     ERR_DEVICE = range(8)
 OUT_F32, OUT_BF16 = 0, 1
-LAUNCH_OVERLAP, LAUNCH_TEST_STALL = 1, 2
+LAUNCH_OVERLAP, LAUNCH_TEST_STALL, LAUNCH_ACCUMULATE = 1, 2, 4
 OP_GEMM, OP_QVIEW_GEMM, OP_ARGMAX, OP_QVIEW_ARGMAX = range(4)
 TILE_N, TILE_K, RECORD_BYTES, VIEW_BYTES, MAX_M = 128, 64, 12288, 8192, 256
 
@@ -99,6 +99,8 @@ def lib() -> ctypes.CDLL:
             "w12_lmhead_certified": ([T, ctypes.POINTER(CQ8Head), P, P, i32, P, P, P, P, P, sz, P], i32),
             "w12_q8_argmax_workspace_size": ([ctypes.POINTER(CQ8Head), i32, ctypes.POINTER(sz)], i32),
             "w12_q8_argmax": ([ctypes.POINTER(CQ8Head), P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
+            "w12_rms_bf16": ([P, i32, i32, P, ctypes.c_uint, P], i32),
+            "w12_mul_bf16": ([P, P, i32, i32, i32, P, ctypes.c_uint, P], i32),
             "w12_q6_shape": ([i32, i32, ctypes.POINTER(CQ6Copy), ctypes.POINTER(sz), ctypes.POINTER(sz)], i32),
             "w12_q6_build": ([P, ctypes.POINTER(CQ6Copy), P], i32),
             "w12_q6_workspace_size": ([ctypes.POINTER(CQ6Copy), i32, i32, ctypes.POINTER(sz)], i32),
@@ -124,6 +126,14 @@ def _check(status: int, what: str) -> None:
 
 def _ptr(t: torch.Tensor | None):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check_out(out: torch.Tensor, M: int, N: int, dtypes=(torch.float32, torch.bfloat16)) -> None:
+    """The output buffer must be a contiguous [M, N] tensor of an accepted type on a CUDA device:
+    the library writes M * N elements of out's own type."""
+    if out.dtype not in dtypes or tuple(out.shape) != (M, N) or not out.is_contiguous() or not out.is_cuda:
+        raise ValueError(f"out must be a contiguous CUDA tensor of shape ({M}, {N}) and type in {dtypes}, "
+                         f"got {tuple(out.shape)} {out.dtype}")
 
 
 def _stream(stream=None):
@@ -253,24 +263,29 @@ def verify(t: W12Tensor, w_ref: torch.Tensor, stream=None) -> int:
 
 def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = False,
          out: torch.Tensor | None = None, stream=None, overlap: bool = False,
-         test_stall: bool = False) -> torch.Tensor:
+         test_stall: bool = False, accumulate: bool = False) -> torch.Tensor:
     """y = x @ W^T over the exact weights (or the 8-bit view when ``qview``).
 
     ``overlap`` launches with ``W12_LAUNCH_OVERLAP`` (``w12_gemm_ex``): the kernel may start, and
     fetch and decode its weights, while the previous kernel on the stream finishes; t's buffers
     must not be written by that kernel. ``test_stall`` sets the ``W12_LAUNCH_TEST_STALL`` test
-    hook (the bounded waits run out; ``check`` then raises)."""
+    hook (the bounded waits run out; ``check`` then raises). ``accumulate`` (fp32 ``out`` only,
+    ``W12_LAUNCH_ACCUMULATE``) adds the result into ``out`` instead of overwriting it."""
     _bits(x)
     M = x.shape[0]
     if x.shape[1] != t.K:
         raise ValueError("x must be [M, K]")
-    ydt = OUT_F32 if out_dtype == torch.float32 else OUT_BF16
+    if accumulate and (out is None or out.dtype != torch.float32):
+        raise ValueError("accumulate needs an fp32 out tensor")
     if out is None:
         out = torch.empty((M, t.N), dtype=out_dtype, device=x.device)
+    _check_out(out, M, t.N)
+    ydt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     op = OP_QVIEW_GEMM if qview else OP_GEMM
     ws, nb = t.workspace(M, op)
-    if overlap or test_stall:
-        flags = (LAUNCH_OVERLAP if overlap else 0) | (LAUNCH_TEST_STALL if test_stall else 0)
+    if overlap or test_stall or accumulate:
+        flags = ((LAUNCH_OVERLAP if overlap else 0) | (LAUNCH_TEST_STALL if test_stall else 0)
+                 | (LAUNCH_ACCUMULATE if accumulate else 0))
         _check(lib().w12_gemm_ex(ctypes.byref(t.c), _ptr(x), M, op, _ptr(out), ydt, None, None, None,
                                  flags, _ptr(ws), nb, _stream(stream)), "w12_gemm_ex")
         return out
@@ -305,6 +320,7 @@ def gemm_noalloc(t: W12Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
     M = x.shape[0]
     if out is None:
         out = torch.empty((M, t.N), dtype=torch.float32, device=x.device)
+    _check_out(out, M, t.N, (torch.float32,))
     _check(lib().w12_gemm_noalloc(ctypes.byref(t.c), _ptr(x), M, _ptr(out), OUT_F32, _stream(stream)),
            "w12_gemm_noalloc")
     return out
@@ -442,6 +458,7 @@ def q6_gemm(c: Q6Copy, x: torch.Tensor, out_dtype=torch.float32, out: torch.Tens
     M = x.shape[0]
     if out is None:
         out = torch.empty(M, c.N, dtype=out_dtype, device=x.device)
+    _check_out(out, M, c.N)
     ydt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     ws, nb = c.workspace(M, False, x.device)
     _check(lib().w12_q6_gemm(ctypes.byref(c.c), _ptr(x), M, _ptr(out), ydt, LAUNCH_OVERLAP if overlap else 0,
@@ -460,3 +477,32 @@ def q6_argmax(c: Q6Copy, x: torch.Tensor, stream=None, overlap: bool = False):
     _check(lib().w12_q6_argmax(ctypes.byref(c.c), _ptr(x), M, _ptr(idx), _ptr(val), _ptr(gap),
                                LAUNCH_OVERLAP if overlap else 0, _ptr(ws), nb, _stream(stream)), "w12_q6_argmax")
     return idx, val, gap
+
+
+def rms_bf16(h: torch.Tensor, out: torch.Tensor | None = None, stream=None, overlap: bool = False) -> torch.Tensor:
+    """The synthetic layer stream's row normalisation: bf16 h * (1 / sqrt(mean(h^2))) of fp32 h
+    [M, K], in fp64 before the one rounding to bf16."""
+    if h.dtype != torch.float32 or not h.is_contiguous() or h.dim() != 2:
+        raise ValueError("h must be a contiguous fp32 [M, K] tensor")
+    M, K = h.shape
+    if out is None:
+        out = torch.empty((M, K), dtype=torch.bfloat16, device=h.device)
+    _check_out(out, M, K, (torch.bfloat16,))
+    _check(lib().w12_rms_bf16(_ptr(h), M, K, _ptr(out), LAUNCH_OVERLAP if overlap else 0, _stream(stream)),
+           "w12_rms_bf16")
+    return out
+
+
+def mul_bf16(gu: torch.Tensor, N: int, out: torch.Tensor | None = None, stream=None,
+             overlap: bool = False) -> torch.Tensor:
+    """The synthetic layer stream's gate-up product: bf16 g * u, where g = gu[:, :N] and
+    u = gu[:, N:2N] of one fp32 [M, 2N] GEMM output (the gate and up weights concatenated)."""
+    if gu.dtype != torch.float32 or not gu.is_contiguous() or gu.dim() != 2 or gu.shape[1] != 2 * N:
+        raise ValueError("gu must be a contiguous fp32 [M, 2N] tensor")
+    M = gu.shape[0]
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=gu.device)
+    _check_out(out, M, N, (torch.bfloat16,))
+    _check(lib().w12_mul_bf16(_ptr(gu), gu.data_ptr() + 4 * N, M, N, 2 * N, _ptr(out),
+                              LAUNCH_OVERLAP if overlap else 0, _stream(stream)), "w12_mul_bf16")
+    return out

@@ -62,6 +62,10 @@ def _load():
         lib.w12o_copy_q6.argtypes = [P, i32, i32, P, P]
         lib.w12o_q6_pack.argtypes = [P, i32, i32, P]
         lib.w12o_gemm_q6.argtypes = [P, i32, P, P, i32, i32, P, P]
+        lib.w12o_double_to_bf16.argtypes = [ctypes.c_double]
+        lib.w12o_double_to_bf16.restype = ctypes.c_uint16
+        lib.w12o_rms_bf16.argtypes = [P, i32, i32, P]
+        lib.w12o_mul_bf16.argtypes = [P, P, i32, i32, i32, P]
         _lib = lib
     return _lib
 
@@ -275,3 +279,27 @@ def gemm_q6(x, c: CopyQ6) -> tuple[np.ndarray, np.ndarray]:
     ad = np.zeros((M, N), dtype=np.float64)
     _load().w12o_gemm_q6(_p(x), M, _p(np.ascontiguousarray(c.q)), _p(c.scale), N, K, _p(y), _p(ad))
     return y, ad
+
+
+def double_to_bf16(v: float) -> int:
+    """bf16 bits of a double, rounded to nearest even."""
+    return int(_load().w12o_double_to_bf16(float(v)))
+
+
+def rms_bf16(h: np.ndarray) -> np.ndarray:
+    """The synthetic stream's row normalisation: bf16 bits of h / sqrt(mean(h^2)), fp64."""
+    h = np.ascontiguousarray(h, dtype=np.float32)
+    M, K = h.shape
+    x = np.zeros((M, K), dtype=np.uint16)
+    _load().w12o_rms_bf16(_p(h), M, K, _p(x))
+    return x
+
+
+def mul_bf16(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """The synthetic stream's gate-up product: bf16 bits of the fp32 product g * u."""
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    M, N = g.shape
+    p = np.zeros((M, N), dtype=np.uint16)
+    _load().w12o_mul_bf16(_p(g), _p(u), M, N, N, _p(p))
+    return p

@@ -562,3 +562,53 @@ void w12o_gemm_q6(const uint16_t *x, int M, const int8_t *q, const float *scale,
         }
     }
 }
+
+/* ---- glue of the synthetic layer stream --------------------------------------------------
+ * The pages give no layer dataflow; the synthetic 64-layer stream that carries M rows from layer
+ * to layer (the build's reading) needs three steps besides the GEMMs: the residual add (y += x W^T,
+ * one fp32 addition per output), the row normalisation and the gate-up product below. */
+
+/* bf16 bits of a double, rounded to nearest even (normal, subnormal, overflow to Inf, NaN). */
+uint16_t w12o_double_to_bf16(double v) {
+    if (isnan(v)) return 0x7FC0;
+    const uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);               /* a = m 2^e, m in [0.5, 1) */
+    int q_exp = e - 8;          /* quantum of an 8-significant-bit value in that binade */
+    if (q_exp < -133) q_exp = -133;  /* bf16 subnormals: quantum 2^-133 */
+    double q = nearbyint(ldexp(a, -q_exp));  /* exact scaling; ties to even */
+    double r = ldexp(q, q_exp);
+    if (r > 0x1.FEp127) return sign | 0x7F80;  /* rounded beyond the largest finite bf16: Inf */
+    /* r is now exactly representable in bf16: take its fp32 bits */
+    float f = (float)r;
+    uint32_t bits;
+    memcpy(&bits, &f, sizeof bits);
+    return (uint16_t)(sign | ((bits >> 16) & 0x7FFF));
+}
+
+/* x[m,k] = bf16(h[m,k] * (1 / sqrt(mean_k h[m,k]^2))), computed in fp64: the squares of fp32
+ * values are exact in fp64 and summed in increasing k, the reciprocal of the root is rounded
+ * once, and each product once before the rounding to bf16; an all-zero row gives zeros. */
+void w12o_rms_bf16(const float *h, int M, int K, uint16_t *x) {
+    for (int m = 0; m < M; ++m) {
+        const float *hr = h + (size_t)m * K;
+        double ss = 0.0;
+        for (int k = 0; k < K; ++k) ss += (double)hr[k] * (double)hr[k];
+        const double r = sqrt(ss / (double)K);
+        const double inv = (r > 0.0) ? 1.0 / r : 0.0;
+        for (int k = 0; k < K; ++k)
+            x[(size_t)m * K + k] = (r > 0.0) ? w12o_double_to_bf16((double)hr[k] * inv) : (uint16_t)0;
+    }
+}
+
+/* p[m,n] = bf16(fp32(g[m,n] u[m,n])): the fp32 product (exact in fp64, rounded once to fp32),
+ * then rounded to nearest even; g and u have row stride ld. */
+void w12o_mul_bf16(const float *g, const float *u, int M, int N, int ld, uint16_t *p) {
+    for (int m = 0; m < M; ++m)
+        for (int n = 0; n < N; ++n) {
+            const float prod = (float)((double)g[(size_t)m * ld + n] * (double)u[(size_t)m * ld + n]);
+            p[(size_t)m * N + n] = w12o_double_to_bf16((double)prod);
+        }
+}

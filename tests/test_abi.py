@@ -120,6 +120,18 @@ def test_q6_copy_shape_and_argument_checks(w12, N, K):
     assert L.w12_q6_argmax(None, None, 1, None, None, None, 0, None, 0, None) == w12.ERR_INVALID_ARG
 
 
+def test_glue_argument_checks(w12):
+    """The layer-stream glue rejects null pointers, bad sizes and unknown flags on the host."""
+    L = w12.lib()
+    P = ctypes.c_void_p
+    one = P(16)  # never dereferenced: every call below fails its argument check first
+    assert L.w12_rms_bf16(None, 1, 64, one, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_rms_bf16(one, 0, 64, one, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_rms_bf16(one, 385, 64, one, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_mul_bf16(one, one, 1, 64, 63, one, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_mul_bf16(one, None, 1, 64, 128, one, 0, None) == w12.ERR_INVALID_ARG
+
+
 def test_binding_fails_loudly_without_the_library(w12, monkeypatch):
     monkeypatch.setattr(w12, "_lib", None)
     monkeypatch.setattr(w12, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libw12.so"))

@@ -111,11 +111,6 @@ def test_lm_head_fused_argmax(w12):
     assert checked + near == 32 and checked >= 30
 
 
-def _rms_bf16(h: torch.Tensor) -> torch.Tensor:
-    """Unit-RMS rows, rounded to bf16 (the synthetic model's normalisation; glue, not W12)."""
-    return (h / h.pow(2).mean(dim=1, keepdim=True).sqrt()).to(torch.bfloat16)
-
-
 def _check_linear_sampled(w12, t, w, x, y, rng, n_samples=256):
     M, N = y.shape
     ms = rng.integers(0, M, n_samples)
@@ -126,41 +121,52 @@ def _check_linear_sampled(w12, t, w, x, y, rng, n_samples=256):
 
 
 def test_model_weight_stream(w12):
-    """64 synthetic layers + the LM head, rows carried layer to layer with residual adds."""
+    """64 synthetic layers + the LM head, rows carried layer to layer through the library's glue:
+    x = rms_bf16(h); a = q(x) (bf16); k(x), v(x) computed and dropped; h += o(a) (accumulate);
+    x2 = rms_bf16(h); p = mul_bf16(gate|up(x2)); h += down(p) (accumulate); then the head's
+    argmax of rms_bf16(h). On sampled layers every linear is checked against the oracle on the
+    GPU's own inputs, the glue against the oracle's glue, and each residual add against the
+    plain GEMM's output added in fp32."""
     layers = []
+    sampled_layers = (0, 37, 63)
     for layer in range(64):
-        lin = {}
-        for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS):
-            w = synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device="cuda")
-            lin[name] = (w12.encode(w), w if layer in (0, 37, 63) else None)
-            if layer not in (0, 37, 63):
-                del w
-        layers.append(lin)
+        ws = {name: synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device="cuda")
+              for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS)}
+        ws["gate|up"] = torch.cat([ws.pop("gate"), ws.pop("up")], dim=0)
+        keep = layer in sampled_layers
+        layers.append({name: (w12.encode(w), w if keep else None) for name, w in ws.items()})
+        del ws
     wh = synth.weights(VOCAB, K, synth.HEAD, seed=synth.seed_for(2, 0), device="cuda")
     th = w12.encode(wh)
     rng = np.random.default_rng(3)
     for M in (1, 16, 32):
         h = synth.activations(M, K, seed=synth.seed_for(3, M), device="cuda").float()
-        for lin in layers:
-            sampled = lin["q"][1] is not None
-            x = _rms_bf16(h)
+        for li, lin in enumerate(layers):
+            sampled = li in sampled_layers
+            x = w12.rms_bf16(h)
             a = w12.gemm(lin["q"][0], x, out_dtype=torch.bfloat16)
             w12.gemm(lin["k"][0], x, out_dtype=torch.bfloat16)  # computed and dropped (no attention)
             w12.gemm(lin["v"][0], x, out_dtype=torch.bfloat16)
-            o = w12.gemm(lin["o"][0], a)
-            h = h + o
-            x2 = _rms_bf16(h)
-            g = w12.gemm(lin["gate"][0], x2)
-            u = w12.gemm(lin["up"][0], x2)
-            pz = (g * u).to(torch.bfloat16)
-            d = w12.gemm(lin["down"][0], pz)
-            h = h + d
+            h0 = h.clone() if sampled else None
+            w12.gemm(lin["o"][0], a, out=h, accumulate=True)
+            h1 = h.clone() if sampled else None
+            x2 = w12.rms_bf16(h)
+            gu = w12.gemm(lin["gate|up"][0], x2)
+            pz = w12.mul_bf16(gu, N_MLP)
+            w12.gemm(lin["down"][0], pz, out=h, accumulate=True)
             if sampled:
+                o = w12.gemm(lin["o"][0], a)
+                assert torch.equal(h1.view(torch.int32), (h0 + o).view(torch.int32))
+                d = w12.gemm(lin["down"][0], pz)
+                assert torch.equal(h.view(torch.int32), (h1 + d).view(torch.int32))
+                assert np.abs(to_np_u16(x).astype(np.int32) - oracle.rms_bf16(h0.cpu().numpy()).astype(np.int32)).max() <= 1
+                assert np.array_equal(to_np_u16(pz), oracle.mul_bf16(gu[:, :N_MLP].cpu().numpy(),
+                                                                      gu[:, N_MLP:].cpu().numpy()))
                 _check_linear_sampled(w12, lin["q"][0], lin["q"][1], x, a, rng)
                 _check_linear_sampled(w12, lin["o"][0], lin["o"][1], a, o, rng)
-                _check_linear_sampled(w12, lin["gate"][0], lin["gate"][1], x2, g, rng)
+                _check_linear_sampled(w12, lin["gate|up"][0], lin["gate|up"][1], x2, gu, rng)
                 _check_linear_sampled(w12, lin["down"][0], lin["down"][1], pz, d, rng)
-        xf = _rms_bf16(h)
+        xf = w12.rms_bf16(h)
         idx, val, gap = w12.lmhead_argmax(th, xf)
         # the head's argmax against the oracle on the GPU's own final hidden rows
         y_ref, ad = oracle.gemm(to_np_u16(xf), to_np_u16(wh))

@@ -13,7 +13,9 @@
   argmax over the whole head (random heads, exact ties, Inf rows);
 - the INT6 Q-pass copy (SpecPilot §5.3, App. C): quantisation properties, hand-derived record
   bytes, a record reader written from the bit layout, and the lossless case of its GEMM against
-  the exact GEMM.
+  the exact GEMM;
+- the glue of the synthetic layer stream: bf16 rounding from fp64, the row normalisation's
+  special cases and invariances, the gate-up product against numpy's fp32 multiply.
 """
 import math
 import os
@@ -516,3 +518,59 @@ def test_gemm_q6_lossless_case_is_the_exact_gemm(orc):
     yq, adq = orc.gemm_q6(x, c)
     assert np.array_equal(yq, y)
     assert np.array_equal(adq, np.abs(bf16_values(x)) @ np.abs(wv.astype(np.float64)).T)
+
+
+# ---------------------------------------------------------------- glue of the synthetic layer stream
+
+def _bf16_rne_from_f32(f: np.ndarray) -> np.ndarray:
+    """bf16 bits of float32 values, round to nearest even (finite inputs), by integer arithmetic."""
+    b = np.ascontiguousarray(f, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def test_double_to_bf16_rounding(orc):
+    """Ties to even at both parities, the subnormal quantum 2^-133, overflow to Inf, and
+    agreement with integer rounding of fp32 values (exact in fp64)."""
+    assert orc.double_to_bf16(1.0 + 2.0 ** -8) == 0x3F80            # tie, even below
+    assert orc.double_to_bf16(1.0 + 3 * 2.0 ** -8) == 0x3F82        # tie, even above
+    assert orc.double_to_bf16(1.0 + 2.0 ** -8 + 2.0 ** -40) == 0x3F81
+    assert orc.double_to_bf16(-27.4 * 2.0 ** -133) == 0x801B        # subnormal
+    assert orc.double_to_bf16(2.0 ** -135) == 0x0000                # below half the quantum
+    assert orc.double_to_bf16(3.3895e38) == 0x7F7F and orc.double_to_bf16(3.3962e38) == 0x7F80
+    rng = np.random.default_rng(5)
+    f = (rng.standard_normal(4000) * np.exp(rng.uniform(-60, 60, 4000))).astype(np.float32)
+    want = _bf16_rne_from_f32(f)
+    got = np.array([orc.double_to_bf16(float(v)) for v in f], dtype=np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_rms_bf16_properties(orc):
+    """Constant rows give +-1; a zero row gives zeros; scaling a row by a power of two changes
+    nothing (fp64 rounding commutes with it); on random rows the result is within one bf16 ulp
+    of numpy's fp64 h / sqrt(mean h^2) and the row's mean square is 1 within bf16 precision."""
+    rng = np.random.default_rng(6)
+    h = (rng.standard_normal((6, 640)) * 3).astype(np.float32)
+    h[1] = 2.5
+    h[2] = -0.75
+    h[3] = 0.0
+    x = orc.rms_bf16(h)
+    assert np.all(x[1] == 0x3F80) and np.all(x[2] == 0xBF80) and np.all(x[3] == 0)
+    assert np.array_equal(orc.rms_bf16(h * np.float32(2.0 ** 40)), x)
+    assert np.array_equal(orc.rms_bf16(h * np.float32(2.0 ** -30)), x)
+    v = h.astype(np.float64)
+    with np.errstate(invalid="ignore"):
+        ref = v / np.sqrt(np.mean(v * v, axis=1, keepdims=True))
+    got = bf16_values(x)
+    ok = np.isfinite(ref)
+    ulp = np.exp2(np.floor(np.log2(np.abs(np.where(ref == 0, 1, ref)))) - 7)
+    assert np.all(np.abs(got[ok] - ref[ok]) <= ulp[ok] / 2 * (1 + 1e-9))
+    ms = np.mean(got[[0, 4, 5]] ** 2, axis=1)
+    assert np.all(np.abs(ms - 1) < 2 ** -7)
+
+
+def test_mul_bf16_is_rounded_fp32_product(orc):
+    """p = bf16(fp32(g u)): against numpy's fp32 multiply and an integer round-to-nearest-even."""
+    rng = np.random.default_rng(7)
+    g = (rng.standard_normal((5, 300)) * 4).astype(np.float32)
+    u = (rng.standard_normal((5, 300)) * 0.01).astype(np.float32)
+    assert np.array_equal(orc.mul_bf16(g, u), _bf16_rne_from_f32(g * u))
