@@ -219,9 +219,10 @@ w12_status w12_gemm_noalloc(const w12_tensor *t, const uint16_t *x, int M, void 
  * completed). Both let the next kernel start early; a GEMM launched with W12_LAUNCH_OVERLAP
  * waits for their completion before it reads x. M in [1, W12_MAX_M]. Asynchronous. */
 
-/* x[m, k] = bf16(h[m, k] * (1 / sqrt(mean_k h[m, k]^2))): the sum of squares, the reciprocal of
- * the root (rounded once) and each product (rounded once) in fp64, then one rounding to bf16,
- * nearest even; zeros for an all-zero row. h: device fp32 [M, K], 16-byte aligned; x: device bf16
+/* x[m, k] = h[m, k] / sqrt(mean_k h[m, k]^2) rounded to bf16 (nearest even), the quotient
+ * evaluated to about 2^-40 relative accuracy before that one rounding (so x can differ from the
+ * correctly rounded quotient only where the quotient lies that close to a rounding boundary);
+ * zeros for an all-zero row. h: device fp32 [M, K], finite, 16-byte aligned; x: device bf16
  * [M, K], 8-byte aligned. K % 4 != 0 returns W12_ERR_UNSUPPORTED_SHAPE. */
 w12_status w12_rms_bf16(const float *h, int M, int K, uint16_t *x, unsigned flags, w12_stream_t stream);
 

@@ -25,34 +25,61 @@ __device__ __forceinline__ uint16_t bf16_bits_rne(double v) {
     const uint16_t sign = static_cast<uint16_t>((b >> 48) & 0x8000u);
     const uint64_t a = b & 0x7FFFFFFFFFFFFFFFull;
     if (a > 0x7FF0000000000000ull) return 0x7FC0;  // NaN
-    const double av = __longlong_as_double(static_cast<long long>(a));
-    if (av < 0x1p-126) return sign | static_cast<uint16_t>(rint(av * 0x1p133));  // 128 = smallest normal
+    if (a < 0x3810000000000000ull)  // below 2^-126: the bf16 subnormal range; 128 = smallest normal
+        return sign | static_cast<uint16_t>(rint(__longlong_as_double(static_cast<long long>(a)) * 0x1p133));
     const uint64_t r = (a + 0x0FFFFFFFFFFFull + ((a >> 45) & 1u)) >> 45;  // exponent field | 7 mantissa bits
     const int e = static_cast<int>(r >> 7) - 1023 + 127;
     if (e >= 255) return sign | 0x7F80;
     return sign | static_cast<uint16_t>((e << 7) | static_cast<int>(r & 0x7Fu));
 }
 
-// Row m, columns [1024 c, 1024 c + 1024) per block (c = blockIdx.x, m = blockIdx.y): GB300's fp64
-// rate is low and a row is short, so the kernel is latency-bound; each block issues all its loads
-// of the row at once (16 bytes per thread and round), sums the row's squares in fp64 itself (each
-// square of an fp32 value is exact in fp64; a fixed reduction order, so every block gets the same
-// sum and the result is reproducible), takes the fp64 reciprocal of sqrt(mean) once, and rounds
-// h * that reciprocal once to bf16 (nearest even) for its 1024 columns, which its threads
-// already hold. An all-zero row gives zeros. K % 4 == 0, h 16-byte aligned.
+// Row m, columns [1024 c, 1024 c + 1024) per block (c = blockIdx.x, m = blockIdx.y). GB300's fp64
+// unit is slow and a row is short, so the kernel is latency-bound; it keeps fp64 off the long
+// dependent paths:
+//   1. every thread loads its 16-byte pieces of the whole row at once (the block's own 1024
+//      columns among them) and the block takes the largest |h|, 2^e its binade;
+//   2. the squares of h * 2^-e (at most 1, so nothing overflows) are summed in fp32 pairs
+//      (hi, lo) with error-free transformations (the exact square as p + e from an FMA; two-sum
+//      additions), across the block in a fixed order: about 2^-40 relative accuracy;
+//   3. the mean's reciprocal square root starts from the fp32 approximation and takes one Newton
+//      step in fp64 (about 2^-43), then the scaling by 2^-e is undone exactly;
+//   4. each of the thread's four columns is multiplied by it in fp64 and rounded once to bf16.
+// The result is the bf16 rounding of h / rms(h) except where that quotient lies within about
+// 2^-40 (relative) of a rounding boundary. An all-zero row gives zeros. K % 4 == 0, h finite and
+// 16-byte aligned.
 constexpr int kRmsChunk = 4 * kRmsThreads;  // columns per block
 constexpr int kRmsRound = 8;                // 16-byte loads in flight per thread
-__global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__restrict__ h, int K,
+
+struct F2 {  // an unevaluated sum hi + lo of two fp32 values
+    float hi, lo;
+};
+// a + b, with the rounding error of the leading addition carried into lo (two-sum)
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float bb = __fsub_rn(s, a.hi);
+    const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+    const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), err);
+    const float hi = __fadd_rn(s, lo);  // renormalise (|s| >= |lo|)
+    return {hi, __fsub_rn(lo, __fsub_rn(hi, s))};
+}
+
+__global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__restrict__ h, int K, double inv_k,
                                                                uint16_t *__restrict__ x) {
     grid_launch_dependents();
     grid_dependency_wait();
     const int m = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     const int K4 = K >> 2;
     const float4 *h4 = reinterpret_cast<const float4 *>(h + static_cast<size_t>(m) * K);
-    double s0 = 0.0, s1 = 0.0;
+    const int nround = (K4 + kRmsThreads * kRmsRound - 1) / (kRmsThreads * kRmsRound);
+    __shared__ float wmax[kRmsThreads / 32];
+    __shared__ F2 wsum[kRmsThreads / 32];
+    __shared__ double inv_s;
     float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);  // columns 4 (256 c + tid) .. +3
-    for (int base = 0; base < K4; base += kRmsThreads * kRmsRound) {
+    // pass 1: the largest |h| of the row (rows longer than one round are read again in pass 2)
+    float amax = 0.f;
+    for (int r = 0; r < nround; ++r) {
         float4 v[kRmsRound];
+        const int base = r * kRmsThreads * kRmsRound;
 #pragma unroll
         for (int j = 0; j < kRmsRound; ++j) {
             const int i = base + j * kRmsThreads + tid;
@@ -60,36 +87,66 @@ __global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__re
         }
 #pragma unroll
         for (int j = 0; j < kRmsRound; ++j) {
-            s0 = fma(static_cast<double>(v[j].x), static_cast<double>(v[j].x), s0);
-            s1 = fma(static_cast<double>(v[j].y), static_cast<double>(v[j].y), s1);
-            s0 = fma(static_cast<double>(v[j].z), static_cast<double>(v[j].z), s0);
-            s1 = fma(static_cast<double>(v[j].w), static_cast<double>(v[j].w), s1);
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
             if (base / kRmsThreads + j == c) mine = v[j];
         }
     }
-    double ss = s0 + s1;
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, off);
-    __shared__ double part[kRmsThreads / 32];
-    __shared__ double inv;
-    if ((tid & 31) == 0) part[tid >> 5] = ss;
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    if ((tid & 31) == 0) wmax[tid >> 5] = amax;
+    __syncthreads();
+    float bmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRmsThreads / 32; ++i) bmax = fmaxf(bmax, wmax[i]);
+    const int col = 4 * (c * kRmsThreads + tid);
+    uint16_t *xr = x + static_cast<size_t>(m) * K;
+    if (bmax == 0.f) {  // an all-zero row (block-uniform)
+        if (col < K) *reinterpret_cast<uint2 *>(xr + col) = make_uint2(0u, 0u);
+        return;
+    }
+    const int e = ilogbf(bmax) + 1;  // |h| * 2^-e < 1
+    // pass 2: the sum of squares of h * 2^-e in fp32 pairs
+    F2 acc = {0.f, 0.f};
+    for (int r = 0; r < nround; ++r) {
+        float4 v[kRmsRound];
+        const int base = r * kRmsThreads * kRmsRound;
+#pragma unroll
+        for (int j = 0; j < kRmsRound; ++j) {
+            const int i = base + j * kRmsThreads + tid;
+            v[j] = (i < K4) ? h4[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kRmsRound; ++j) {
+            const float q[4] = {ldexpf(v[j].x, -e), ldexpf(v[j].y, -e), ldexpf(v[j].z, -e), ldexpf(v[j].w, -e)};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float p = __fmul_rn(q[t], q[t]);
+                acc = f2_add(acc, F2{p, __fmaf_rn(q[t], q[t], -p)});  // q^2 = p + that, exactly
+            }
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        acc = f2_add(acc, F2{__shfl_xor_sync(0xFFFFFFFFu, acc.hi, off), __shfl_xor_sync(0xFFFFFFFFu, acc.lo, off)});
+    if ((tid & 31) == 0) wsum[tid >> 5] = acc;
     __syncthreads();
     if (tid == 0) {
-        double t = 0.0;
-        for (int i = 0; i < kRmsThreads / 32; ++i) t += part[i];
-        const double r = sqrt(t / static_cast<double>(K));
-        inv = (r > 0.0) ? 1.0 / r : 0.0;
+        F2 t = wsum[0];
+        for (int i = 1; i < kRmsThreads / 32; ++i) t = f2_add(t, wsum[i]);
+        const double mean = (static_cast<double>(t.hi) + static_cast<double>(t.lo)) * inv_k;
+        const double y0 = static_cast<double>(rsqrtf(static_cast<float>(mean)));
+        const double y1 = y0 * fma(-0.5 * mean * y0, y0, 1.5);  // one Newton step for 1 / sqrt(mean)
+        inv_s = ldexp(y1, -e);  // exact: undo the scaling of h
     }
     __syncthreads();
-    const int col = 4 * (c * kRmsThreads + tid);
     if (col < K) {
-        const double q = inv;
+        const double q = inv_s;
         uint2 out;
         out.x = static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.x) * q)) |
                 (static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.y) * q)) << 16);
         out.y = static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.z) * q)) |
                 (static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.w) * q)) << 16);
-        *reinterpret_cast<uint2 *>(x + static_cast<size_t>(m) * K + col) = out;
+        *reinterpret_cast<uint2 *>(xr + col) = out;
     }
 }
 
@@ -149,7 +206,7 @@ extern "C" w12_status w12_rms_bf16(const float *h, int M, int K, uint16_t *x, un
     W12_TRY(launch_cfg(&cfg, attr, flags, stream));
     cfg.gridDim = dim3(static_cast<unsigned>((K + kRmsChunk - 1) / kRmsChunk), static_cast<unsigned>(M));
     cfg.blockDim = dim3(kRmsThreads);
-    W12_CUDA(cudaLaunchKernelEx(&cfg, rms_bf16_kernel, h, K, x));
+    W12_CUDA(cudaLaunchKernelEx(&cfg, rms_bf16_kernel, h, K, 1.0 / static_cast<double>(K), x));
     return W12_OK;
 }
 
