@@ -117,3 +117,58 @@ def test_accumulate_rejects_bf16_and_argmax(w12):
                                w12._ptr(idx), w12._ptr(val), w12._ptr(val), w12.LAUNCH_ACCUMULATE, w12._ptr(ws), nb,
                                w12._stream())
     assert st == w12.ERR_INVALID_ARG
+
+
+def test_carried_chain_in_cuda_graph_matches_eager(w12):
+    """Two layers of the carried step as the benchmark runs them (overlapped GEMMs, the residual
+    adds accumulated into h, stream-ordered glue, all captured in one CUDA graph) give the eager
+    stream-ordered chain's h and head argmax bit for bit, replay after replay."""
+    K, NM = synth.HIDDEN, 2048
+    shapes = (("q", K, 1024), ("kv", K, 512), ("o", 1024, K), ("gu", K, 2 * NM), ("down", NM, K))
+    layers = []
+    for layer in range(2):
+        layers.append({n: w12.encode(synth.weights(no, ki, synth.PROJ, seed=97 * layer + i, device="cuda"))
+                       for i, (n, ki, no) in enumerate(shapes)})
+    th = w12.encode(synth.weights(4096, K, synth.HEAD, seed=99, device="cuda"))
+    M = 16
+    h0 = synth.activations(M, K, seed=98, device="cuda").float()
+    h = torch.empty_like(h0)
+    xa = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    a = torch.empty((M, 1024), dtype=torch.bfloat16, device="cuda")
+    kv = torch.empty((M, 512), dtype=torch.bfloat16, device="cuda")
+    gu = torch.empty((M, 2 * NM), dtype=torch.float32, device="cuda")
+    pz = torch.empty((M, NM), dtype=torch.bfloat16, device="cuda")
+
+    def chain(overlap):
+        h.copy_(h0)
+        for L in layers:
+            w12.rms_bf16(h, out=xa)
+            w12.gemm(L["q"], xa, out=a, overlap=overlap)
+            w12.gemm(L["kv"], xa, out=kv, overlap=overlap)
+            w12.gemm(L["o"], a, out=h, accumulate=True, overlap=overlap)
+            w12.rms_bf16(h, out=xa)
+            w12.gemm(L["gu"], xa, out=gu, overlap=overlap)
+            w12.mul_bf16(gu, NM, out=pz)
+            w12.gemm(L["down"], pz, out=h, accumulate=True, overlap=overlap)
+        w12.rms_bf16(h, out=xa)
+        return w12.lmhead_argmax(th, xa, overlap=overlap)
+
+    ref_idx, ref_val, _ = chain(False)
+    ref_h = h.clone()
+    torch.cuda.synchronize()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        chain(True)  # workspaces and kernel attributes before capture
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=st):
+            gi, gv, _ = chain(True)
+        for _ in range(3):
+            g.replay()
+            st.synchronize()
+            assert torch.equal(h.view(torch.int32), ref_h.view(torch.int32))
+            assert torch.equal(gi, ref_idx) and torch.equal(gv, ref_val)
+    for L in layers:
+        for t in L.values():
+            w12.check(t)
+    w12.check(th)
