@@ -8,15 +8,15 @@
 // the library's written format specification.
 //
 // Passes (all HBM-streaming, integer only):
-//   window   one warp per channel: exponent histogram -> E_n
-//   pack     one block per 128x64 record: planes and escape flags of 8192 weights; counting
-//            mode writes per-(channel, k-tile) and per-record escape counts, writing mode writes
-//            the record bytes, the per-record index and the per-channel list
+//   window   one warp per channel: exponent histogram -> E_n, then the channel's escape count
+//            per k tile and each record's total
 //   rowscan  one warp per channel: exclusive prefix of its per-k-tile counts
 //   scan     two blocks in one launch: exclusive prefixes over channels and over records ->
 //            the offsets of both escape lists
-// w12_encode_sizes runs window, pack (counting), rowscan and scan; w12_encode reuses their
-// results from the scratch and runs pack (writing) only.
+//   pack     one block per 128x64 record: planes and escape flags of 8192 weights; the record
+//            bytes, the per-record index and the per-channel list
+// w12_encode_sizes runs window, rowscan and scan; w12_encode reuses their results from the
+// scratch and runs pack only.
 #include "w12_internal.cuh"
 
 namespace w12 {
@@ -25,26 +25,26 @@ namespace {
 constexpr int kWindowWarps = 8;
 constexpr int kScanThreads = 1024;
 
-// planes of a real weight u under window base En (format rules 2 and 3)
-__device__ __forceinline__ void planes(uint32_t u, int En, uint32_t &view, uint32_t &lo, bool &esc) {
-    const uint32_t s = u >> 15, e = (u >> 7) & 0xFFu, f = u & 0x7Fu;
-    const bool normal = (e >= 1u) && (e <= 254u);
-    const bool inside = normal && (static_cast<int>(e) >= En - 15) && (static_cast<int>(e) <= En);
-    if (inside) {
-        view = ((e - static_cast<uint32_t>(En - 15)) << 4) | ((f >> 4) << 1) | s;
-        lo = f & 0xFu;
-    } else if (e == 255u || (normal && static_cast<int>(e) > En)) {
-        view = (15u << 4) | (7u << 1) | s;
-        lo = 15u;
-    } else {
-        view = s;
-        lo = 0u;
-    }
+// planes of a real weight u under the window [lo_e, lo_e + 15] = [E_n - 15, E_n] (format rules 2
+// and 3), without branches. E_n lies in [16, 254], so the window holds normal exponents only: a
+// weight is inside iff its biased exponent lies in it, above it (larger, Inf, NaN: clamped to the
+// window top, E = 15, m_hi = 7, B = 15) or below it (smaller, zero, subnormal: E = m_hi = B = 0).
+__device__ __forceinline__ void planes(uint32_t u, int lo_e, uint32_t &view, uint32_t &lo, bool &esc) {
+    const int x = static_cast<int>((u >> 7) & 0xFFu) - lo_e;  // exponent offset in the window
+    const bool inside = static_cast<uint32_t>(x) <= 15u;
+    const uint32_t t = inside ? (u & 0x7Fu) : (x > 15 ? 0x7Fu : 0u);  // mantissa or its clamp
+    const uint32_t dc = static_cast<uint32_t>(min(max(x, 0), 15));
+    view = (dc << 4) | ((t >> 3) & 0xEu) | (u >> 15);
+    lo = t & 0xFu;
     esc = !inside;
 }
 
+// One warp per channel: the exponent histogram -> E_n; then the channel's escape count per k
+// tile (the row read again, mostly from cache) into ct, and each count added to its record's
+// total (integer atomics, so the totals do not depend on the order).
 __global__ void __launch_bounds__(kWindowWarps * 32)
-window_kernel(const uint16_t *__restrict__ w, int N, int K, uint8_t *__restrict__ base_exp) {
+window_kernel(const uint16_t *__restrict__ w, int N, int K, int k_tiles, uint8_t *__restrict__ base_exp,
+              uint32_t *__restrict__ ct, uint32_t *__restrict__ rec_cnt) {
     __shared__ uint32_t hist[kWindowWarps][256];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x * kWindowWarps + warp;
@@ -88,15 +88,41 @@ window_kernel(const uint16_t *__restrict__ w, int N, int K, uint8_t *__restrict_
         }
     }
     if (lane == 0) base_exp[n] = static_cast<uint8_t>(n < N ? best_E : 16);
+    // escapes per k tile: lane l holds 16-byte piece i = l + 32 j (k = 8 i .. 8 i + 7), so the 8
+    // lanes of each lane octet share one k tile (4 j + l / 8); a weight stays in the window iff
+    // its biased exponent lies in [E_n - 15, E_n] (that range holds normal exponents only)
+    const uint32_t lo_e = static_cast<uint32_t>(best_E - 15);
+    const uint4 *row = reinterpret_cast<const uint4 *>(w + static_cast<size_t>(n) * K);
+    const int nvec = K / 8;
+    const int nt = n / kTileN;
+    for (int j0 = 0; j0 < 8 * k_tiles; j0 += 32) {
+        const int i = j0 + lane;
+        uint32_t c = 0;
+        if (n < N && i < nvec) {
+            const uint4 v = __ldg(row + i);
+            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t e = (wd[q >> 1] >> (16 * (q & 1) + 7)) & 0xFFu;
+                c += (e - lo_e > 15u) ? 1u : 0u;
+            }
+        }
+        c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+        c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
+        c += __shfl_xor_sync(0xFFFFFFFFu, c, 4);
+        const int kt = i >> 3;
+        if ((lane & 7) == 0 && kt < k_tiles) {
+            ct[static_cast<size_t>(n) * k_tiles + kt] = c;
+            if (c) atomicAdd(&rec_cnt[static_cast<size_t>(nt) * k_tiles + kt], c);
+        }
+    }
 }
 
 struct PackArgs {
     const uint16_t *w;
     int N, K, k_tiles;
     const uint8_t *base_exp;
-    uint32_t *ct;       // [n_pad * k_tiles] per-(channel, k-tile) counts / exclusive prefixes
-    uint32_t *rec_cnt;  // [R]
-    // writing mode only
+    const uint32_t *ct;  // [n_pad * k_tiles] per-(channel, k-tile) exclusive prefixes
     uint8_t *records;
     const uint32_t *rec_off;
     uint32_t *rec_esc;
@@ -131,7 +157,8 @@ __device__ __forceinline__ uint32_t block_excl_scan256(uint32_t v, uint32_t *tot
     return before + incl - v;
 }
 
-template <bool kWrite>
+// one block per record: planes of its 128 x 64 weights, the record bytes, its index segment and
+// its share of the per-channel lists
 __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
     const int r = blockIdx.x;
     const int nt = r / a.k_tiles, kt = r % a.k_tiles;
@@ -161,7 +188,7 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
         const bool real = (n < a.N) && (k0 + j < a.K);
         uint32_t view = 0, lo = 0;
         bool esc = false;
-        if (real) planes(bits, En, view, lo, esc);
+        if (real) planes(bits, En - 15, view, lo, esc);
         vw[j >> 2] |= view << (8 * (j & 3));
         const int i = j & 7;
         bw[j >> 3] |= lo << (4 * ((i >> 1) + 4 * (i & 1)));
@@ -169,14 +196,6 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
     }
     const uint32_t cnt = __popc(mask);
     const uint32_t partner = __shfl_xor_sync(0xFFFFFFFFu, cnt, 1);
-
-    if (!kWrite) {
-        if (half == 0) a.ct[static_cast<size_t>(n) * a.k_tiles + kt] = cnt + partner;
-        uint32_t total;
-        block_excl_scan256(cnt, &total);
-        if (threadIdx.x == 0) a.rec_cnt[r] = total;
-        return;
-    }
 
     uint8_t *rec = a.records + static_cast<size_t>(r) * kRecordBytes;
     reinterpret_cast<uint4 *>(rec + 2048 * (2 * half) + 16 * nl)[0] = make_uint4(vw[0], vw[1], vw[2], vw[3]);
@@ -334,17 +353,8 @@ w12_status count_pass(const uint16_t *w, int N, int K, const Scratch &s, uint8_t
     const int k_tiles = static_cast<int>(ceil_div(K, kTileK));
     const int n_pad = n_tiles * kTileN;
     const int R = n_tiles * k_tiles;
-    window_kernel<<<n_pad / kWindowWarps, kWindowWarps * 32, 0, st>>>(w, N, K, base_exp);
-    W12_CUDA(cudaGetLastError());
-    PackArgs a{};
-    a.w = w;
-    a.N = N;
-    a.K = K;
-    a.k_tiles = k_tiles;
-    a.base_exp = base_exp;
-    a.ct = s.ct;
-    a.rec_cnt = s.rec_cnt;
-    pack_kernel<false><<<R, 256, 0, st>>>(a);
+    W12_CUDA(cudaMemsetAsync(s.rec_cnt, 0, sizeof(uint32_t) * static_cast<size_t>(R), st));
+    window_kernel<<<n_pad / kWindowWarps, kWindowWarps * 32, 0, st>>>(w, N, K, k_tiles, base_exp, s.ct, s.rec_cnt);
     W12_CUDA(cudaGetLastError());
     rowscan_kernel<<<static_cast<int>(ceil_div(n_pad, 8)), 256, 0, st>>>(s.ct, n_pad, k_tiles, s.chan_cnt);
     W12_CUDA(cudaGetLastError());
@@ -414,7 +424,6 @@ extern "C" w12_status w12_encode(const uint16_t *w, int N, int K, void *scratch,
     a.k_tiles = t->k_tiles;
     a.base_exp = t->base_exp;
     a.ct = s.ct;
-    a.rec_cnt = s.rec_cnt;
     a.records = t->records;
     a.rec_off = t->rec_esc_off;
     a.rec_esc = t->rec_esc;
@@ -423,7 +432,7 @@ extern "C" w12_status w12_encode(const uint16_t *w, int N, int K, void *scratch,
     a.esc_k = t->esc_k;
     a.esc_bits = t->esc_bits;
     a.esc_cap = t->n_esc;
-    pack_kernel<true><<<R, 256, 0, st>>>(a);
+    pack_kernel<<<R, 256, 0, st>>>(a);
     W12_CUDA(cudaGetLastError());
     uint32_t tot[2] = {0, 0};
     W12_CUDA(cudaMemcpyAsync(&tot[0], t->esc_off + N, 4, cudaMemcpyDeviceToHost, st));
