@@ -604,7 +604,7 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
     them: 257 GEMMs). Concatenating output channels changes no record: a W12 tensor of
     [Wq; Wk; Wv] holds the three tensors' records one after another. The third ("carried") is
     the step itself: M rows carried from layer to layer through the library's glue (row
-    normalisation, residual adds fused into the GEMMs, the gate-up product): 321 GEMMs and 193
+    normalisation, residual adds fused into the GEMMs, the gate-up product): 257 GEMMs and 193
     glue kernels; its cuBLAS counterpart runs the same chain with torch glue."""
     from lossless_bit_weight_gb300 import w12
 
@@ -617,8 +617,9 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
                   for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS)}
             groups = {"separate": [["q"], ["k"], ["v"], ["o"], ["gate"], ["up"], ["down"]],
                       "fused": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
-                      # carried: a is its own output (o reads it), k|v are computed and dropped
-                      "carried": [["q"], ["k", "v"], ["o"], ["gate", "up"], ["down"]]}[layout]
+                      # carried: q|k|v in one GEMM (o reads the q columns in place; k and v
+                      # are computed and dropped)
+                      "carried": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]]}[layout]
             for g in groups:
                 wb = ws[g[0]] if len(g) == 1 else torch.cat([ws[n] for n in g], dim=0)
                 lin.append((w12.encode(wb), wb))
@@ -649,8 +650,8 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
                 h0 = synth.activations(M, K_HID, seed=synth.seed_for(3, M), device=dev).float()
                 h = torch.empty_like(h0)
                 xa = torch.empty((M, K_HID), dtype=torch.bfloat16, device=dev)
-                a_q = torch.empty((M, 6144), dtype=torch.bfloat16, device=dev)
-                kv = torch.empty((M, 2048), dtype=torch.bfloat16, device=dev)
+                qkv = torch.empty((M, 8192), dtype=torch.bfloat16, device=dev)
+                a_q = qkv[:, :6144]  # rows 8192 apart: the o projection reads them in place
                 gu = torch.empty((M, 2 * N_MLP), dtype=torch.float32, device=dev)
                 pz = torch.empty((M, N_MLP), dtype=torch.bfloat16, device=dev)
 
@@ -660,11 +661,10 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
                 # kernel before it runs
                 def w12_step():
                     h.copy_(h0)
-                    for i in range(0, len(lin), 5):
-                        (tq, _), (tkv, _), (to, _), (tgu, _), (td, _) = lin[i:i + 5]
+                    for i in range(0, len(lin), 4):
+                        (tqkv, _), (to, _), (tgu, _), (td, _) = lin[i:i + 4]
                         w12.rms_bf16(h, out=xa)
-                        w12.gemm(tq, xa, out=a_q, overlap=True)
-                        w12.gemm(tkv, xa, out=kv, overlap=True)
+                        w12.gemm(tqkv, xa, out=qkv, overlap=True)
                         w12.gemm(to, a_q, out=h, accumulate=True, overlap=True)
                         w12.rms_bf16(h, out=xa)
                         w12.gemm(tgu, xa, out=gu, overlap=True)
@@ -676,11 +676,10 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
                 def cublas_step():
                     # the same chain on bf16 weights: cuBLAS GEMMs, torch glue
                     h.copy_(h0)
-                    for i in range(0, len(lin), 5):
-                        (_, wq), (_, wkv), (_, wo), (_, wgu), (_, wd) = lin[i:i + 5]
+                    for i in range(0, len(lin), 4):
+                        (_, wqkv), (_, wo), (_, wgu), (_, wd) = lin[i:i + 4]
                         x = (h / h.pow(2).mean(dim=1, keepdim=True).sqrt()).to(torch.bfloat16)
-                        torch.matmul(x, wq.t(), out=a_q)
-                        torch.matmul(x, wkv.t(), out=kv)
+                        torch.matmul(x, wqkv.t(), out=qkv)
                         h.add_(torch.matmul(a_q, wo.t()).float())
                         x2 = (h / h.pow(2).mean(dim=1, keepdim=True).sqrt()).to(torch.bfloat16)
                         g = torch.matmul(x2, wgu.t()).float()

@@ -193,6 +193,14 @@ w12_status w12_gemm_ex(const w12_tensor *t, const uint16_t *x, int M, int op, vo
                        int32_t *idx, float *val, float *gap, unsigned flags, void *workspace,
                        size_t workspace_bytes, w12_stream_t stream);
 
+/* w12_gemm_ex with activation rows ldx elements apart (the paper has no counterpart): x is row m
+ * at x + m * ldx, K elements each, so a column range of a wider bf16 output (say the q part of
+ * a concatenated q|k|v projection) feeds the next GEMM without a copy. ldx >= K and ldx % 8 == 0
+ * (16-byte rows); otherwise W12_ERR_INVALID_ARG. Everything else as w12_gemm_ex. Asynchronous. */
+w12_status w12_gemm_strided(const w12_tensor *t, const uint16_t *x, int ldx, int M, int op, void *y, int y_dtype,
+                            int32_t *idx, float *val, float *gap, unsigned flags, void *workspace,
+                            size_t workspace_bytes, w12_stream_t stream);
+
 /* The paper has no counterpart of this call. It is w12_gemm for callers that cannot allocate
  * device memory: a plug-in whose host framework owns all device memory and hands none out, or a
  * serving loop that must not call cudaMalloc because cudaMalloc can synchronise the device. The

@@ -1192,9 +1192,10 @@ w12_status launch_variant(const CUtensorMap &map, const CUtensorMap &map2, const
     return W12_OK;
 }
 
+// ldx: elements between consecutive rows of x (K when 0)
 w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, int y_dtype,
                int32_t *idx, float *val, float *gap, void *ws, size_t ws_bytes, w12_stream_t stream,
-               unsigned flags = 0, const float *row_scale = nullptr, int *run_flag = nullptr) {
+               unsigned flags = 0, const float *row_scale = nullptr, int *run_flag = nullptr, int ldx = 0) {
     if (is_copy_op(op)) {
         // a separate copy (INT8 or INT6): records and row scales only
         if (!t || !t->records || !row_scale || t->N < 1 || t->K < 1) return W12_ERR_INVALID_ARG;
@@ -1219,7 +1220,9 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     if (!enc) return W12_ERR_CUDA;
     CUtensorMap map;
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(t->K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(t->K) * 2};
+    if (ldx == 0) ldx = t->K;
+    if (ldx < t->K || ldx % 8 != 0) return W12_ERR_INVALID_ARG;  // rows 16-byte aligned for the copies
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldx) * 2};
     const cuuint32_t box[2] = {kTileK, static_cast<cuuint32_t>(L.npad > 256 ? L.npad / 2 : L.npad)};
     const cuuint32_t estr[2] = {1, 1};
     if (enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t *>(x), dims, strides, box, estr,
@@ -1234,7 +1237,7 @@ w12_status run(const w12_tensor *t, const uint16_t *x, int M, int op, void *y, i
     if (L.rps == 2 && t->K % kTileK == 0) {
         const cuuint64_t dims3[3] = {static_cast<cuuint64_t>(kTileK), static_cast<cuuint64_t>(M),
                                      static_cast<cuuint64_t>(t->K / kTileK)};
-        const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(t->K) * 2, static_cast<cuuint64_t>(kTileK) * 2};
+        const cuuint64_t strides3[2] = {static_cast<cuuint64_t>(ldx) * 2, static_cast<cuuint64_t>(kTileK) * 2};
         const cuuint32_t box3[3] = {kTileK, static_cast<cuuint32_t>(L.npad), 2};
         const cuuint32_t estr3[3] = {1, 1, 1};
         x_pair = enc(&map2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(x), dims3, strides3, box3,
@@ -1422,6 +1425,17 @@ extern "C" w12_status w12_gemm_ex(const w12_tensor *t, const uint16_t *x, int M,
     if (argmax && y) return W12_ERR_INVALID_ARG;
     if (!argmax && (idx || val || gap)) return W12_ERR_INVALID_ARG;
     return w12::run(t, x, M, op, y, y_dtype, idx, val, gap, workspace, workspace_bytes, stream, flags);
+}
+
+extern "C" w12_status w12_gemm_strided(const w12_tensor *t, const uint16_t *x, int ldx, int M, int op, void *y,
+                                       int y_dtype, int32_t *idx, float *val, float *gap, unsigned flags,
+                                       void *workspace, size_t workspace_bytes, w12_stream_t stream) {
+    if (op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX || ldx < 1) return W12_ERR_INVALID_ARG;
+    const bool argmax = (op == W12_OP_ARGMAX || op == W12_OP_QVIEW_ARGMAX);
+    if (argmax && y) return W12_ERR_INVALID_ARG;
+    if (!argmax && (idx || val || gap)) return W12_ERR_INVALID_ARG;
+    return w12::run(t, x, M, op, y, y_dtype, idx, val, gap, workspace, workspace_bytes, stream, flags, nullptr,
+                    nullptr, ldx);
 }
 
 // ------------------------------------------------------------------------------------------

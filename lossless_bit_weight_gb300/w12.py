@@ -91,6 +91,7 @@ def lib() -> ctypes.CDLL:
             "w12_check": ([P, sz, P], i32),
             "w12_gemm_noalloc": ([T, P, i32, P, i32, P], i32),
             "w12_gemm_ex": ([T, P, i32, i32, P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
+            "w12_gemm_strided": ([T, P, i32, i32, i32, P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
             "w12_gemm_config": ([T, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                  ctypes.POINTER(i32)], i32),
             "w12_q8_shape": ([i32, i32, ctypes.POINTER(CQ8Head), ctypes.POINTER(sz), ctypes.POINTER(sz)], i32),
@@ -145,6 +146,14 @@ def _bits(t: torch.Tensor) -> torch.Tensor:
     if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
         raise ValueError("expected a contiguous bf16 CUDA tensor")
     return t
+
+
+def _rows(x: torch.Tensor) -> int:
+    """Row stride of a 2-D bf16 CUDA tensor whose rows are contiguous (a column slice of a wider
+    row-major tensor qualifies)."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda or x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("expected a bf16 CUDA tensor [M, K] with contiguous rows")
+    return x.stride(0)
 
 
 @dataclass
@@ -269,9 +278,11 @@ def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = F
     ``overlap`` launches with ``W12_LAUNCH_OVERLAP`` (``w12_gemm_ex``): the kernel may start, and
     fetch and decode its weights, while the previous kernel on the stream finishes; t's buffers
     must not be written by that kernel. ``test_stall`` sets the ``W12_LAUNCH_TEST_STALL`` test
-    hook (the bounded waits run out; ``check`` then raises). ``accumulate`` (fp32 ``out`` only,
+    hook (the bounded waits run out; ``check`` then raises). x may be a column slice of a wider
+    tensor (rows contiguous, row stride a multiple of 8): it then goes through
+    ``w12_gemm_strided``. ``accumulate`` (fp32 ``out`` only,
     ``W12_LAUNCH_ACCUMULATE``) adds the result into ``out`` instead of overwriting it."""
-    _bits(x)
+    ldx = _rows(x)
     M = x.shape[0]
     if x.shape[1] != t.K:
         raise ValueError("x must be [M, K]")
@@ -283,6 +294,12 @@ def gemm(t: W12Tensor, x: torch.Tensor, out_dtype=torch.float32, qview: bool = F
     ydt = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32
     op = OP_QVIEW_GEMM if qview else OP_GEMM
     ws, nb = t.workspace(M, op)
+    if ldx != t.K:
+        flags = ((LAUNCH_OVERLAP if overlap else 0) | (LAUNCH_TEST_STALL if test_stall else 0)
+                 | (LAUNCH_ACCUMULATE if accumulate else 0))
+        _check(lib().w12_gemm_strided(ctypes.byref(t.c), _ptr(x), ldx, M, op, _ptr(out), ydt, None, None, None,
+                                      flags, _ptr(ws), nb, _stream(stream)), "w12_gemm_strided")
+        return out
     if overlap or test_stall or accumulate:
         flags = ((LAUNCH_OVERLAP if overlap else 0) | (LAUNCH_TEST_STALL if test_stall else 0)
                  | (LAUNCH_ACCUMULATE if accumulate else 0))

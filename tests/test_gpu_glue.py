@@ -120,11 +120,12 @@ def test_accumulate_rejects_bf16_and_argmax(w12):
 
 
 def test_carried_chain_in_cuda_graph_matches_eager(w12):
-    """Two layers of the carried step as the benchmark runs them (overlapped GEMMs, the residual
-    adds accumulated into h, stream-ordered glue, all captured in one CUDA graph) give the eager
-    stream-ordered chain's h and head argmax bit for bit, replay after replay."""
+    """Two layers of the carried step as the benchmark runs them (overlapped GEMMs, q|k|v in one
+    GEMM whose q columns feed the o projection in place, the residual adds accumulated into h,
+    stream-ordered glue, all captured in one CUDA graph) give the eager stream-ordered chain's h
+    and head argmax bit for bit, replay after replay."""
     K, NM = synth.HIDDEN, 2048
-    shapes = (("q", K, 1024), ("kv", K, 512), ("o", 1024, K), ("gu", K, 2 * NM), ("down", NM, K))
+    shapes = (("qkv", K, 1536), ("o", 1024, K), ("gu", K, 2 * NM), ("down", NM, K))
     layers = []
     for layer in range(2):
         layers.append({n: w12.encode(synth.weights(no, ki, synth.PROJ, seed=97 * layer + i, device="cuda"))
@@ -134,8 +135,8 @@ def test_carried_chain_in_cuda_graph_matches_eager(w12):
     h0 = synth.activations(M, K, seed=98, device="cuda").float()
     h = torch.empty_like(h0)
     xa = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
-    a = torch.empty((M, 1024), dtype=torch.bfloat16, device="cuda")
-    kv = torch.empty((M, 512), dtype=torch.bfloat16, device="cuda")
+    qkv = torch.empty((M, 1536), dtype=torch.bfloat16, device="cuda")
+    a = qkv[:, :1024]  # the o projection reads the q columns in place (rows 1536 apart)
     gu = torch.empty((M, 2 * NM), dtype=torch.float32, device="cuda")
     pz = torch.empty((M, NM), dtype=torch.bfloat16, device="cuda")
 
@@ -143,8 +144,7 @@ def test_carried_chain_in_cuda_graph_matches_eager(w12):
         h.copy_(h0)
         for L in layers:
             w12.rms_bf16(h, out=xa)
-            w12.gemm(L["q"], xa, out=a, overlap=overlap)
-            w12.gemm(L["kv"], xa, out=kv, overlap=overlap)
+            w12.gemm(L["qkv"], xa, out=qkv, overlap=overlap)
             w12.gemm(L["o"], a, out=h, accumulate=True, overlap=overlap)
             w12.rms_bf16(h, out=xa)
             w12.gemm(L["gu"], xa, out=gu, overlap=overlap)

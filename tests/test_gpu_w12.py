@@ -332,6 +332,31 @@ def test_overlap_chain_in_cuda_graph(w12):
     w12.check(t2)
 
 
+@pytest.mark.parametrize("M", [1, 16, 33, 192])
+def test_strided_activations(w12, M):
+    """x as a column slice of a wider bf16 tensor (w12_gemm_strided) gives the contiguous copy's
+    results bit for bit, plain, overlapped and accumulated; row strides that are not a multiple
+    of 8 elements never reach a kernel."""
+    N, K, W = 2176, 320, 512
+    w = synth.weights(N, K, synth.PROJ, seed=71 + M, device="cuda")
+    t = w12.encode(w)
+    big = synth.activations(M, W, seed=72 + M, device="cuda")
+    xs = big[:, :K]
+    xc = xs.contiguous()
+    ref = w12.gemm(t, xc)
+    assert torch.equal(w12.gemm(t, xs).view(torch.int32), ref.view(torch.int32))
+    assert torch.equal(w12.gemm(t, xs, overlap=True).view(torch.int32), ref.view(torch.int32))
+    assert torch.equal(w12.gemm(t, xs, qview=True).view(torch.int32), w12.gemm(t, xc, qview=True).view(torch.int32))
+    y0 = torch.randn((M, N), device="cuda")
+    y = y0.clone()
+    w12.gemm(t, xs, out=y, accumulate=True)
+    assert torch.equal(y.view(torch.int32), (y0 + ref).view(torch.int32))
+    w12.check(t)
+    odd = synth.activations(M, K + 4, seed=73, device="cuda")[:, :K]
+    with pytest.raises(w12.W12Error):
+        w12.gemm(t, odd)
+
+
 def test_rows_above_limit_rejected(w12):
     """M = 385 is outside [1, 384]: the call reports an unsupported shape and launches nothing."""
     w = synth.weights(256, 128, synth.TINY, seed=61, device="cuda")
