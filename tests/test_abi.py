@@ -97,6 +97,8 @@ def test_null_tensor_is_rejected_before_device_work(w12):
     assert L.w12_workspace_size(None, 1, 0, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
     assert L.w12_gemm(None, None, 1, None, 0, None, 0, None) == w12.ERR_INVALID_ARG
     assert L.w12_gemm_noalloc(None, None, 1, None, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_gemm_strided(None, None, 64, 1, 0, None, 0, None, None, None, 0, None, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_gemm_strided(None, None, 0, 1, 0, None, 0, None, None, None, 0, None, 0, None) == w12.ERR_INVALID_ARG
     assert L.w12_encode(None, 64, 64, None, 0, None, None) == w12.ERR_INVALID_ARG
 
 
