@@ -22,12 +22,15 @@
  *     survivors): [SP] §4.1 "Certified LM head".
  *   - INT6 Q-pass copy (per-row scale, 6-bit codes, its GEMM): [SP] §5.3 "Generality Through
  *     Memory"; App. C.
+ *   - glue of the synthetic layer stream (residual add, row normalisation, gate-up product):
+ *     no page gives a layer dataflow; these follow the build's written reading of one.
  *
  * Physical details the pages leave open (window tie rule, placeholders, byte and nibble order,
  * per-record escape index) follow the build's written W12 specification; every function states
  * the rule it implements. Parity status: every function here is pinned by a CPU test
  * (round trip over all 65,536 bf16 patterns, brute-force window search, exact rational GEMM,
- * brute-force argmax, hand-derived byte fixtures); none is "parity unpinned".
+ * brute-force argmax, hand-derived byte fixtures, the lossless case of the INT6 copy, rounding
+ * ties and fp32 integer rounding for the bf16 conversion); none is "parity unpinned".
  */
 #include <math.h>
 #include <stdint.h>
