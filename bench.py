@@ -203,7 +203,7 @@ def run_reference(args, budget_s: float = 90.0):
     value = o.bytes_per_step * args.steps / el / 1e9
     cb = {"value": value, "unit": "GB/s", "cores": o.oracle.threads(), "kind": "oracle",
           "sample": o.describe(args.steps, el)}
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 0,
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / max(args.steps, 1),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD, "K": K_HID, "N": N_MLP, "M": list(MS),
