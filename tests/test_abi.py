@@ -134,6 +134,21 @@ def test_glue_argument_checks(w12):
     assert L.w12_mul_bf16(one, None, 1, 64, 128, one, 0, None) == w12.ERR_INVALID_ARG
 
 
+def test_plain_c_caller(w12, tmp_path):
+    """The header compiles as C99 with warnings as errors, a C program links against the library,
+    and its host-only calls answer without a GPU."""
+    import subprocess
+    exe = tmp_path / "c_abi_check"
+    libdir = os.path.dirname(w12.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c_abi_check.c"), "-L", libdir, "-l:libw12.so",
+                    f"-Wl,-rpath,{libdir}", "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    nt, kt = 17408 // 128, 5120 // 64
+    assert out == [str(nt), str(kt), str(nt * kt * 12288), str(nt * 128), str(1187 * kt * 8192),
+                   str(1187 * kt * 6144), "W12_ERR_TIMEOUT"]
+
+
 def test_binding_fails_loudly_without_the_library(w12, monkeypatch):
     monkeypatch.setattr(w12, "_lib", None)
     monkeypatch.setattr(w12, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libw12.so"))
