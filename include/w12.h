@@ -210,9 +210,10 @@ w12_status w12_gemm_strided(const w12_tensor *t, const uint16_t *x, int ldx, int
  * Limits: 1 <= M <= 32, at most 4096 tiles of 128 output channels (N <= 524288) and at most 256
  * thread blocks; larger problems return W12_ERR_UNSUPPORTED_SHAPE. The call allocates nothing:
  * it clears the array's counters and error word with cudaMemsetAsync on `stream`, then launches
- * the GEMM kernel. The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture. All calls on a device share the one array, so calls that overlap on the GPU race:
+ * the GEMM kernel. Every call looks up the array's device address on the current device
+ * (cudaGetSymbolAddress); the first call on a device may also load the library's device code
+ * there, so make that first call before any stream capture. All calls on a device share the one
+ * array, so calls that overlap on the GPU race:
  * order them (one stream, or events). A kernel that gives up one of its bounded waits is not
  * reported by this call (use w12_gemm with w12_check where that matters). Asynchronous. */
 w12_status w12_gemm_noalloc(const w12_tensor *t, const uint16_t *x, int M, void *y, int y_dtype,

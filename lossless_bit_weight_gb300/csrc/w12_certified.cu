@@ -1,7 +1,9 @@
 // Certified LM head (SpecPilot §4.1 "Certified LM head"): an INT8 copy of the head with a
 // per-row Cauchy-Schwarz error bound. Tokens that provably cannot be the argmax are discarded;
-// the survivors are rescored exactly from the W12 head; with too many survivors the full W12
-// argmax runs instead. The argmax is that of the whole head.
+// the survivors are rescored from the exact weights of the W12 head, with fp32 accumulation;
+// with too many survivors the full W12 argmax runs instead. The argmax is that of the whole
+// head, under the same near-tie rule as the fused argmax: a rescored logit carries fp32
+// summation error, so rows whose top-1/top-2 gap is within that error may rank either way.
 //
 // One call is five stream-ordered launches:
 //   1. the GEMM kernel over the INT8 copy (8 KB records of sign-magnitude codes, decoded exactly
@@ -10,13 +12,14 @@
 //   3. q8_select_kernel: the survivors, tokens whose upper bound yh + ||x|| d_n reaches L (they
 //      include the exact top-1 and top-2: the top-1 is at least the best lower bound, and the
 //      top-2 at least the smaller of the two best);
-//   4. q8_rescore_kernel: each survivor's exact logit, from the bf16 head's row when the caller
+//   4. q8_rescore_kernel: each survivor's fp32 logit over the exact weights, from the bf16 head's
+//      row when the caller
 //      keeps one (contiguous reads) or else from its W12 records and escapes (a gather of
 //      16-byte pieces), and the argmax and top-1/top-2 gap over the survivors;
 //   5. the W12 fused argmax, which does nothing unless a row had more survivors than the list
 //      holds.
 // All bounds are evaluated with directed rounding, and the copy's bound d_n includes the fp32
-// evaluation error of yh, so that the exact logit lies within yh -+ ||x|| d_n.
+// evaluation error of yh, so that the exact (real-number) logit lies within yh -+ ||x|| d_n.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -115,8 +118,9 @@ __global__ void __launch_bounds__(256) q8_build_kernel(const uint16_t *__restric
 }
 
 // ------------------------------------------------------------------------------------------
-// an upper bound on ||x_m||: the squares of bf16 values are exact in fp32, and every sum and
-// the square root round upwards, so the result bounds the exact norm whatever the order
+// an upper bound on ||x_m||: every square, sum and the square root round upwards, so the
+// result bounds the exact norm whatever the order (a square of a bf16 value is exact in fp32
+// unless it falls below the normal range, where the upward rounding keeps the bound)
 // ------------------------------------------------------------------------------------------
 template <int kBlock>
 __device__ float row_norm_up(const uint16_t *__restrict__ xm, int K, float *red) {
@@ -128,8 +132,8 @@ __device__ float row_norm_up(const uint16_t *__restrict__ xm, int K, float *red)
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const float a = __uint_as_float(wv[j] << 16), b = __uint_as_float(wv[j] & 0xFFFF0000u);
-            s = __fadd_ru(s, a * a);
-            s = __fadd_ru(s, b * b);
+            s = __fadd_ru(s, __fmul_ru(a, a));
+            s = __fadd_ru(s, __fmul_ru(b, b));
         }
     }
 #pragma unroll
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kBoundThreads) q8_select_kernel(const float *_
 }
 
 // ------------------------------------------------------------------------------------------
-// exact rescoring of the survivors from the W12 head
+// fp32 rescoring of the survivors over the exact weights of the W12 head
 // ------------------------------------------------------------------------------------------
 struct W12View {
     const uint16_t *wrow;  // the bf16 head, row-major [N, K], or null (rescore from the records)
@@ -247,7 +251,7 @@ __device__ __forceinline__ int xs_index(int k) { return k + (k >> 6); }
 // decodes its 64 weights of each (view bytes and plane B; in a tile that holds one of the row's
 // escapes, the escaped weights are replaced as they are used), and the lanes' sums are added by
 // a fixed shuffle tree
-__device__ float exact_logit(const W12View &h, int n, const float *xs, int lane) {
+__device__ float rescore_logit(const W12View &h, int n, const float *xs, int lane) {
     const int nt = n / 128, nl = n % 128;
     const uint32_t base2 = base2_of(h.base_exp[nt * 128 + nl]);
     const uint32_t e0 = h.esc_off[n], e1 = h.esc_off[n + 1];
@@ -318,7 +322,7 @@ __device__ float exact_logit(const W12View &h, int n, const float *xs, int lane)
 
 // y = x . w_n from the bf16 head's row n, by one warp: lane l reads the 16-byte pieces l, l + 32,
 // ... of the row (K % 8 == 0), and the lanes' sums are added by a fixed shuffle tree
-__device__ float exact_logit_bf16(const W12View &h, int n, const float *xs, int lane) {
+__device__ float rescore_logit_bf16(const W12View &h, int n, const float *xs, int lane) {
     const uint4 *row = reinterpret_cast<const uint4 *>(h.wrow + static_cast<size_t>(n) * h.K);
     const int pieces = h.K / 8;
     float acc = 0.f;
@@ -387,7 +391,7 @@ __global__ void __launch_bounds__(kRescoreThreads) q8_rescore_kernel(W12View h, 
     if (cnt <= static_cast<uint32_t>(kCap)) {
         for (uint32_t j = b * kRescoreWarps + warp; j < cnt; j += nrb * kRescoreWarps) {
             const int n = surv[static_cast<size_t>(m) * kCap + j];
-            float y = h.wrow ? exact_logit_bf16(h, n, xs, lane) : exact_logit(h, n, xs, lane);
+            float y = h.wrow ? rescore_logit_bf16(h, n, xs, lane) : rescore_logit(h, n, xs, lane);
             if (isnan(y)) y = -INFINITY;  // a NaN logit never wins (as in the fused argmax)
             top2_add(v1, i1, v2, y, n, -INFINITY);
         }
@@ -566,7 +570,7 @@ extern "C" w12_status w12_lmhead_certified(const w12_tensor *t, const w12_q8_hea
     W12_CUDA(cudaGetLastError());
     q8_select_kernel<<<bg, kBoundThreads, 0, st>>>(yh, h->N, h->bound, rnorm, Lrow, scnt, surv);
     W12_CUDA(cudaGetLastError());
-    // 4. exact rescoring from the W12 head
+    // 4. fp32 rescoring of the survivors over the exact weights
     W12View v{w_bf16, t->records, t->base_exp, t->esc_off, t->esc_k, t->esc_bits, t->N, t->K, t->k_tiles};
     const size_t xs_bytes = sizeof(float) * static_cast<size_t>(t->k_tiles) * 65;
     static std::atomic<uint64_t> smem_set{0};

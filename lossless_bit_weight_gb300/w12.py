@@ -20,7 +20,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_WORKSPACE, ERR_CUDA, ERR_MISMATC
 OUT_F32, OUT_BF16 = 0, 1
 LAUNCH_OVERLAP, LAUNCH_TEST_STALL, LAUNCH_ACCUMULATE = 1, 2, 4
 OP_GEMM, OP_QVIEW_GEMM, OP_ARGMAX, OP_QVIEW_ARGMAX = range(4)
-TILE_N, TILE_K, RECORD_BYTES, VIEW_BYTES, MAX_M = 128, 64, 12288, 8192, 256
+TILE_N, TILE_K, RECORD_BYTES, VIEW_BYTES, MAX_M = 128, 64, 12288, 8192, 384
 
 
 class W12Error(RuntimeError):

@@ -57,6 +57,7 @@ def _load():
         lib.w12o_bf16_to_double.argtypes = [ctypes.c_uint16]
         lib.w12o_bf16_to_double.restype = ctypes.c_double
         lib.w12o_threads.restype = i32
+        lib.w12o_set_threads.argtypes = [i32]
         lib.w12o_head_q8.argtypes = [P, i32, i32, P, P, P, P]
         lib.w12o_certified_argmax.argtypes = [P, i32, P, i32, i32, P, P, P, P, P, P, P]
         lib.w12o_copy_q6.argtypes = [P, i32, i32, P, P]
@@ -202,6 +203,11 @@ def threads() -> int:
     return int(_load().w12o_threads())
 
 
+def set_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on (timings on one core or on all)."""
+    _load().w12o_set_threads(int(n))
+
+
 def bf16_to_double(u: int) -> float:
     return float(_load().w12o_bf16_to_double(int(u)))
 
@@ -241,6 +247,20 @@ def certified_argmax(x, w, h: HeadQ8):
     _load().w12o_certified_argmax(_p(x), M, _p(w), N, K, _p(h.scale), _p(np.ascontiguousarray(h.q)),
                                   _p(h.resid), _p(idx), _p(val), _p(gap), _p(cnt))
     return idx, val, gap, cnt
+
+
+def gemm_q8(x, h: HeadQ8) -> tuple[np.ndarray, np.ndarray]:
+    """(yq, ad) [M, N] of the Q pass over the INT8 copy (SpecPilot §5.3 and App. C: the Q pass
+    reads a separate low-precision copy): yq = s_n (x . q_n) and ad = s_n sum_k |x_k q_nk|, in
+    fp64. The scaled-code product is the same definition as the INT6 copy's; only the codes
+    differ, so both go through one routine."""
+    x = _u16(x)
+    M, K = x.shape
+    N = h.q.shape[0]
+    y = np.zeros((M, N), dtype=np.float64)
+    ad = np.zeros((M, N), dtype=np.float64)
+    _load().w12o_gemm_q6(_p(x), M, _p(np.ascontiguousarray(h.q)), _p(h.scale), N, K, _p(y), _p(ad))
+    return y, ad
 
 
 @dataclass

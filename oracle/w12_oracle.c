@@ -355,8 +355,11 @@ void w12o_argmax(const double *y, int M, int N, int32_t *idx, double *val, doubl
 #ifdef _OPENMP
 #include <omp.h>
 int w12o_threads(void) { return omp_get_max_threads(); }
+/* threads the parallel loops use from now on (n >= 1): one core or all of them for the timings */
+void w12o_set_threads(int n) { omp_set_num_threads(n > 0 ? n : 1); }
 #else
 int w12o_threads(void) { return 1; }
+void w12o_set_threads(int n) { (void)n; }
 #endif
 
 /* ---- certified LM head: an INT8 copy with a per-row error bound -----------------------------

@@ -7,7 +7,8 @@
   survivor counts at or above the oracle's;
 - the fallback when a row has more survivors than the list holds, and that the next call runs
   without it;
-- the full-size head (vocabulary 151936 x 5120, 32 rows) against the fused W12 argmax.
+- the full-size head (vocabulary 151936 x 5120, 32 rows) against the oracle's fp64 argmax;
+- the INT8 Q pass's argmax against the oracle's INT8 logits.
 """
 import numpy as np
 import pytest
@@ -147,8 +148,10 @@ def test_certified_fallback_and_recovery(w12):
 
 
 def test_certified_full_head(w12):
-    """The LM head workload (vocabulary 151936, K=5120, 32 rows): the certified argmax equals the
-    fused W12 argmax wherever the latter's gap is clear of fp32 rounding."""
+    """The LM head workload (vocabulary 151936, K=5120, 32 rows): the certified argmax, rescored
+    from the W12 records and from a bf16 copy, against the oracle's fp64 argmax of the whole head
+    (exact top-1 wherever the oracle's gap is clear of the near-tie band, value within the GEMM
+    bound); the fused W12 argmax agrees with it."""
     V, K = 151936, 5120
     w = synth.weights(V, K, synth.HEAD, seed=synth.seed_for(2, 0), device="cuda")
     x = synth.activations(32, K, seed=synth.seed_for(2, 1), device="cuda")
@@ -158,12 +161,12 @@ def test_certified_full_head(w12):
     idx, val, gap, surv = w12.lmhead_certified(t, h, x)
     fidx, fval, fgap = w12.lmhead_argmax(t, x)
     w12.check(t)
-    assert torch.equal(idx, ib) and torch.equal(surv, sb)
-    assert np.allclose(val.cpu().numpy(), vb.cpu().numpy(), rtol=1e-5, atol=1e-4)
-    clear = fgap.cpu().numpy() > 1e-3 * fval.abs().cpu().numpy()
-    assert clear.sum() >= 30
-    assert np.array_equal(idx.cpu().numpy()[clear], fidx.cpu().numpy()[clear])
-    assert np.allclose(val.cpu().numpy(), fval.cpu().numpy(), rtol=1e-5, atol=1e-4)
+    y_ref, ad = oracle.gemm(to_np_u16(x), to_np_u16(w))
+    for i, v, g in ((idx, val, gap), (ib, vb, gb), (fidx, fval, fgap)):
+        checked, near, wrong, det = argmax_check(i.cpu().numpy(), v.cpu().numpy(), g.cpu().numpy(), y_ref, ad)
+        assert wrong == 0, det
+        assert checked + near == 32 and checked >= 30
+    assert torch.equal(surv, sb)
     s = surv.cpu().numpy()
     assert np.all(s >= 2) and np.all(s <= 4096)
 
@@ -178,12 +181,7 @@ def test_q8_argmax_matches_oracle(w12, N, K, M, seed):
     idx, val, gap = w12.q8_argmax(h, x)
     io, vo, go = w12.q8_argmax(h, x, overlap=True)
     assert torch.equal(idx, io) and torch.equal(val.view(torch.int32), vo.view(torch.int32))
-    ref = oracle.head_q8(to_np_u16(w))
-    xv = (to_np_u16(x).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    qf = ref.q.astype(np.float64)
-    s = ref.scale.astype(np.float64)[None, :]
-    yh = (xv @ qf.T) * s
-    ad = (np.abs(xv) @ np.abs(qf).T) * s
+    yh, ad = oracle.gemm_q8(to_np_u16(x), oracle.head_q8(to_np_u16(w)))
     checked, near, wrong, det = argmax_check(idx.cpu().numpy(), val.cpu().numpy(), gap.cpu().numpy(), yh, ad)
     assert wrong == 0, det
     assert checked + near == M

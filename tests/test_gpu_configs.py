@@ -2,8 +2,8 @@
 benchmark times, against the CPU oracle (fp64).
 
   tiny        K=256,  N=512,    M=1: encode bytes, decode, GEMM, Q view, argmax
-  projection  K=5120, N=17408,  M in {1,4,8,16,32}: every output element of every M; and the
-              same shape with 0.1% exact zeros (escape-heavy)
+  projection  K=5120, N=17408,  M in {1,4,8,16,32}: every output element of every M (0.1% exact
+              zeros: about nine escapes per record); and the same shape without the zeros
   LM head     K=5120, N=151936, M=32: fused argmax against the oracle's fp64 argmax
   model       64 layers (q/k/v/o, gate/up/down) + LM head, M in {1,16,32}: each linear of sampled
               layers on sampled outputs, fed the GPU's own bf16 inputs (chaining amplifies rounding)
@@ -80,15 +80,15 @@ def test_projection_gemm_every_row_count(w12, projection):
     w12.check(t)
 
 
-def test_zero_heavy_projection(w12):
-    """The projection with 0.1% exact zeros (about nine escapes per record, ten times the pages'
-    escape fraction): encode bytes, verify, and every output at M = 1, 8, 32."""
-    w = synth.weights(N_MLP, K, synth.ZERO_HEAVY, seed=synth.seed_for(1, 7), device="cuda")
+def test_light_projection(w12):
+    """The projection without exact zeros (about one escape per record, the escape fraction the
+    pages report for real models): encode bytes, verify, and every output at M = 1, 8, 32."""
+    w = synth.weights(N_MLP, K, synth.LIGHT, seed=synth.seed_for(1, 7), device="cuda")
     t = w12.encode(w)
     e = oracle.encode(to_np_u16(w))
     assert np.array_equal(t.records.cpu().numpy(), e.records)
     assert np.array_equal(t.rec_esc.cpu().numpy().view(np.uint32)[: t.n_rec_esc], e.rec_esc)
-    assert t.n_esc > 8 * t.n_tiles * t.k_tiles
+    assert t.n_esc < 2 * t.n_tiles * t.k_tiles
     assert w12.verify(t, w) == 0
     x32 = synth.activations(32, K, seed=synth.seed_for(1, 232), device="cuda")
     y_ref, ad = oracle.gemm(to_np_u16(x32), to_np_u16(w))

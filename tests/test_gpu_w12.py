@@ -183,7 +183,7 @@ def test_gemm_repeat_stress(w12, M, qview):
     bitwise equal to the first. Covers
     the ring configurations where the pipeline's stage count is not a multiple of the decode
     groups (slots shared between groups) as well as those where it is."""
-    w = synth.weights(17408, 5120, synth.ZERO_HEAVY, seed=13, device="cuda")
+    w = synth.weights(17408, 5120, synth.PROJ, seed=13, device="cuda")
     t = w12.encode(w)
     del w
     copies = [t] + [t.clone_records() for _ in range(2)]

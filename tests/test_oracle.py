@@ -520,6 +520,42 @@ def test_gemm_q6_lossless_case_is_the_exact_gemm(orc):
     assert np.array_equal(adq, np.abs(bf16_values(x)) @ np.abs(wv.astype(np.float64)).T)
 
 
+def test_gemm_q8_lossless_case_and_brute_force(orc):
+    """The INT8 Q pass: rows whose weights are integers times 2^-e with a maximum of 127 * 2^-e
+    quantise without loss (scale 2^-e, codes the integers), so its logits equal the exact fp64
+    GEMM bit for bit; on an ordinary tiny head each logit equals s_n times the brute-force sum of
+    x_k q_nk, written out with Python integers and fractions."""
+    from fractions import Fraction
+
+    rng = np.random.default_rng(23)
+    N, K, M = 24, 192, 3
+    ints = rng.integers(-127, 128, size=(N, K))
+    ints[:, 5] = -127
+    e = rng.integers(2, 10, size=N)
+    wv = (ints * (2.0 ** -e)[:, None]).astype(np.float32)
+    w = (wv.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(bf16_values(w), wv.astype(np.float64))
+    x = synth.activations(M, K, seed=24).view(torch.int16).numpy().view(np.uint16)
+    h = orc.head_q8(w)
+    assert np.array_equal(h.scale.astype(np.float64), 2.0 ** -e)
+    assert np.array_equal(h.q.astype(np.int64), ints)
+    y, _ = orc.gemm(x, w)
+    yq, adq = orc.gemm_q8(x, h)
+    assert np.array_equal(yq, y)
+    assert np.array_equal(adq, np.abs(bf16_values(x)) @ np.abs(wv.astype(np.float64)).T)
+    # an ordinary head: compare with exact rational sums (the fp64 sum of at most 64 products of
+    # a bf16 value and a 7-bit integer is exact, so equality is exact too)
+    w2 = synth.weights(16, 64, synth.HEAD, seed=25).view(torch.int16).numpy().view(np.uint16)
+    x2 = synth.activations(2, 64, seed=26).view(torch.int16).numpy().view(np.uint16)
+    h2 = orc.head_q8(w2)
+    yq2, _ = orc.gemm_q8(x2, h2)
+    xv = bf16_values(x2)
+    for m in range(2):
+        for n in range(16):
+            acc = sum(Fraction(float(xv[m, k])) * int(h2.q[n, k]) for k in range(64))
+            assert yq2[m, n] == float(Fraction(float(h2.scale[n])) * acc)
+
+
 # ---------------------------------------------------------------- glue of the synthetic layer stream
 
 def _bf16_rne_from_f32(f: np.ndarray) -> np.ndarray:

@@ -3,9 +3,10 @@
 It serves callers that cannot allocate device memory (a plug-in whose host framework hands out
 no device memory, a serving loop that must not call cudaMalloc because it can synchronise the
 device): its workspace is a fixed array inside the library. These tests call it through the C
-ABI and check its output against w12_gemm's, within the GEMM error bound the other tests use,
-on two calls in a row (the array keeps the previous call's contents). The file name sorts last,
-so a run that stops at the first failure has already run every other test.
+ABI and check its output against w12_gemm's and against the oracle's fp64 product, within the
+GEMM error bound the other tests use, on two calls in a row (the array keeps the previous call's
+contents). The file name sorts last, so a run that stops at the first failure has already run
+every other test.
 """
 import ctypes
 
@@ -43,15 +44,15 @@ def test_noalloc_matches_gemm_on_two_calls(w12, N, K, M):
     t = w12.encode(w)
     x = synth.activations(M, K, seed=M, device="cuda")
     ref = w12.gemm(t, x)
-    _, absdot = oracle.gemm_sampled(to_np_u16(x), to_np_u16(w), np.repeat(np.arange(M), N),
-                                    np.tile(np.arange(N), M))
-    tol = REL * absdot.reshape(M, N) + ABS
+    y_ref, absdot = oracle.gemm(to_np_u16(x), to_np_u16(w))
+    tol = REL * absdot + ABS
     for _ in range(2):
         y = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
         assert _call(w12, t, x, y) == w12.OK
         torch.cuda.synchronize()
         diff = (y - ref).abs().double().cpu().numpy()
         assert np.all(diff <= tol)
+        assert np.all(np.abs(y.double().cpu().numpy() - y_ref) <= tol)
 
 
 def test_noalloc_rejects_problems_beyond_its_array(w12):
