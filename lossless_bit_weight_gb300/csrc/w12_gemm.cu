@@ -576,12 +576,13 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             decode_chunk16<false, 0>(v2, b1, base2, w + 16, m3, m15);
             decode_chunk16<false, 1>(v3, b1, base2, w + 24, m3, m15);
         };
-        // Restore the escapes of record q of slot s that fall in this warp's 32 rows, in the
-        // registers of the decoded row before it goes to tensor memory. The segment header gives
-        // the warp's entry range directly (the typical warp has 0-3 entries); every lane reads
-        // the same entry (a broadcast), so the loop and the word index are warp-uniform, and only
-        // the owner lane's word changes: keep = all ones and put = 0 leave the others as they are.
-        auto patch_record = [&](int s, int q, uint2 ei, uint32_t (&w)[32]) {
+        // Restore the escapes of record q of slot s that fall in this warp's 32 rows, in tensor
+        // memory after the decoded record was stored there: read the entry's column, let the
+        // owner lane overwrite its half, write the column back. One entry per round trip (a
+        // few instructions each; the typical warp has 0-3). The segment header gives the
+        // warp's entry range directly; every lane reads the same entry (a broadcast), so the
+        // control flow is warp-uniform.
+        auto patch_record = [&](int s, int q, uint2 ei) {
             const uint32_t hdr = ei.x;
             const uint32_t total = hdr & 0x7FFFFFFFu;
             const uint32_t split = ei.y;
@@ -590,12 +591,16 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             const uint32_t *seg = ((hdr >> 31) ? p.rec_esc + ctrl->esc_src[s]
                                                : reinterpret_cast<const uint32_t *>(stage_esc(s))) + sg0;
             const uint32_t i_hi = seg[qw];
+            const uint32_t tbase = a_slot(s, q) + (static_cast<uint32_t>(32 * qw) << 16);
             for (uint32_t i = (qw == 0) ? 0u : seg[qw - 1]; i < i_hi; ++i) {
                 const uint32_t ent = seg[4 + i];
-                const bool mine = lane == static_cast<int>((ent >> 6) & 31u);
-                const uint32_t keep = mine ? ((ent & 1u) ? 0x0000FFFFu : 0xFFFF0000u) : 0xFFFFFFFFu;
-                const uint32_t put = mine ? ((ent & 1u) ? (ent & 0xFFFF0000u) : (ent >> 16)) : 0u;
-                patch_word32(w, (ent & 63u) >> 1, keep, put);
+                const uint32_t taddr = tbase + ((ent & 63u) >> 1);
+                const uint32_t old = tmem_ld_32x32b_x1(taddr);
+                tmem_wait_ld();
+                const uint32_t nv = (ent & 1u) ? ((old & 0x0000FFFFu) | (ent & 0xFFFF0000u))
+                                               : ((old & 0xFFFF0000u) | (ent >> 16));
+                tmem_st_32x32b_x1(taddr, lane == static_cast<int>((ent >> 6) & 31u) ? nv : old);
+                tmem_wait_st();
             }
         };
         int js = g;
@@ -620,21 +625,24 @@ w12_gemm_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant_
             const bool ok_full = mbar_wait(smem_u32(&ctrl->full[s]), st.phase, abort, p.err, kErrDecode);
             if (!__all_sync(0xFFFFFFFFu, ok_full)) break;
             const int nr = min(RPS, nrec - js * RPS);
-            // the escape feeder wrote the slot's index summary before its arrive on full
-            const uint2 ei = kQView ? make_uint2(0u, 0u) : ctrl->esc_info[s];
             // the slot's tensor-memory buffers are free: the producer refilled this slot only
             // after the MMAs that last read it completed
             decode_record(s, 0, kCopy ? 0u : base2_for(tile), wa);
-            if (!kQView && ei.x != 0) patch_record(s, 0, ei, wa);  // the slot has index words
             tc_fence_after();
             tmem_st_32x32b_x32(a_slot(s, 0) + (static_cast<uint32_t>(32 * qw) << 16), wa);
             if (nr == 2) {
                 const int tile1 = (kt + 1 == p.k_tiles) ? tile + 1 : tile;
                 decode_record(s, 1, kCopy ? 0u : base2_for(tile1), wb);
-                if (!kQView && ei.x != 0) patch_record(s, 1, ei, wb);
                 tmem_st_32x32b_x32(a_slot(s, 1) + (static_cast<uint32_t>(32 * qw) << 16), wb);
             }
             tmem_wait_st();
+            if (!kQView) {
+                const uint2 ei = ctrl->esc_info[s];
+                if (ei.x != 0) {  // the slot has index words
+                    patch_record(s, 0, ei);
+                    if (nr == 2) patch_record(s, 1, ei);
+                }
+            }
             tc_fence_before();
             mbar_arrive(smem_u32(&ctrl->afull[s]));
             st.advance(kDecGroups, S);

@@ -415,6 +415,16 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         : "memory");
 }
 
+// One 32-bit column of the warp's 32 lanes (each lane its own value).
+__device__ __forceinline__ uint32_t tmem_ld_32x32b_x1(uint32_t taddr) {
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr) : "memory");
+    return v;
+}
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
 // Each lane loads 16 consecutive 32-bit columns of its own TMEM lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -567,58 +577,6 @@ __device__ __forceinline__ void decode_q6_group16(uint32_t lw0, uint32_t lw1, ui
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(o) : "r"(v), "r"(0x43204320u));
         out[j] = o;
     }
-}
-
-// w[j] = (w[j] & keep) | put for a run-time word index j in [0, 32), with w held in registers.
-// An indexed register array would be moved to local memory, and 32 compares and selects cost
-// more than the escape they patch; an indirect branch through a 32-entry table (brx.idx) runs
-// one logic op. j must lie in [0, 32): brx.idx with an index outside its table is undefined.
-// Callers pass a warp-uniform j, so the branch does not diverge.
-__device__ __forceinline__ void patch_word32(uint32_t (&w)[32], uint32_t j, uint32_t keep, uint32_t put) {
-    asm volatile(
-        "{\n\t"
-        "Ltab: .branchtargets L0, L1, L2, L3, L4, L5, L6, L7, L8, L9, L10, L11, L12, L13, L14, L15, "
-        "L16, L17, L18, L19, L20, L21, L22, L23, L24, L25, L26, L27, L28, L29, L30, L31;\n\t"
-        "brx.idx %32, Ltab;\n\t"
-        "L0: lop3.b32 %0, %0, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L1: lop3.b32 %1, %1, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L2: lop3.b32 %2, %2, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L3: lop3.b32 %3, %3, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L4: lop3.b32 %4, %4, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L5: lop3.b32 %5, %5, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L6: lop3.b32 %6, %6, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L7: lop3.b32 %7, %7, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L8: lop3.b32 %8, %8, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L9: lop3.b32 %9, %9, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L10: lop3.b32 %10, %10, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L11: lop3.b32 %11, %11, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L12: lop3.b32 %12, %12, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L13: lop3.b32 %13, %13, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L14: lop3.b32 %14, %14, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L15: lop3.b32 %15, %15, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L16: lop3.b32 %16, %16, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L17: lop3.b32 %17, %17, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L18: lop3.b32 %18, %18, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L19: lop3.b32 %19, %19, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L20: lop3.b32 %20, %20, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L21: lop3.b32 %21, %21, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L22: lop3.b32 %22, %22, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L23: lop3.b32 %23, %23, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L24: lop3.b32 %24, %24, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L25: lop3.b32 %25, %25, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L26: lop3.b32 %26, %26, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L27: lop3.b32 %27, %27, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L28: lop3.b32 %28, %28, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L29: lop3.b32 %29, %29, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L30: lop3.b32 %30, %30, %33, %34, 0xEA;\n\tbra.uni Lend;\n\t"
-        "L31: lop3.b32 %31, %31, %33, %34, 0xEA;\n\t"
-        "Lend:\n\t}"
-        : "+r"(w[0]), "+r"(w[1]), "+r"(w[2]), "+r"(w[3]), "+r"(w[4]), "+r"(w[5]), "+r"(w[6]), "+r"(w[7]),
-          "+r"(w[8]), "+r"(w[9]), "+r"(w[10]), "+r"(w[11]), "+r"(w[12]), "+r"(w[13]), "+r"(w[14]),
-          "+r"(w[15]), "+r"(w[16]), "+r"(w[17]), "+r"(w[18]), "+r"(w[19]), "+r"(w[20]), "+r"(w[21]),
-          "+r"(w[22]), "+r"(w[23]), "+r"(w[24]), "+r"(w[25]), "+r"(w[26]), "+r"(w[27]), "+r"(w[28]),
-          "+r"(w[29]), "+r"(w[30]), "+r"(w[31])
-        : "r"(j & 31u), "r"(keep), "r"(put));
 }
 
 __device__ __forceinline__ uint32_t base2_of(int En) {
