@@ -668,11 +668,11 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
         if rec is not synth.HEAD:
             del wa, ta
     out["qpass_top1_agreement_M64"] = agree
-    out["model_stream"] = model_stream(dev, th, wh)
+    out["model_stream"] = model_stream(dev, th, wh, hbm_peak)
     return out
 
 
-def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
+def model_stream(dev, th, wh, hbm_peak, Ms=(1, 16, 32), steps=5, layouts=("separate", "fused", "carried")):
     """One decoding step of the synthetic 64-layer model, captured once in a CUDA graph and
     replayed; the same sequence with bf16 cuBLAS on the unencoded weights beside it. Three
     layouts. Two stream the weights on fixed activations (no glue between the GEMMs): the seven
@@ -687,8 +687,9 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
 
     res = {"layers": 64, "by_layout": {}}
     stream = torch.cuda.Stream(device=dev)
-    for layout in ("separate", "fused", "carried"):
+    for layout in layouts:
         lin = []
+        stream_layers = []
         for layer in range(64):
             ws = {name: synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device=dev)
                   for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS)}
@@ -700,6 +701,11 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
             for g in groups:
                 wb = ws[g[0]] if len(g) == 1 else torch.cat([ws[n] for n in g], dim=0)
                 lin.append((w12.encode(wb), wb))
+            if layout == "carried":
+                # the persistent step reads gate|up interleaved in blocks of 64 rows
+                t_qkv, t_o, t_d = lin[-4][0], lin[-3][0], lin[-1][0]
+                stream_layers.append({"qkv": t_qkv, "o": t_o, "down": t_d,
+                                      "gate_up": w12.encode(w12.stream_interleave(ws["gate"], ws["up"]))})
             del ws
         w12_bytes = sum(t.gemm_bytes() for t, _ in lin) + th.gemm_bytes()
         bf16_bytes = sum(wb.numel() * 2 for _, wb in lin) + wh.numel() * 2
@@ -786,6 +792,30 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
                 nbytes = w12_bytes if name == "w12" else bf16_bytes
                 row[name] = {"ms_per_step": round(ms, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
                 del g
+            if layout == "carried":
+                # the same step in one persistent launch (w12_stream_step), then the LM head's
+                # argmax as an overlapped launch; timed between events over `steps` steps
+                step = w12.StreamStep(stream_layers, M, 6144)
+                xo = torch.empty((M, K_HID), dtype=torch.bfloat16, device=dev)
+                with torch.cuda.stream(stream):
+                    for _ in range(2):
+                        h.copy_(h0)
+                        step(h, xo)
+                        w12.lmhead_argmax(th, xo, overlap=True)
+                    torch.cuda.synchronize()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    for _ in range(steps):
+                        h.copy_(h0)
+                        step(h, xo)
+                        w12.lmhead_argmax(th, xo, overlap=True)
+                    b.record(stream)
+                    b.synchronize()
+                step.check()
+                ms = a.elapsed_time(b) / steps
+                row["w12_persistent"] = {"ms_per_step": round(ms, 3), "gbs": round(w12_bytes / (ms * 1e-3) / 1e9, 1),
+                                         "frac_of_roofline": round(w12_bytes / (hbm_peak * 1e9) / (ms * 1e-3), 3)}
+                del step
             for t, _ in lin[:7]:
                 w12.check(t)
             row_l["by_m"][str(M)] = row
@@ -793,7 +823,7 @@ def model_stream(dev, th, wh, Ms=(1, 16, 32), steps=5):
             row_l["glue_kernels_per_step"] = 2 * 64 + 64 + 1
             row_l["gemms_per_step"] = len(lin) + 1
         res["by_layout"][layout] = row_l
-        del lin
+        del lin, stream_layers
         torch.cuda.empty_cache()
     return res
 

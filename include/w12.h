@@ -241,6 +241,59 @@ w12_status w12_rms_bf16(const float *h, int M, int K, uint16_t *x, unsigned flag
 w12_status w12_mul_bf16(const float *g, const float *u, int M, int N, int ld, uint16_t *p, unsigned flags,
                         w12_stream_t stream);
 
+/* ---- f3: the persistent cross-GEMM kernel of the layer stream (SpecPilot App. F and Table
+ *      A7, "persistent cross-GEMM W12": one kernel over a sequence of W12 GEMMs) ---------------
+ * One cooperative launch runs a whole decoding step of the synthetic layer stream above, every
+ * GEMM and every glue step of n_layers layers, then the final row normalisation:
+ *   per layer  x = rms_bf16(h); qkv = bf16(x Wqkv^T); h += qkv[:, :n_q] Wo^T;
+ *              x2 = rms_bf16(h); p = bf16((x2 Wg^T) * (x2 Wu^T)); h += p Wd^T
+ *   then       x_out = rms_bf16(h)
+ * with the arithmetic of the separate calls (w12_gemm with the same work split, w12_rms_bf16,
+ * w12_mul_bf16, W12_LAUNCH_ACCUMULATE), so it gives the rows that chain of launches gives.
+ * Weights stream continuously from one GEMM to the next: a GEMM's records are fetched and
+ * decoded while the phase before it finishes, and only its activation copies wait for that
+ * phase to complete on every block. The kernel uses every SM (one block each; a cooperative
+ * launch, so it fails with W12_ERR_CUDA rather than starting when the GPU cannot hold them all). */
+enum { W12_STREAM_MAX_LAYERS = 80, W12_STREAM_MAX_M = 32 };
+
+/* The four encoded linears of one layer. All layers must have the same shapes:
+ *   qkv      [n_qkv, hidden]: q in its first n_q rows, then k and v (their outputs are dropped)
+ *   o        [hidden, n_q]
+ *   gate_up  [2 * ffn, hidden]: rows 128 i .. 128 i + 63 are gate rows 64 i .., rows
+ *            128 i + 64 .. 128 i + 127 the matching up rows (w12_stream_interleave builds it)
+ *   down     [hidden, ffn]
+ * hidden, ffn and n_q must be multiples of 64 and n_qkv a multiple of 8, else
+ * W12_ERR_UNSUPPORTED_SHAPE. */
+typedef struct {
+    w12_tensor qkv, o, gate_up, down;
+} w12_stream_layer;
+
+/* Workspace bytes of w12_stream_step (host only). The workspace must be zero-filled once before
+ * its first use; every completed step leaves its counters zeroed. It also holds the step's
+ * intermediate activations. 1 <= n_layers <= W12_STREAM_MAX_LAYERS, 1 <= M <= W12_STREAM_MAX_M. */
+w12_status w12_stream_workspace_size(const w12_stream_layer *layers, int n_layers, int M, int n_q, size_t *bytes);
+
+/* Byte offsets inside the workspace of the last layer's intermediates after a step (host only,
+ * for inspection and tests): offsets[0] x (bf16 [M, hidden]), [1] the q|k|v output (bf16
+ * [M, n_qkv]), [2] x2 (bf16 [M, hidden]), [3] p (bf16 [M, ffn]). */
+w12_status w12_stream_buffers(const w12_stream_layer *layers, int n_layers, int M, int n_q, size_t offsets[4]);
+
+/* One decoding step over n_layers layers (layers: a HOST array of n_layers descriptors whose
+ * buffers are device memory). h: device fp32 [M, hidden], 16-byte aligned, the rows carried in
+ * (updated in place); x_out: device bf16 [M, hidden], 8-byte aligned, receives rms_bf16 of the
+ * final h (the LM head's input). workspace: device, 256-byte aligned, w12_stream_workspace_size
+ * bytes. Asynchronous on `stream`. Every wait inside the kernel is bounded (about a second); a
+ * block that gives up sets the workspace's error word (w12_check reports W12_ERR_TIMEOUT). */
+w12_status w12_stream_step(const w12_stream_layer *layers, int n_layers, int M, int n_q, float *h, uint16_t *x_out,
+                           void *workspace, size_t workspace_bytes, w12_stream_t stream);
+
+/* The gate|up layout w12_stream_step reads, from gate and up (device bf16 [ffn, hidden] each,
+ * row-major; ffn % 64 == 0): gate_up (device bf16 [2 * ffn, hidden]) gets gate rows 64 i .. 64 i
+ * + 63 at rows 128 i .., and up rows 64 i .. at rows 128 i + 64 ... Two strided device copies on
+ * `stream`; asynchronous. */
+w12_status w12_stream_interleave(const uint16_t *gate, const uint16_t *up, int ffn, int hidden, uint16_t *gate_up,
+                                 w12_stream_t stream);
+
 /* SYNCHRONISES `stream`, then reports W12_ERR_TIMEOUT if a GEMM kernel that used this
  * workspace gave up one of its bounded waits (its outputs are then invalid and the workspace
  * must be zero-filled again); W12_OK otherwise. Clears the flag. */

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libw12.so")
-SOURCES = ["w12_common.cu", "w12_encode.cu", "w12_decode.cu", "w12_gemm.cu", "w12_certified.cu", "w12_q6.cu", "w12_glue.cu"]
+SOURCES = ["w12_common.cu", "w12_encode.cu", "w12_decode.cu", "w12_gemm.cu", "w12_certified.cu", "w12_q6.cu", "w12_glue.cu", "w12_stream.cu"]
 HEADERS = [os.path.join(CSRC, "w12_internal.cuh"), os.path.join(ROOT, "include", "w12.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,5 +1,7 @@
 // Host-side plumbing shared by every W12 entry point: status names, device check, shape and
 // tensor validation.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "w12_internal.cuh"
@@ -29,6 +31,21 @@ w12_status require_device(int *sm_count) {
     if (g_device_ok[dev] != 1) return W12_ERR_DEVICE;
     if (sm_count) *sm_count = g_sm_count[dev];
     return W12_OK;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link to libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
 }
 
 w12_status check_shape(int N, int K) {

@@ -1051,20 +1051,6 @@ w12_reduce_kernel(const Params p) {
 // host side
 // ------------------------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    });
-    return fn;
-}
-
 // internal operations over the INT8 head copy (reached through the certified-head entry points)
 constexpr int kOpQ8 = 100;        // y = scale_n (x . q_n)
 constexpr int kOpQ8Argmax = 101;  // its row argmax (the Q pass over the separate copy)

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,6 +42,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 w12_status check_shape(int N, int K);
+// cuTensorMapEncodeTiled from the driver, or null if the driver does not provide it
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 w12_status check_tensor(const w12_tensor *t);
 
 // GEMM entry points shared between translation units (defined in w12_gemm.cu):
@@ -577,6 +580,37 @@ __device__ __forceinline__ void decode_q6_group16(uint32_t lw0, uint32_t lw1, ui
         asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(o) : "r"(v), "r"(0x43204320u));
         out[j] = o;
     }
+}
+
+// ---- arithmetic of the layer stream's row normalisation (shared by its kernels) ----------
+
+// bf16 bits of a double, rounded to nearest even in one step: on the bit pattern for results in
+// the normal range (the 52-bit mantissa rounded to 7 bits; a carry moves into the exponent, and
+// an exponent beyond 127 gives Inf), by an exact scaling to the subnormal quantum 2^-133 below.
+__device__ __forceinline__ uint16_t bf16_bits_rne(double v) {
+    const uint64_t b = static_cast<uint64_t>(__double_as_longlong(v));
+    const uint16_t sign = static_cast<uint16_t>((b >> 48) & 0x8000u);
+    const uint64_t a = b & 0x7FFFFFFFFFFFFFFFull;
+    if (a > 0x7FF0000000000000ull) return 0x7FC0;  // NaN
+    if (a < 0x3810000000000000ull)  // below 2^-126: the bf16 subnormal range; 128 = smallest normal
+        return sign | static_cast<uint16_t>(rint(__longlong_as_double(static_cast<long long>(a)) * 0x1p133));
+    const uint64_t r = (a + 0x0FFFFFFFFFFFull + ((a >> 45) & 1u)) >> 45;  // exponent field | 7 mantissa bits
+    const int e = static_cast<int>(r >> 7) - 1023 + 127;
+    if (e >= 255) return sign | 0x7F80;
+    return sign | static_cast<uint16_t>((e << 7) | static_cast<int>(r & 0x7Fu));
+}
+
+struct F2 {  // an unevaluated sum hi + lo of two fp32 values
+    float hi, lo;
+};
+// a + b, with the rounding error of the leading addition carried into lo (two-sum)
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
+    const float s = __fadd_rn(a.hi, b.hi);
+    const float bb = __fsub_rn(s, a.hi);
+    const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(b.hi, bb));
+    const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), err);
+    const float hi = __fadd_rn(s, lo);  // renormalise (|s| >= |lo|)
+    return {hi, __fsub_rn(lo, __fsub_rn(hi, s))};
 }
 
 __device__ __forceinline__ uint32_t base2_of(int En) {

@@ -42,6 +42,12 @@ class CTensor(ctypes.Structure):
     ]
 
 
+class CStreamLayer(ctypes.Structure):
+    """Mirror of ``w12_stream_layer``."""
+
+    _fields_ = [("qkv", CTensor), ("o", CTensor), ("gate_up", CTensor), ("down", CTensor)]
+
+
 class CQ8Head(ctypes.Structure):
     """Mirror of ``w12_q8_head``."""
 
@@ -107,6 +113,10 @@ def lib() -> ctypes.CDLL:
             "w12_q6_workspace_size": ([ctypes.POINTER(CQ6Copy), i32, i32, ctypes.POINTER(sz)], i32),
             "w12_q6_gemm": ([ctypes.POINTER(CQ6Copy), P, i32, P, i32, ctypes.c_uint, P, sz, P], i32),
             "w12_q6_argmax": ([ctypes.POINTER(CQ6Copy), P, i32, P, P, P, ctypes.c_uint, P, sz, P], i32),
+            "w12_stream_workspace_size": ([ctypes.POINTER(CStreamLayer), i32, i32, i32, ctypes.POINTER(sz)], i32),
+            "w12_stream_buffers": ([ctypes.POINTER(CStreamLayer), i32, i32, i32, ctypes.POINTER(sz)], i32),
+            "w12_stream_step": ([ctypes.POINTER(CStreamLayer), i32, i32, i32, P, P, P, sz, P], i32),
+            "w12_stream_interleave": ([P, P, i32, i32, P, P], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -523,3 +533,76 @@ def mul_bf16(gu: torch.Tensor, N: int, out: torch.Tensor | None = None, stream=N
     _check(lib().w12_mul_bf16(_ptr(gu), gu.data_ptr() + 4 * N, M, N, 2 * N, _ptr(out),
                               LAUNCH_OVERLAP if overlap else 0, _stream(stream)), "w12_mul_bf16")
     return out
+
+
+STREAM_MAX_LAYERS, STREAM_MAX_M = 80, 32
+
+
+def stream_interleave(gate: torch.Tensor, up: torch.Tensor, stream=None) -> torch.Tensor:
+    """The gate|up matrix the layer-stream step reads (``w12_stream_interleave``): bf16 [2F, H]
+    with gate rows 64i.. at rows 128i.. and the matching up rows at rows 128i+64..; gate and up
+    are bf16 [F, H] CUDA tensors."""
+    _bits(gate)
+    _bits(up)
+    if gate.shape != up.shape:
+        raise ValueError("gate and up must have the same shape")
+    F, H = gate.shape
+    out = torch.empty((2 * F, H), dtype=torch.bfloat16, device=gate.device)
+    _check(lib().w12_stream_interleave(_ptr(gate), _ptr(up), F, H, _ptr(out), _stream(stream)),
+           "w12_stream_interleave")
+    return out
+
+
+class StreamStep:
+    """One decoding step of the synthetic layer stream in one persistent launch
+    (``w12_stream_step``): every layer's row normalisations, q|k|v, o (added into h), gate|up with
+    the gate-up product, down (added into h), then the final row normalisation.
+
+    ``layers`` is a list of dicts with encoded tensors under "qkv", "o", "gate_up" (interleaved by
+    ``stream_interleave``) and "down"; the workspace is allocated here and kept."""
+
+    def __init__(self, layers: list, M: int, n_q: int, device="cuda"):
+        n = len(layers)
+        if not 1 <= n <= STREAM_MAX_LAYERS:
+            raise ValueError(f"1 to {STREAM_MAX_LAYERS} layers")
+        self.tensors = layers  # keeps the device buffers alive
+        self.arr = (CStreamLayer * n)()
+        for i, ly in enumerate(layers):
+            self.arr[i] = CStreamLayer(ly["qkv"].c, ly["o"].c, ly["gate_up"].c, ly["down"].c)
+        self.n, self.M, self.n_q = n, M, n_q
+        nb = ctypes.c_size_t()
+        _check(lib().w12_stream_workspace_size(self.arr, n, M, n_q, ctypes.byref(nb)), "w12_stream_workspace_size")
+        self.ws_bytes = int(nb.value)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=device)
+        offs = (ctypes.c_size_t * 4)()
+        _check(lib().w12_stream_buffers(self.arr, n, M, n_q, offs), "w12_stream_buffers")
+        self.offsets = [int(o) for o in offs]
+        self.hidden = layers[0]["qkv"].K
+        self.n_qkv = layers[0]["qkv"].N
+        self.ffn = layers[0]["down"].K
+
+    def __call__(self, h: torch.Tensor, x_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """Runs the step on fp32 h [M, hidden] (updated in place); returns x_out = rms_bf16(final h)."""
+        if h.dtype != torch.float32 or not h.is_contiguous() or tuple(h.shape) != (self.M, self.hidden):
+            raise ValueError(f"h must be a contiguous fp32 tensor of shape ({self.M}, {self.hidden})")
+        if x_out is None:
+            x_out = torch.empty((self.M, self.hidden), dtype=torch.bfloat16, device=h.device)
+        _check_out(x_out, self.M, self.hidden, (torch.bfloat16,))
+        _check(lib().w12_stream_step(self.arr, self.n, self.M, self.n_q, _ptr(h), _ptr(x_out), _ptr(self.ws),
+                                     self.ws_bytes, _stream(stream)), "w12_stream_step")
+        return x_out
+
+    def buffers(self) -> dict:
+        """Views of the last layer's intermediates in the workspace (valid after a step): x, qkv,
+        x2 (bf16 [M, hidden], [M, n_qkv], [M, hidden]) and p (bf16 [M, ffn])."""
+        M = self.M
+
+        def view(off, cols):
+            return self.ws[off: off + 2 * M * cols].view(torch.bfloat16).view(M, cols)
+
+        return {"x": view(self.offsets[0], self.hidden), "qkv": view(self.offsets[1], self.n_qkv),
+                "x2": view(self.offsets[2], self.hidden), "p": view(self.offsets[3], self.ffn)}
+
+    def check(self, stream=None) -> None:
+        """Synchronise and raise if the step's kernel gave up a bounded wait."""
+        _check(lib().w12_check(_ptr(self.ws), self.ws_bytes, _stream(stream)), "w12_check")
