@@ -250,7 +250,7 @@ def main():
                          "finishes; weights are static); plain: ordinary stream-ordered launches")
     ap.add_argument("--profile-gemm", type=int, default=0, metavar="M",
                     help="only run `--steps` W12 GEMM launches at M rows on the projection (for ncu)")
-    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax", "certified", "q6"])
+    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax", "certified", "q6", "stream"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -445,6 +445,8 @@ def profile_gemm(args):
     build.build()
     dev = torch.device("cuda", 0)
     M = args.profile_gemm
+    if args.profile_op == "stream":
+        return profile_stream(args, dev, M)
     head = args.profile_op in ("argmax", "certified")
     N = VOCAB if head else N_MLP
     rec = synth.HEAD if head else synth.PROJ
@@ -475,6 +477,37 @@ def profile_gemm(args):
     w12.check(t)
     print(json.dumps({"op": args.profile_op, "M": M, "N": N, "K": K_HID, "launch_us_median": statistics.median(ts),
                       "bytes": t.gemm_bytes(args.profile_op == "qview")}))
+
+
+def profile_stream(args, dev, M, n_layers=2):
+    """A few persistent layer-stream steps over `n_layers` layers of the 64-layer model's shapes
+    (the command under ncu for w12_stream_kernel); prints the median step time."""
+    from lossless_bit_weight_gb300 import w12
+
+    layers = []
+    for layer in range(n_layers):
+        ws = {name: synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device=dev)
+              for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS)}
+        layers.append({"qkv": w12.encode(torch.cat([ws["q"], ws["k"], ws["v"]])), "o": w12.encode(ws["o"]),
+                       "gate_up": w12.encode(w12.stream_interleave(ws["gate"], ws["up"])),
+                       "down": w12.encode(ws["down"])})
+        del ws
+    step = w12.StreamStep(layers, M, 6144)
+    h0 = synth.activations(M, K_HID, seed=synth.seed_for(3, M), device=dev).float()
+    h = torch.empty_like(h0)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        h.copy_(h0)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        step(h)
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            ts.append(a.elapsed_time(b) * 1e3)
+    step.check()
+    print(json.dumps({"op": "stream", "M": M, "layers": n_layers, "step_us_median": statistics.median(ts),
+                      "w12_bytes": sum(sum(t.gemm_bytes() for t in ly.values()) for ly in layers)}))
 
 
 def _time(fn, reps=20, warm=3):

@@ -154,3 +154,27 @@ def test_binding_fails_loudly_without_the_library(w12, monkeypatch):
     monkeypatch.setattr(w12, "LIB_PATH", os.path.join(ROOT, "no_such_dir", "libw12.so"))
     with pytest.raises(RuntimeError, match="not built"):
         w12.lib()
+
+
+def test_stream_argument_checks(w12):
+    """The persistent layer-stream calls reject null pointers, layer counts, row counts and shapes
+    they do not take on the host, before any device work."""
+    L = w12.lib()
+    P = ctypes.c_void_p
+    one = P(256)  # never dereferenced: every call below fails its argument check first
+    nb = ctypes.c_size_t()
+    offs = (ctypes.c_size_t * 4)()
+    arr = (w12.CStreamLayer * 2)()  # zeroed descriptors: no buffers
+    assert L.w12_stream_workspace_size(None, 1, 8, 192, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_workspace_size(arr, 0, 8, 192, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_workspace_size(arr, w12.STREAM_MAX_LAYERS + 1, 8, 192, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_workspace_size(arr, 1, 0, 192, ctypes.byref(nb)) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_stream_workspace_size(arr, 1, w12.STREAM_MAX_M + 1, 192, ctypes.byref(nb)) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_stream_workspace_size(arr, 1, 8, 192, ctypes.byref(nb)) == w12.ERR_INVALID_ARG  # no buffers
+    assert L.w12_stream_workspace_size(arr, 1, 8, 192, None) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_buffers(arr, 1, 8, 192, None) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_buffers(arr, 1, 8, 192, offs) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_step(arr, 1, 8, 192, None, one, one, 1 << 20, None) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_step(arr, 1, 8, 192, one, one, P(258), 1 << 20, None) == w12.ERR_INVALID_ARG  # misaligned
+    assert L.w12_stream_interleave(None, one, 128, 64, one, None) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_interleave(one, one, 100, 64, one, None) == w12.ERR_UNSUPPORTED_SHAPE
