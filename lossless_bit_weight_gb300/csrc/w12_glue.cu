@@ -26,8 +26,9 @@ constexpr int kMulThreads = 256;
 //      (hi, lo) with error-free transformations (the exact square as p + e from an FMA; two-sum
 //      additions), across the block in a fixed order: about 2^-40 relative accuracy;
 //   3. the mean's reciprocal square root starts from the fp32 approximation and takes one Newton
-//      step in fp64 (about 2^-43), then the scaling by 2^-e is undone exactly;
-//   4. each of the thread's four columns is multiplied by it in fp64 and rounded once to bf16.
+//      step in fp64 (about 2^-43), kept as an fp32 pair;
+//   4. each of the thread's four columns, scaled by 2^-e (exact), is multiplied by it and rounded
+//      once to bf16 (fp32 arithmetic; fp64 only for results near the bottom of the fp32 range).
 // The result is the bf16 rounding of h / rms(h) except where that quotient lies within about
 // 2^-40 (relative) of a rounding boundary. An all-zero row gives zeros. K % 4 == 0, h finite and
 // 16-byte aligned.
@@ -44,7 +45,7 @@ __global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__re
     const int nround = (K4 + kRmsThreads * kRmsRound - 1) / (kRmsThreads * kRmsRound);
     __shared__ float wmax[kRmsThreads / 32];
     __shared__ F2 wsum[kRmsThreads / 32];
-    __shared__ double inv_s;
+    __shared__ RmsScale scale;
     float4 mine = make_float4(0.f, 0.f, 0.f, 0.f);  // columns 4 (256 c + tid) .. +3
     // pass 1: the largest |h| of the row (rows longer than one round are read again in pass 2)
     float amax = 0.f;
@@ -88,7 +89,8 @@ __global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__re
         }
 #pragma unroll
         for (int j = 0; j < kRmsRound; ++j) {
-            const float q[4] = {ldexpf(v[j].x, -e), ldexpf(v[j].y, -e), ldexpf(v[j].z, -e), ldexpf(v[j].w, -e)};
+            const float q[4] = {scale_pow2(v[j].x, -e), scale_pow2(v[j].y, -e), scale_pow2(v[j].z, -e),
+                                scale_pow2(v[j].w, -e)};
 #pragma unroll
             for (int t = 0; t < 4; ++t) {
                 const float p = __fmul_rn(q[t], q[t]);
@@ -104,19 +106,16 @@ __global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__re
     if (tid == 0) {
         F2 t = wsum[0];
         for (int i = 1; i < kRmsThreads / 32; ++i) t = f2_add(t, wsum[i]);
-        const double mean = (static_cast<double>(t.hi) + static_cast<double>(t.lo)) * inv_k;
-        const double y0 = static_cast<double>(rsqrtf(static_cast<float>(mean)));
-        const double y1 = y0 * fma(-0.5 * mean * y0, y0, 1.5);  // one Newton step for 1 / sqrt(mean)
-        inv_s = ldexp(y1, -e);  // exact: undo the scaling of h
+        scale = rms_scale(t, inv_k);
     }
     __syncthreads();
     if (col < K) {
-        const double q = inv_s;
+        const float yh = scale.yh, yl = scale.yl;
         uint2 out;
-        out.x = static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.x) * q)) |
-                (static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.y) * q)) << 16);
-        out.y = static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.z) * q)) |
-                (static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(mine.w) * q)) << 16);
+        out.x = static_cast<uint32_t>(bf16_mul_rne(scale_pow2(mine.x, -e), yh, yl)) |
+                (static_cast<uint32_t>(bf16_mul_rne(scale_pow2(mine.y, -e), yh, yl)) << 16);
+        out.y = static_cast<uint32_t>(bf16_mul_rne(scale_pow2(mine.z, -e), yh, yl)) |
+                (static_cast<uint32_t>(bf16_mul_rne(scale_pow2(mine.w, -e), yh, yl)) << 16);
         *reinterpret_cast<uint2 *>(xr + col) = out;
     }
 }

@@ -600,6 +600,38 @@ __device__ __forceinline__ uint16_t bf16_bits_rne(double v) {
     return sign | static_cast<uint16_t>((e << 7) | static_cast<int>(r & 0x7Fu));
 }
 
+// v * 2^s exactly (up to the final rounding of a subnormal result, as ldexpf): one multiply when
+// 2^s is a normal fp32 value
+__device__ __forceinline__ float scale_pow2(float v, int s) {
+    if (s >= -126 && s <= 127) return __fmul_rn(v, __uint_as_float(static_cast<uint32_t>(127 + s) << 23));
+    return ldexpf(v, s);
+}
+
+// bf16 bits of w * y, nearest even, for y = yh + yl (|yl| <= ulp(yh) / 2) and w fp32, without fp64
+// in the common case. p = fl(w yh) is within 1.5 fp32 ulps of w y (the product's rounding error
+// plus w yl), so unless p lies within one ulp of the midpoint between its two bf16 neighbours,
+// p rounds like w y. Near the midpoint m, the sign of (p - m) + (w yh - p) + w yl decides (p - m
+// is exact; the product error comes from an FMA). Results near or below the fp32 normal range,
+// and non-finite ones, take the fp64 route.
+__device__ __forceinline__ uint16_t bf16_mul_rne(float w, float yh, float yl) {
+    const float p = __fmul_rn(w, yh);
+    const uint32_t bits = __float_as_uint(p);
+    const uint32_t mag = bits & 0x7FFFFFFFu;
+    if (mag < 0x04000000u || mag >= 0x7F000000u)  // |p| < 2^-119, or at least 2^127 (Inf, NaN)
+        return bf16_bits_rne(static_cast<double>(w) * (static_cast<double>(yh) + static_cast<double>(yl)));
+    const uint32_t lo16 = bits & 0xFFFFu;
+    if (lo16 - 0x7FFFu > 2u)  // not within one ulp of the midpoint
+        return static_cast<uint16_t>((bits + 0x7FFFu + ((bits >> 16) & 1u)) >> 16);
+    const float m = __uint_as_float((bits & 0xFFFF0000u) | 0x8000u);
+    const float t = __fadd_rn(__fmaf_rn(w, yh, -p), __fmul_rn(w, yl));
+    float d = __fadd_rn(__fsub_rn(p, m), t);  // w y - m, its sign exact but for a cancellation below 2^-149
+    if (bits >> 31) d = -d;                   // in magnitude
+    const uint32_t down = bits >> 16;         // the neighbour toward zero
+    if (d > 0.f) return static_cast<uint16_t>(down + 1u);
+    if (d < 0.f) return static_cast<uint16_t>(down);
+    return static_cast<uint16_t>(down + (down & 1u));  // on the midpoint: the even neighbour
+}
+
 struct F2 {  // an unevaluated sum hi + lo of two fp32 values
     float hi, lo;
 };
@@ -611,6 +643,20 @@ __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
     const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), err);
     const float hi = __fadd_rn(s, lo);  // renormalise (|s| >= |lo|)
     return {hi, __fsub_rn(lo, __fsub_rn(hi, s))};
+}
+
+// 1 / rms of a row from the sum of squares of its values scaled by 2^-e (t, in fp32 pairs) and 1 / K:
+// the fp32 reciprocal square root of the mean and one Newton step in fp64 (about 2^-43), split
+// into an fp32 pair (yh, yl). The row's x = bf16(h / rms(h)) is then bf16_mul_rne(h * 2^-e, yh, yl).
+struct RmsScale {
+    float yh, yl;
+};
+__device__ __forceinline__ RmsScale rms_scale(F2 t, double inv_k) {
+    const double mean = (static_cast<double>(t.hi) + static_cast<double>(t.lo)) * inv_k;
+    const double y0 = static_cast<double>(rsqrtf(static_cast<float>(mean)));
+    const double y1 = y0 * fma(-0.5 * mean * y0, y0, 1.5);
+    const float yh = __double2float_rn(y1);
+    return {yh, __double2float_rn(y1 - static_cast<double>(yh))};
 }
 
 __device__ __forceinline__ uint32_t base2_of(int En) {

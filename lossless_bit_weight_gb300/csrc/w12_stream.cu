@@ -15,10 +15,11 @@
 // w12_mul_bf16, the accumulate mode), so the step gives the same rows as the chain of launches.
 //
 // Design on GB300: one block per SM (cooperative launch, so all blocks are resident), the warp
-// roles of the W12 GEMM kernel (copy producer, two MMA issuers, escape feeder, four epilogue
-// warps, three decode groups of four warps) and one ring of slots that runs through every GEMM of
-// the step. Weights are static, so the producer keeps fetching the records of the next GEMM into
-// free slots and the decode groups keep decoding them into tensor memory while the previous phase
+// roles of the W12 GEMM kernel (activation producer, two MMA issuers, a feeder of records and
+// escape words, four epilogue warps, three decode groups of four warps) and one ring of slots that
+// runs through every GEMM of the step. Weights are static, so the feeder keeps fetching the records
+// of the next GEMM into free slots and the decode groups keep decoding them into tensor memory
+// while the previous phase
 // is still finishing; only the activation copies of a GEMM wait, until every block has completed
 // the phase that writes them (a per-phase completion counter in global memory, polled with a
 // bounded wait). The epilogue warps write each GEMM's outputs (a tile split between blocks is
@@ -46,6 +47,7 @@ constexpr int kWProducer = 0, kWMma = 1, kWEscape = 2, kWMma2 = 3, kWEpi0 = 4, k
 constexpr int kEscCapS = 128;      // index words staged per slot; more -> read from global
 constexpr int kAColsS = 32;        // tensor-memory columns of one decoded record
 constexpr int kMaxStagesS = 8;
+constexpr int kRowF4 = 10;  // 16-byte words of a row one epilogue thread holds in a normalisation unit
 constexpr int kTmemColsS = 512;
 constexpr int kSmemLimitS = 232448;
 constexpr int kEpiBarS = 1;
@@ -76,11 +78,10 @@ struct SKind {  // shape and work split of one of the four linears (the same in 
 };
 
 struct SParams {
-    CUtensorMap xmap[kKinds];   // the activations of each kind: one 64-wide k slice
-    CUtensorMap xmap2[kKinds];  // two consecutive k slices in one copy
     STensor t[kMaxLayersS][kKinds];
     SKind kind[kKinds];
     int L, M, npad, stages, nacc, acc_cols, G, H, F, Nqkv, rms_chunks, sbytes;
+    double inv_h;  // 1 / H
     float *h;
     uint16_t *xa, *xm, *qkv, *pg, *x_out;
     float *partials;     // [2][G][2][M][128]
@@ -98,13 +99,14 @@ struct SCtrl {
     uint2 esc_info[kMaxStagesS];
     const uint32_t *esc_ptr[kMaxStagesS];  // the slot's index words in global memory (when not staged)
     int slot_nr[kMaxStagesS];              // records in the slot (1 or 2)
+    int slot_en1[kMaxStagesS];             // offset of the second record's window bases (0: same tile)
     int nslots;                            // slots in the block's whole sequence
     uint32_t tmem_base;
     int abort;
     int last;            // this block published a split tile's part last and sums it
     float red_max[4];    // the row normalisation's cross-warp reductions
     F2 red_sum[4];
-    double inv_s;
+    RmsScale scale;
 };
 constexpr size_t kSCtrlBytes = (sizeof(SCtrl) + 127) / 128 * 128;
 constexpr size_t kXchgBytes = 16 * 64 * 4;  // up-half values of 16 rows x 64 columns
@@ -195,7 +197,15 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_constant__ SParams p) {
+// The activations of each GEMM kind, as kernel parameters of their own (like the GEMM kernel's):
+// one 64-wide k slice (a*) and two consecutive slices in one copy (b*), for q|k|v, o, gate|up
+// and down.
+__global__ void __launch_bounds__(kThreadsS, 1)
+w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap b0,
+                  const __grid_constant__ CUtensorMap a1, const __grid_constant__ CUtensorMap b1,
+                  const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap b2,
+                  const __grid_constant__ CUtensorMap a3, const __grid_constant__ CUtensorMap b3,
+                  const __grid_constant__ SParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,7 +225,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
     if (warp == kWProducer) {
         if (lane == 0) {
             for (int s = 0; s < S; ++s) {
-                mbar_init(smem_u32(&ctrl->full[s]), 2);  // producer's records + escape feeder
+                mbar_init(smem_u32(&ctrl->full[s]), 1);  // the escape feeder's copies
                 mbar_init(smem_u32(&ctrl->afull[s]), 128);
                 mbar_init(smem_u32(&ctrl->empty[s]), 2);  // one arrival per MMA issuer
                 mbar_init(smem_u32(&ctrl->xfull[s]), 1);
@@ -234,10 +244,14 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
             }
             ctrl->nslots = ns;
             fence_barrier_init();
-            for (int k = 0; k < kKinds; ++k) {
-                prefetch_tensormap(&p.xmap[k]);
-                prefetch_tensormap(&p.xmap2[k]);
-            }
+            prefetch_tensormap(&a0);
+            prefetch_tensormap(&b0);
+            prefetch_tensormap(&a1);
+            prefetch_tensormap(&b1);
+            prefetch_tensormap(&a2);
+            prefetch_tensormap(&b2);
+            prefetch_tensormap(&a3);
+            prefetch_tensormap(&b3);
         }
         __syncwarp();
     }
@@ -250,7 +264,8 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
     const uint32_t tmem = ctrl->tmem_base;
     auto a_slot = [&](int s, int q) { return tmem + p.acc_cols + (s * 2 + q) * kAColsS; };
     volatile int *abort = &ctrl->abort;
-    int issued = 0, xissued = 0;  // producer: slots whose records / activations were requested
+    int issued = 0;   // escape feeder: slots whose records were requested
+    int xissued = 0;  // producer: slots whose activations were requested
     int mma_issued = 0;           // issuers: slots they issued MMAs for
 
     SlotIt start;
@@ -260,95 +275,51 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
 
     if (warp == kWProducer) {
         // ---------------------------------------------------------------- producer (warp-wide)
-        // Two cursors over the block's slots: records (weights) of a slot are requested as soon
-        // as its ring slot is free, activations once the phase that writes them has completed on
-        // every block. Records therefore run up to a ring's depth ahead of the activations, across
-        // GEMM boundaries.
-        SlotIt ri = start, xi = start;
-        RingS rr, xr;
+        // Activation tiles of each slot, in slot order: once the slot's ring position is free and
+        // the phase that writes the GEMM's input has completed on every block. The records of the
+        // slots go out from the escape feeder, which runs up to a ring's depth ahead of the
+        // activations, across GEMM boundaries. This loop stays short: the warp shares its
+        // scheduler with three decode warps, and every instruction here delays the next copy.
+        SlotIt xi = start;
+        RingS xr;
         int known = 0;  // phases [0, known) are known to be complete on every block
-        uint64_t t_idle = 0;
-        // what each cursor needs of its current GEMM phase, loaded once per phase (parameter
-        // reads with run-time indices are slow, and this loop runs once per slot)
+        // the current GEMM phase's constants, loaded once per phase (parameter reads with run-time
+        // indices are slow)
         int xgp = -1, xKT = 1, xkt = 0, xneed = 0;
         const CUtensorMap *xm1 = nullptr, *xm2 = nullptr;
-        int rgp = -1;
-        const uint8_t *rbase = nullptr;
         while (!xi.end(p)) {
-            bool did = false;
-            // activations of every slot whose records are requested, as soon as the phase that
-            // writes them has completed; in the steady state each slot's activation copy goes
-            // right behind its records, at a phase boundary the waiting ones go out together
-            while (xi.js < ri.js) {
-                if (xi.gp != xgp) {
-                    xgp = xi.gp;
-                    const int k = xgp & 3;
-                    xKT = p.kind[k].k_tiles;
-                    xkt = xi.r % xKT;
-                    xm1 = &p.xmap[k];
-                    xm2 = &p.xmap2[k];
-                    xneed = gemm_phase(xgp) - 1;  // the phase that writes this GEMM's input
-                }
-                if (xneed >= known) {
-                    uint32_t v = 0;
-                    if (lane == 0) v = ld_acquire_gpu(p.done + xneed);
-                    v = __shfl_sync(kAllOnes, v, 0);
-                    if (v < Gu) break;
-                    known = xneed + 1;
-                    fence_proxy_async_global();  // generic writes of other SMs before async reads
-                }
-                const uint32_t xb = smem_u32(&ctrl->xfull[xr.idx]);
-                mbar_arrive_expect_tx_elect(xb, static_cast<uint32_t>(xi.nr * xbytes));
-                if (xi.nr == 2 && xkt + 1 < xKT) {
-                    tma_3d_g2s_elect(smem_u32(stage_x(xr.idx, 0)), xm2, 0, 0, xkt, xb);
-                } else {
-                    tma_2d_g2s_elect(smem_u32(stage_x(xr.idx, 0)), xm1, xkt * kTileK, 0, xb);
-                    if (xi.nr == 2)
-                        tma_2d_g2s_elect(smem_u32(stage_x(xr.idx, 1)), xm1, ((xkt + 1) % xKT) * kTileK, 0, xb);
-                }
-                xkt += xi.nr;
-                while (xkt >= xKT) xkt -= xKT;
-                xi.next(p, c);
-                xr.advance(1, S);
-                xissued = xi.js;
-                did = true;
+            const bool okf = mbar_wait(smem_u32(&ctrl->empty[xr.idx]), xr.phase ^ 1u, abort, p.err, kErrProducer);
+            if (!__all_sync(kAllOnes, okf)) break;
+            if (xi.gp != xgp) {
+                xgp = xi.gp;
+                const int k = xgp & 3;
+                xKT = p.kind[k].k_tiles;
+                xkt = xi.r % xKT;
+                xm1 = (k == 0) ? &a0 : (k == 1) ? &a1 : (k == 2) ? &a2 : &a3;
+                xm2 = (k == 0) ? &b0 : (k == 1) ? &b1 : (k == 2) ? &b2 : &b3;
+                xneed = gemm_phase(xgp) - 1;  // the phase that writes this GEMM's input
             }
-            // records of the next slot as soon as its ring slot is free
-            if (!ri.end(p)) {
-                const bool free_slot = ri.js < S || mbar_test_wait(smem_u32(&ctrl->empty[rr.idx]), rr.phase ^ 1u);
-                if (__all_sync(kAllOnes, free_slot)) {
-                    if (ri.gp != rgp) {
-                        rgp = ri.gp;
-                        rbase = p.t[rgp >> 2][rgp & 3].records;
-                    }
-                    const uint32_t fb = smem_u32(&ctrl->full[rr.idx]);
-                    const uint32_t bytes = static_cast<uint32_t>(ri.nr) * kRecordBytes;
-                    mbar_arrive_expect_tx_elect(fb, bytes);
-                    bulk_g2s_elect(smem_u32(stage_rec(rr.idx, 0)), rbase + static_cast<size_t>(ri.r) * kRecordBytes, bytes,
-                                   fb);
-                    ri.next(p, c);
-                    rr.advance(1, S);
-                    issued = ri.js;
-                    continue;  // its activations next, if their input is complete
-                }
+            if (xneed >= known) {
+                bool okp = true;
+                if (lane == 0) okp = wait_count(p.done + xneed, Gu, abort, p.err, kErrProducer);
+                if (!__shfl_sync(kAllOnes, okp, 0)) break;
+                known = xneed + 1;
+                fence_proxy_async_global();  // generic writes of other SMs before async reads
             }
-            if (did) {
-                t_idle = 0;
+            const uint32_t xb = smem_u32(&ctrl->xfull[xr.idx]);
+            mbar_arrive_expect_tx_elect(xb, static_cast<uint32_t>(xi.nr * xbytes));
+            if (xi.nr == 2 && xkt + 1 < xKT) {
+                tma_3d_g2s_elect(smem_u32(stage_x(xr.idx, 0)), xm2, 0, 0, xkt, xb);
             } else {
-                if (*abort) break;
-                const uint64_t now = global_timer_ns();
-                if (t_idle == 0) {
-                    t_idle = now;
-                } else if (now - t_idle > kWaitLimitNs) {
-                    if (lane == 0) {
-                        *abort = 1;
-                        atomicOr(p.err, kErrProducer);
-                    }
-                    __syncwarp();
-                    break;
-                }
-                __nanosleep(64);
+                tma_2d_g2s_elect(smem_u32(stage_x(xr.idx, 0)), xm1, xkt * kTileK, 0, xb);
+                if (xi.nr == 2)
+                    tma_2d_g2s_elect(smem_u32(stage_x(xr.idx, 1)), xm1, ((xkt + 1) % xKT) * kTileK, 0, xb);
             }
+            xkt += xi.nr;
+            while (xkt >= xKT) xkt -= xKT;
+            xi.next(p, c);
+            xr.advance(1, S);
+            xissued = xi.js;
         }
     } else if (warp == kWMma || warp == kWMma2) {
         // ---------------------------------------------------------------- MMA issuers (warp-wide)
@@ -422,18 +393,19 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
             js_base += nslots;
         }
     } else if (warp == kWEscape) {
-        // ---------------------------------------------------------------- escape feeder (warp-wide)
-        // Per slot: the summary of the slot's index words (how many, how many belong to its first
-        // record, where they start) for the decode groups, and one bulk copy of the words next to
-        // the records. Lane l holds rec_esc_off[wbase + l] (cur) and [wbase + 32 + l] (nxt) of the
+        // ------------------------------------------------- record and escape feeder (warp-wide)
+        // Per slot, as soon as its ring position is free: the summary of the slot's index words
+        // (how many, how many belong to its first record, where they start) for the decode groups,
+        // and the bulk copies of the slot's records, of its index words and of its window bases,
+        // all counted on the slot's full barrier. Lane l holds rec_esc_off[wbase + l] (cur) and [wbase + 32 + l] (nxt) of the
         // current phase's tensor, so the offsets are loaded 32 at a time, ahead of use.
         SlotIt it = start;
         RingS st;
         int wgp = -1, wbase = 0;
         uint32_t cur = 0, nxt = 0;
         const uint32_t *offs = nullptr, *words = nullptr;
-        const uint8_t *bases = nullptr;
-        int R = 0, KT = 1;
+        const uint8_t *bases = nullptr, *recs = nullptr;
+        int R = 0, KT = 1, ftile = 0, fkt = 0;  // tile and k tile of the slot's first record
         auto load_off = [&](int i) -> uint32_t { return (i <= R) ? __ldg(offs + i) : 0u; };
         while (!it.end(p)) {
             if (it.gp != wgp) {  // the phase's buffers, loaded once per phase
@@ -442,11 +414,14 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
                 offs = T.rec_esc_off;
                 words = T.rec_esc;
                 bases = T.base_exp;
+                recs = T.records;
                 R = p.kind[wgp & 3].R;
                 KT = p.kind[wgp & 3].k_tiles;
                 wbase = it.r;
                 cur = load_off(wbase + lane);
                 nxt = load_off(wbase + 32 + lane);
+                ftile = it.r / KT;
+                fkt = it.r - ftile * KT;
             }
             while (it.r + it.nr >= wbase + 64) {
                 wbase += 32;
@@ -460,7 +435,8 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
                 return dd < 32 ? a : b2;
             };
             const uint32_t lo = off_of(it.r), mid = off_of(it.r + 1), hi = off_of(it.r + it.nr);
-            const int tile0 = it.r / KT, tile1 = (it.r + it.nr - 1) / KT;
+            const int tile0 = ftile;
+            const bool new_tile = it.nr == 2 && fkt + 1 == KT;  // the second record starts the next tile
             const int s = st.idx;
             const bool ok = mbar_wait(smem_u32(&ctrl->empty[s]), st.phase ^ 1, abort, p.err, kErrEscape);
             if (!__all_sync(kAllOnes, ok)) break;
@@ -472,17 +448,26 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
                                                (it.nr == 2) ? mid - lo : cnt);
                 ctrl->esc_ptr[s] = words + lo;
                 ctrl->slot_nr[s] = it.nr;
+                ctrl->slot_en1[s] = new_tile ? kTileN : 0;
             }
             __syncwarp();
-            // the slot's escape words (when they fit) and the window bases of its records' tiles
-            const uint32_t en_bytes = static_cast<uint32_t>(it.nr) * kTileN;
-            mbar_arrive_expect_tx_elect(fb, (staged ? cnt * 4 : 0u) + en_bytes);
+            // the slot's records, its escape words (when they fit) and the window bases of its
+            // records' tiles
+            const uint32_t en_bytes = new_tile ? 2u * kTileN : kTileN;
+            const uint32_t rbytes = static_cast<uint32_t>(it.nr) * kRecordBytes;
+            mbar_arrive_expect_tx_elect(fb, rbytes + (staged ? cnt * 4 : 0u) + en_bytes);
+            bulk_g2s_elect(smem_u32(stage_rec(s, 0)), recs + static_cast<size_t>(it.r) * kRecordBytes, rbytes, fb);
             if (staged) bulk_g2s_elect(smem_u32(stage_esc(s)), words + lo, cnt * 4, fb);
-            bulk_g2s_elect(smem_u32(stage_en(s)), bases + static_cast<size_t>(tile0) * kTileN, kTileN, fb);
-            if (it.nr == 2)
-                bulk_g2s_elect(smem_u32(stage_en(s)) + kTileN, bases + static_cast<size_t>(tile1) * kTileN, kTileN, fb);
+            bulk_g2s_elect(smem_u32(stage_en(s)), bases + static_cast<size_t>(tile0) * kTileN, new_tile ? 2u * kTileN : kTileN,
+                           fb);
+            fkt += it.nr;
+            while (fkt >= KT) {
+                fkt -= KT;
+                ++ftile;
+            }
             it.next(p, c);
             st.advance(1, S);
+            issued = it.js;
         }
     } else if (warp >= kWDec0) {
         // ---------------------------------------------------------------- decode groups
@@ -549,7 +534,7 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
             tc_fence_after();
             tmem_st_32x32b_x32(a_slot(s, 0) + lanes, wa);
             if (nr == 2) {
-                decode_record(s, 1, base2_of(en[kTileN + nl]), wb);
+                decode_record(s, 1, base2_of(en[ctrl->slot_en1[s] + nl]), wb);
                 tmem_st_32x32b_x32(a_slot(s, 1) + lanes, wb);
             }
             tmem_wait_st();
@@ -593,6 +578,74 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
             const int H = p.H, H4 = H >> 2;
             const int C = p.rms_chunks;
             const int Q4 = (H4 + C - 1) / C;
+            if (H4 <= 128 * kRowF4) {
+                // The row fits in the unit (thread et holds float4 et + 128 t, the array in local
+                // memory): one round of loads, then the same arithmetic in the same order as the
+                // passes below, in rolled loops. The phase runs once per layer from a cold
+                // instruction cache, and unrolled it took longer to fetch than to execute.
+                for (int u = c; !dead && u < M * C; u += G) {
+                    const int m = u / C, ch = u % C;
+                    const float4 *h4 = reinterpret_cast<const float4 *>(p.h + static_cast<size_t>(m) * H);
+                    float4 v[kRowF4];
+#pragma unroll
+                    for (int t = 0; t < kRowF4; ++t)
+                        v[t] = (et + 128 * t < H4) ? __ldcg(h4 + et + 128 * t) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float amax = 0.f;
+#pragma unroll 1
+                    for (int t = 0; t < kRowF4; ++t)
+                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v[t].x), fabsf(v[t].y)), fmaxf(fabsf(v[t].z), fabsf(v[t].w))));
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kAllOnes, amax, off));
+                    if (lane == 0) ctrl->red_max[qw] = amax;
+                    named_bar_sync(kEpiBarS, 128);
+                    const float bmax = fmaxf(fmaxf(ctrl->red_max[0], ctrl->red_max[1]), fmaxf(ctrl->red_max[2], ctrl->red_max[3]));
+                    uint16_t *xr = x + static_cast<size_t>(m) * H;
+                    const int i_lo = ch * Q4, i_hi = min((ch + 1) * Q4, H4);
+                    if (bmax == 0.f) {  // an all-zero row
+                        for (int i = i_lo + et; i < i_hi; i += 128) __stcg(reinterpret_cast<uint2 *>(xr) + i, make_uint2(0u, 0u));
+                        named_bar_sync(kEpiBarS, 128);
+                        continue;
+                    }
+                    const int e = ilogbf(bmax) + 1;  // |h| * 2^-e < 1
+                    F2 acc = {0.f, 0.f};
+#pragma unroll 1
+                    for (int t = 0; t < kRowF4; ++t) {
+                        const float q[4] = {scale_pow2(v[t].x, -e), scale_pow2(v[t].y, -e), scale_pow2(v[t].z, -e),
+                                            scale_pow2(v[t].w, -e)};
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const float pp = __fmul_rn(q[j], q[j]);
+                            acc = f2_add(acc, F2{pp, __fmaf_rn(q[j], q[j], -pp)});
+                        }
+                    }
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1)
+                        acc = f2_add(acc, F2{__shfl_xor_sync(kAllOnes, acc.hi, off), __shfl_xor_sync(kAllOnes, acc.lo, off)});
+                    if (lane == 0) ctrl->red_sum[qw] = acc;
+                    named_bar_sync(kEpiBarS, 128);
+                    if (et == 0) {
+                        F2 tt = ctrl->red_sum[0];
+                        for (int i = 1; i < 4; ++i) tt = f2_add(tt, ctrl->red_sum[i]);
+                        ctrl->scale = rms_scale(tt, p.inv_h);
+                    }
+                    named_bar_sync(kEpiBarS, 128);
+                    const float yh = ctrl->scale.yh, yl = ctrl->scale.yl;
+#pragma unroll 1
+                    for (int t = 0; t < kRowF4; ++t) {
+                        const int i = et + 128 * t;
+                        if (i >= i_lo && i < i_hi) {
+                            uint2 out;
+                            out.x = static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[t].x, -e), yh, yl)) |
+                                    (static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[t].y, -e), yh, yl)) << 16);
+                            out.y = static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[t].z, -e), yh, yl)) |
+                                    (static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[t].w, -e), yh, yl)) << 16);
+                            __stcg(reinterpret_cast<uint2 *>(xr) + i, out);
+                        }
+                    }
+                    named_bar_sync(kEpiBarS, 128);  // ctrl's scratch is free for the next unit
+                }
+                return;
+            }
             for (int u = c; !dead && u < M * C; u += G) {
                 const int m = u / C, ch = u % C;
                 const float4 *h4 = reinterpret_cast<const float4 *>(p.h + static_cast<size_t>(m) * H);
@@ -629,7 +682,8 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
                         v[j] = (base + 128 * j < H4) ? __ldcg(h4 + base + 128 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                     for (int j = 0; j < kRF; ++j) {
-                        const float q[4] = {ldexpf(v[j].x, -e), ldexpf(v[j].y, -e), ldexpf(v[j].z, -e), ldexpf(v[j].w, -e)};
+                        const float q[4] = {scale_pow2(v[j].x, -e), scale_pow2(v[j].y, -e), scale_pow2(v[j].z, -e),
+                                            scale_pow2(v[j].w, -e)};
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
                             const float pp = __fmul_rn(q[t], q[t]);
@@ -645,13 +699,10 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
                 if (et == 0) {
                     F2 t = ctrl->red_sum[0];
                     for (int i = 1; i < 4; ++i) t = f2_add(t, ctrl->red_sum[i]);
-                    const double mean = (static_cast<double>(t.hi) + static_cast<double>(t.lo)) / static_cast<double>(H);
-                    const double y0 = static_cast<double>(rsqrtf(static_cast<float>(mean)));
-                    const double y1 = y0 * fma(-0.5 * mean * y0, y0, 1.5);  // one Newton step for 1 / sqrt(mean)
-                    ctrl->inv_s = ldexp(y1, -e);
+                    ctrl->scale = rms_scale(t, p.inv_h);
                 }
                 named_bar_sync(kEpiBarS, 128);
-                const double q = ctrl->inv_s;
+                const float yh = ctrl->scale.yh, yl = ctrl->scale.yl;
                 for (int base = i_lo + et; base < i_hi; base += 128 * kRF) {
                     float4 v[kRF];
 #pragma unroll
@@ -661,10 +712,10 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
                     for (int j = 0; j < kRF; ++j) {
                         if (base + 128 * j < i_hi) {
                             uint2 out;
-                            out.x = static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(v[j].x) * q)) |
-                                    (static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(v[j].y) * q)) << 16);
-                            out.y = static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(v[j].z) * q)) |
-                                    (static_cast<uint32_t>(bf16_bits_rne(static_cast<double>(v[j].w) * q)) << 16);
+                            out.x = static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[j].x, -e), yh, yl)) |
+                                    (static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[j].y, -e), yh, yl)) << 16);
+                            out.y = static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[j].z, -e), yh, yl)) |
+                                    (static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[j].w, -e), yh, yl)) << 16);
                             __stcg(reinterpret_cast<uint2 *>(xr) + base + 128 * j, out);
                         }
                     }
@@ -845,10 +896,12 @@ __global__ void __launch_bounds__(kThreadsS, 1) w12_stream_kernel(const __grid_c
 
     // ---------------------------------------------------------------- teardown
     __syncthreads();
-    if (warp == kWProducer && lane == 0 && ctrl->abort) {
-        // let copies still in flight land before the block's shared memory is released
+    // after an abort, let copies still in flight land before the block's shared memory is released
+    if (warp == kWEscape && lane == 0 && ctrl->abort) {
         for (int js = (issued > S ? issued - S : 0); js < issued; ++js)
             if (!mbar_wait_drain(smem_u32(&ctrl->full[js % S]), (js / S) & 1)) atomicOr(p.err, kErrDrain);
+    }
+    if (warp == kWProducer && lane == 0 && ctrl->abort) {
         for (int js = (xissued > S ? xissued - S : 0); js < xissued; ++js)
             if (!mbar_wait_drain(smem_u32(&ctrl->xfull[js % S]), (js / S) & 1)) atomicOr(p.err, kErrDrain);
     }
@@ -1039,6 +1092,7 @@ extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_laye
     p.F = P.F;
     p.Nqkv = P.Nqkv;
     p.rms_chunks = P.rms_chunks;
+    p.inv_h = 1.0 / static_cast<double>(P.H);
     p.sbytes = P.sbytes;
     p.h = h;
     p.xa = reinterpret_cast<uint16_t *>(ws + P.off_xa);
@@ -1062,10 +1116,11 @@ extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_laye
     w12_status st = W12_OK;
     // the activations each kind reads: x (normalised rows), the q columns of q|k|v in place, the
     // normalised MLP input, the gate-up product
-    if (st == W12_OK) st = x_maps(p.xa, P.H, P.H, M, P.npad, &p.xmap[kKindQkv], &p.xmap2[kKindQkv]);
-    if (st == W12_OK) st = x_maps(p.qkv, P.nq, P.Nqkv, M, P.npad, &p.xmap[kKindO], &p.xmap2[kKindO]);
-    if (st == W12_OK) st = x_maps(p.xm, P.H, P.H, M, P.npad, &p.xmap[kKindGu], &p.xmap2[kKindGu]);
-    if (st == W12_OK) st = x_maps(p.pg, P.F, P.F, M, P.npad, &p.xmap[kKindDown], &p.xmap2[kKindDown]);
+    CUtensorMap xm[kKinds], xm2[kKinds];
+    if (st == W12_OK) st = x_maps(p.xa, P.H, P.H, M, P.npad, &xm[kKindQkv], &xm2[kKindQkv]);
+    if (st == W12_OK) st = x_maps(p.qkv, P.nq, P.Nqkv, M, P.npad, &xm[kKindO], &xm2[kKindO]);
+    if (st == W12_OK) st = x_maps(p.xm, P.H, P.H, M, P.npad, &xm[kKindGu], &xm2[kKindGu]);
+    if (st == W12_OK) st = x_maps(p.pg, P.F, P.F, M, P.npad, &xm[kKindDown], &xm2[kKindDown]);
     if (st == W12_OK) {
         static std::atomic<uint64_t> smem_set{0};
         int dev = 0;
@@ -1090,7 +1145,9 @@ extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_laye
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, w12_stream_kernel, p) != cudaSuccess) st = W12_ERR_CUDA;
+        if (cudaLaunchKernelEx(&cfg, w12_stream_kernel, xm[0], xm2[0], xm[1], xm2[1], xm[2], xm2[2], xm[3], xm2[3], p) !=
+            cudaSuccess)
+            st = W12_ERR_CUDA;
     }
     delete sp;
     return st;
