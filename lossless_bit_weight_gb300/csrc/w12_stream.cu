@@ -569,6 +569,7 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                 if (ph == kPhasesPerLayer * L && old == Gu - 1) {
                     // every block has passed every wait of this launch: leave the counters zeroed
                     for (int i = 0; i <= kPhasesPerLayer * L; ++i) p.done[i] = 0;
+                    for (int i = 0; i < kKinds * p.max_tiles; ++i) p.tile_cnt[i] = 0;
                 }
             }
         };
@@ -777,6 +778,8 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                 const int sl = (bstart(cc) / KT == tile) ? 0 : 1;
                 return part_base + (static_cast<size_t>(cc) * 2 + sl) * M * kTileN;
             };
+            // split tiles of this phase whose sum this block shares (its first and last segment)
+            int split_tile[2], split_lo[2], split_hi[2], nsplit = 0;
             for (int seg_start = r0; seg_start < r1; ++jseg) {
                 const int tile = seg_start / KT;
                 const int seg_end = min(r1, (tile + 1) * KT);
@@ -795,6 +798,7 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                     const uint32_t ln = static_cast<uint32_t>(32 * qw) << 16;
                     const uint32_t t0 = tmem + ln + (0 * p.nacc + b) * p.npad;
                     const uint32_t t1 = tmem + ln + (1 * p.nacc + b) * p.npad;
+#pragma unroll 1
                     for (int m0 = 0; m0 < M; m0 += 16) {
                         float f[16];
                         uint32_t v[16];
@@ -823,8 +827,18 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                     tc_fence_before();
                 }
                 mbar_arrive(smem_u32(&ctrl->accempty[b]));
-                if (!full && !dead) {
-                    // split tile: whichever block publishes its part last sums all parts in block order
+                if (!full && !dead && k != kKindGu) {
+                    // publish the part; the tile's sum is formed after the block's last segment
+                    __threadfence();
+                    named_bar_sync(kEpiBarS, 128);
+                    if (et == 0) atomicAdd(p.tile_cnt + k * p.max_tiles + tile, 1u);
+                    split_tile[nsplit] = tile;
+                    split_lo[nsplit] = c_lo;
+                    split_hi[nsplit] = c_hi;
+                    ++nsplit;
+                } else if (!full && !dead) {
+                    // gate|up split tile: whichever block publishes its part last sums all parts in
+                    // block order (the product needs both halves of every row of the tile)
                     __threadfence();
                     named_bar_sync(kEpiBarS, 128);
                     if (et == 0) {
@@ -834,32 +848,17 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                     named_bar_sync(kEpiBarS, 128);
                     if (ctrl->last) {
                         __threadfence();
-                        // the parts are summed in increasing block order; their loads go out two
-                        // parts by eight rows at a time
-                        constexpr int kPB = 2;
+#pragma unroll 1
                         for (int m0 = 0; m0 < M; m0 += 16) {
                             float f[16];
 #pragma unroll
                             for (int i = 0; i < 16; ++i) f[i] = 0.f;
-                            for (int cb = c_lo; cb <= c_hi; cb += kPB) {
+#pragma unroll 1
+                            for (int cb = c_lo; cb <= c_hi; ++cb) {
+                                const float *src = part_of(cb, tile);
 #pragma unroll
-                                for (int ih = 0; ih < 16; ih += 8) {
-                                    float v[kPB][8];
-#pragma unroll
-                                    for (int j = 0; j < kPB; ++j) {
-                                        const float *src = part_of(min(cb + j, c_hi), tile);
-#pragma unroll
-                                        for (int i = 0; i < 8; ++i)
-                                            v[j][i] = (cb + j <= c_hi && m0 + ih + i < M)
-                                                          ? __ldcg(src + static_cast<size_t>(m0 + ih + i) * kTileN + nl)
-                                                          : 0.f;
-                                    }
-#pragma unroll
-                                    for (int j = 0; j < kPB; ++j)
-#pragma unroll
-                                        for (int i = 0; i < 8; ++i)
-                                            if (cb + j <= c_hi) f[ih + i] += v[j][i];
-                                }
+                                for (int i = 0; i < 16; ++i)
+                                    if (m0 + i < M) f[i] += __ldcg(src + static_cast<size_t>(m0 + i) * kTileN + nl);
                             }
                             finalize(k, tile, m0, f);
                         }
@@ -868,6 +867,85 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                     named_bar_sync(kEpiBarS, 128);  // ctrl->last is read by every thread before it changes
                 }
                 seg_start = seg_end;
+            }
+            // Sums of the split tiles. Every block of a tile published its part above before it
+            // waits here, so the waits cannot form a cycle. Once all parts are in (the tile's
+            // counter grows by its block count in every layer), block c_lo + i sums the i-th of
+            // the tile's c_hi - c_lo + 1 slices of 16-byte groups (row m, columns 4j..4j+3) over the
+            // parts in increasing block order, the same additions in the same order as a single
+            // summing block, and writes them out.
+            const uint32_t layer1 = static_cast<uint32_t>((gp >> 2) + 1);
+#pragma unroll 1
+            for (int sidx = 0; sidx < nsplit && !dead; ++sidx) {
+                const int tile = split_tile[sidx], c_lo = split_lo[sidx], c_hi = split_hi[sidx];
+                const int np = c_hi - c_lo + 1;
+                bool okc = true;
+                if (et == 0) {
+                    okc = wait_count(p.tile_cnt + k * p.max_tiles + tile, layer1 * static_cast<uint32_t>(np), abort, p.err,
+                                     kErrEpilogue);
+                    __threadfence();
+                }
+                dead = named_bar_or(kEpiBarS, 128, !okc) || dead;
+                if (dead) break;
+                const int G4 = M * (kTileN / 4);
+                const int g_lo = (c - c_lo) * G4 / np, g_hi = (c - c_lo + 1) * G4 / np;
+                constexpr int kG = 2, kP = 4;  // groups per thread per round, parts per round of loads
+#pragma unroll 1
+                for (int g0 = g_lo + et; g0 < g_hi; g0 += 128 * kG) {
+                    float4 acc[kG], hv[kG];
+#pragma unroll
+                    for (int q = 0; q < kG; ++q) {
+                        acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const int g = g0 + 128 * q;
+                        const int m = g / (kTileN / 4), n = tile * kTileN + 4 * (g % (kTileN / 4));
+                        hv[q] = (k != kKindQkv && g < g_hi)
+                                    ? __ldcg(reinterpret_cast<const float4 *>(p.h + static_cast<size_t>(m) * p.H + n))
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+#pragma unroll 1
+                    for (int cb = c_lo; cb <= c_hi; cb += kP) {
+                        float4 v[kP][kG];
+#pragma unroll
+                        for (int j = 0; j < kP; ++j) {
+                            const float4 *src = reinterpret_cast<const float4 *>(part_of(min(cb + j, c_hi), tile));
+#pragma unroll
+                            for (int q = 0; q < kG; ++q)
+                                v[j][q] = (cb + j <= c_hi && g0 + 128 * q < g_hi) ? __ldcg(src + g0 + 128 * q)
+                                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+#pragma unroll
+                        for (int j = 0; j < kP; ++j) {
+                            if (cb + j > c_hi) break;
+#pragma unroll
+                            for (int q = 0; q < kG; ++q) {
+                                acc[q].x += v[j][q].x;
+                                acc[q].y += v[j][q].y;
+                                acc[q].z += v[j][q].z;
+                                acc[q].w += v[j][q].w;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < kG; ++q) {
+                        const int g = g0 + 128 * q;
+                        if (g >= g_hi) break;
+                        const int m = g / (kTileN / 4), n = tile * kTileN + 4 * (g % (kTileN / 4));
+                        if (n >= K.N) continue;
+                        if (k == kKindQkv) {
+                            uint2 o;
+                            o.x = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[q].x))) |
+                                  (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[q].y))) << 16);
+                            o.y = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[q].z))) |
+                                  (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(acc[q].w))) << 16);
+                            __stcg(reinterpret_cast<uint2 *>(reinterpret_cast<unsigned short *>(p.qkv) +
+                                                             static_cast<size_t>(m) * p.Nqkv + n), o);
+                        } else {  // o and down: one fp32 addition into h per element
+                            const float4 r = make_float4(hv[q].x + acc[q].x, hv[q].y + acc[q].y, hv[q].z + acc[q].z,
+                                                         hv[q].w + acc[q].w);
+                            __stcg(reinterpret_cast<float4 *>(p.h + static_cast<size_t>(m) * p.H + n), r);
+                        }
+                    }
+                }
             }
         };
         for (int l = 0; l < L && !dead; ++l) {
