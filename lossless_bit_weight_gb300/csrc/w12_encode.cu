@@ -9,13 +9,13 @@
 //
 // Passes (all HBM-streaming, integer only):
 //   window   one warp per channel: exponent histogram -> E_n, then the channel's escape count
-//            per k tile and each record's total
-//   rowscan  one warp per channel: exclusive prefix of its per-k-tile counts
+//            per k tile (as an exclusive prefix over its k tiles, and its total) and each
+//            record's total
 //   scan     two blocks in one launch: exclusive prefixes over channels and over records ->
 //            the offsets of both escape lists
 //   pack     one block per 128x64 record: planes and escape flags of 8192 weights; the record
 //            bytes, the per-record index and the per-channel list
-// w12_encode_sizes runs window, rowscan and scan; w12_encode reuses their results from the
+// w12_encode_sizes runs window and scan; w12_encode reuses their results from the
 // scratch and runs pack only.
 #include "w12_internal.cuh"
 
@@ -24,44 +24,45 @@ namespace {
 
 constexpr int kWindowWarps = 8;
 constexpr int kScanThreads = 1024;
-
-// planes of a real weight u under the window [lo_e, lo_e + 15] = [E_n - 15, E_n] (format rules 2
-// and 3), without branches. E_n lies in [16, 254], so the window holds normal exponents only: a
-// weight is inside iff its biased exponent lies in it, above it (larger, Inf, NaN: clamped to the
-// window top, E = 15, m_hi = 7, B = 15) or below it (smaller, zero, subnormal: E = m_hi = B = 0).
-__device__ __forceinline__ void planes(uint32_t u, int lo_e, uint32_t &view, uint32_t &lo, bool &esc) {
-    const int x = static_cast<int>((u >> 7) & 0xFFu) - lo_e;  // exponent offset in the window
-    const bool inside = static_cast<uint32_t>(x) <= 15u;
-    const uint32_t t = inside ? (u & 0x7Fu) : (x > 15 ? 0x7Fu : 0u);  // mantissa or its clamp
-    const uint32_t dc = static_cast<uint32_t>(min(max(x, 0), 15));
-    view = (dc << 4) | ((t >> 3) & 0xEu) | (u >> 15);
-    lo = t & 0xFu;
-    esc = !inside;
-}
+constexpr int kScanPer = 32;    // values per scan thread per tile
+constexpr int kWinBatch = 4;    // 16-byte loads in flight per lane in the window pass
+constexpr size_t kScanSmem = sizeof(uint32_t) * (kScanThreads * kScanPer + kScanThreads * kScanPer / 32);
 
 // One warp per channel: the exponent histogram -> E_n; then the channel's escape count per k
 // tile (the row read again, mostly from cache) into ct, and each count added to its record's
 // total (integer atomics, so the totals do not depend on the order).
 __global__ void __launch_bounds__(kWindowWarps * 32)
 window_kernel(const uint16_t *__restrict__ w, int N, int K, int k_tiles, uint8_t *__restrict__ base_exp,
-              uint32_t *__restrict__ ct, uint32_t *__restrict__ rec_cnt) {
-    __shared__ uint32_t hist[kWindowWarps][256];
+              uint32_t *__restrict__ ct, uint32_t *__restrict__ rec_cnt, uint32_t *__restrict__ chan_cnt) {
+    __shared__ __align__(1024) uint32_t hist[kWindowWarps][256];  // 1 KB per warp, 1 KB aligned
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n = blockIdx.x * kWindowWarps + warp;
     uint32_t *h = hist[warp];
     for (int i = lane; i < 256; i += 32) h[i] = 0;
     __syncwarp();
     if (n < N) {
+        // Both weights of a 32-bit word at once: (word >> 5) masked leaves 4 * exponent in each
+        // half, OR-ed with the histogram's shared-memory address in both halves; every exponent
+        // is counted (bins 0 and 255, zero/subnormal and Inf/NaN, are never read below).
+        const uint32_t hb = static_cast<uint32_t>(__cvta_generic_to_shared(h));
+        const uint32_t hb2 = hb | (hb << 16);  // 1 KB aligned, below 64 KB: OR adds 4 * exponent
         const uint4 *row = reinterpret_cast<const uint4 *>(w + static_cast<size_t>(n) * K);
         const int nvec = K / 8;
-        for (int i = lane; i < nvec; i += 32) {
-            const uint4 v = __ldg(row + i);
-            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        // kWinBatch 16-byte loads per lane go out together, then their counts
+        for (int i0 = lane; i0 < nvec; i0 += 32 * kWinBatch) {
+            uint4 v[kWinBatch];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t u = (wd[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-                const uint32_t e = (u >> 7) & 0xFFu;
-                if (e >= 1u && e <= 254u) atomicAdd(&h[e], 1u);
+            for (int b = 0; b < kWinBatch; ++b) v[b] = (i0 + 32 * b < nvec) ? __ldg(row + i0 + 32 * b) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int b = 0; b < kWinBatch; ++b) {
+                if (i0 + 32 * b >= nvec) break;
+                const uint32_t wd[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t a2 = ((wd[q] >> 5) & 0x03FC03FCu) | hb2;
+                    asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(a2 & 0xFFFFu) : "memory");
+                    asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(a2 >> 16) : "memory");
+                }
             }
         }
     }
@@ -91,31 +92,56 @@ window_kernel(const uint16_t *__restrict__ w, int N, int K, int k_tiles, uint8_t
     // escapes per k tile: lane l holds 16-byte piece i = l + 32 j (k = 8 i .. 8 i + 7), so the 8
     // lanes of each lane octet share one k tile (4 j + l / 8); a weight stays in the window iff
     // its biased exponent lies in [E_n - 15, E_n] (that range holds normal exponents only)
-    const uint32_t lo_e = static_cast<uint32_t>(best_E - 15);
+    const uint32_t lo2 = static_cast<uint32_t>(best_E - 15) * 0x00010001u;
     const uint4 *row = reinterpret_cast<const uint4 *>(w + static_cast<size_t>(n) * K);
     const int nvec = K / 8;
     const int nt = n / kTileN;
-    for (int j0 = 0; j0 < 8 * k_tiles; j0 += 32) {
-        const int i = j0 + lane;
-        uint32_t c = 0;
-        if (n < N && i < nvec) {
-            const uint4 v = __ldg(row + i);
-            const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+    // kWinBatch chunks of 32 pieces (4 k tiles each) per round of loads; the counts become this
+    // channel's exclusive prefix over its k tiles (ct) and its total (chan_cnt) on the way
+    uint32_t run = 0;  // escapes of this channel in earlier k tiles
+    for (int j00 = 0; j00 < 8 * k_tiles; j00 += 32 * kWinBatch) {
+        uint4 v[kWinBatch];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t e = (wd[q >> 1] >> (16 * (q & 1) + 7)) & 0xFFu;
-                c += (e - lo_e > 15u) ? 1u : 0u;
-            }
+        for (int b = 0; b < kWinBatch; ++b) {
+            const int i = j00 + 32 * b + lane;
+            v[b] = (n < N && i < nvec) ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
         }
-        c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
-        c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
-        c += __shfl_xor_sync(0xFFFFFFFFu, c, 4);
-        const int kt = i >> 3;
-        if ((lane & 7) == 0 && kt < k_tiles) {
-            ct[static_cast<size_t>(n) * k_tiles + kt] = c;
-            if (c) atomicAdd(&rec_cnt[static_cast<size_t>(nt) * k_tiles + kt], c);
+#pragma unroll
+        for (int b = 0; b < kWinBatch; ++b) {
+            const int j0 = j00 + 32 * b;
+            if (j0 >= 8 * k_tiles) break;
+            const int i = j0 + lane;
+            uint32_t c = 0;
+            if (n < N && i < nvec) {
+                // two weights per word: D = E - lo_e + 256 per half (no borrow between halves);
+                // outside the window iff bits 4..8 of D differ from 10000b; the flags land in
+                // bits 9 and 25 and are summed as two 16-bit fields
+                const uint32_t wd[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+                uint32_t acc = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t D = ((wd[q] >> 7) & 0x00FF00FFu) + 0x01000100u - lo2;
+                    acc += (((D ^ 0x01000100u) & 0x01F001F0u) + 0x01F001F0u) & 0x02000200u;
+                }
+                c = ((acc >> 9) & 0xFFFFu) + (acc >> 25);
+            }
+            c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+            c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
+            c += __shfl_xor_sync(0xFFFFFFFFu, c, 4);
+            // the chunk's four k-tile counts (octets 0..3) and this octet's prefix among them
+            const uint32_t c0 = __shfl_sync(0xFFFFFFFFu, c, 0), c1 = __shfl_sync(0xFFFFFFFFu, c, 8);
+            const uint32_t c2 = __shfl_sync(0xFFFFFFFFu, c, 16), c3 = __shfl_sync(0xFFFFFFFFu, c, 24);
+            const int oct = lane >> 3;
+            const uint32_t before = run + (oct > 0 ? c0 : 0u) + (oct > 1 ? c1 : 0u) + (oct > 2 ? c2 : 0u);
+            const int kt = i >> 3;
+            if ((lane & 7) == 0 && kt < k_tiles) {
+                ct[static_cast<size_t>(n) * k_tiles + kt] = before;
+                if (c) atomicAdd(&rec_cnt[static_cast<size_t>(nt) * k_tiles + kt], c);
+            }
+            run += c0 + c1 + c2 + c3;
         }
     }
+    if (lane == 0) chan_cnt[n] = run;
 }
 
 struct PackArgs {
@@ -166,6 +192,11 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
     const int n = nt * kTileN + nl;
     const int k0 = kt * kTileK + 32 * half;
     const int En = a.base_exp[n];
+    // the offsets this thread needs after the block scan, requested now so their latency
+    // overlaps the weight loads and the encoding
+    const uint32_t rec_off_r = a.rec_off[r];
+    const uint32_t chan_off_n = (n < a.N) ? a.chan_off[n] : 0u;
+    const uint32_t ct_nk = (n < a.N) ? a.ct[static_cast<size_t>(n) * a.k_tiles + kt] : 0u;
 
     uint32_t u[16];  // 32 bf16 patterns, two per word, k ascending
 #pragma unroll
@@ -179,20 +210,43 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
         u[4 * g + 3] = v.w;
     }
 
-    uint32_t vw[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // view bytes, 4 per word
-    uint32_t bw[4] = {0, 0, 0, 0};              // B nibbles, 8 per word
-    uint32_t mask = 0;                          // escape flags, bit j <-> k0 + j
+    // Planes of a weight under the window [lo_e, lo_e + 15] = [E_n - 15, E_n] (format rules 2
+    // and 3): inside it, view byte = (E - lo_e) << 4 | m_hi << 1 | s and B = the low mantissa
+    // nibble. Two weights per 32-bit word at a time (weight 2p in the low half of u[p], 2p + 1
+    // in the high half), every weight first encoded as if inside the window; the escapes, rare,
+    // get their placeholder codes below. Per half: D = E - lo_e + 256 lies in [2, 510] (no
+    // borrow between the halves), the weight is inside iff D >> 4 == 16, and then its exponent
+    // code is D & 15.
+    const uint32_t lo2 = static_cast<uint32_t>(En - 15) * 0x00010001u;
+    uint32_t view16[16], lo16[16];
+    uint32_t mask = 0;  // escape flags, bit j <-> k0 + j
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-        const uint32_t bits = (u[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-        const bool real = (n < a.N) && (k0 + j < a.K);
-        uint32_t view = 0, lo = 0;
-        bool esc = false;
-        if (real) planes(bits, En - 15, view, lo, esc);
-        vw[j >> 2] |= view << (8 * (j & 3));
-        const int i = j & 7;
-        bw[j >> 3] |= lo << (4 * ((i >> 1) + 4 * (i & 1)));
-        if (esc) mask |= 1u << j;
+    for (int q = 0; q < 16; ++q) {
+        const uint32_t w2 = u[q];
+        const uint32_t D = ((w2 >> 7) & 0x00FF00FFu) + 0x01000100u - lo2;
+        const uint32_t viol = (D ^ 0x01000100u) & 0x01F001F0u;  // nonzero in a half iff outside
+        view16[q] = ((D & 0x000F000Fu) << 4) | ((w2 >> 3) & 0x000E000Eu) | ((w2 >> 15) & 0x00010001u);
+        lo16[q] = w2 & 0x000F000Fu;
+        const uint32_t e2 = (viol + 0x01F001F0u) & 0x02000200u;  // bit 9: weight 2q, bit 25: 2q + 1
+        mask |= ((e2 >> 9) & 1u) << (2 * q);
+        mask |= (e2 >> 25) << (2 * q + 1);
+    }
+    uint32_t vw[8], bw[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) vw[i] = __byte_perm(view16[2 * i], view16[2 * i + 1], 0x6420);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        bw[i] = lo16[4 * i] | (lo16[4 * i + 1] << 4) | (lo16[4 * i + 2] << 8) | (lo16[4 * i + 3] << 12);
+    // weights past the matrix (rows n >= N, columns k >= K: whole groups of 8) hold zero codes
+    const int vk = (n < a.N) ? min(32, max(0, a.K - k0)) : 0;
+    if (vk < 32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (4 * i >= vk) vw[i] = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (8 * i >= vk) bw[i] = 0;
+        mask &= (vk > 0) ? (0xFFFFFFFFu >> (32 - vk)) : 0u;
     }
     const uint32_t cnt = __popc(mask);
     const uint32_t partner = __shfl_xor_sync(0xFFFFFFFFu, cnt, 1);
@@ -206,23 +260,35 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
     // pos = 64*n_l + k_l (thread order), then padding to a multiple of 4 words
     uint32_t total;
     const uint32_t rank = block_excl_scan256(cnt, &total);
-    const int64_t seg = static_cast<int64_t>(a.rec_off[r]);
+    const int64_t seg = static_cast<int64_t>(rec_off_r);
     if (total > 0 && (threadIdx.x & 63) == 63) {  // last thread of 32-row quarter q
         const int64_t hi = seg + (threadIdx.x >> 6);
         if (hi < a.rec_cap) a.rec_esc[hi] = rank + cnt;
     }
     const int64_t rbase = seg + 4 + rank;
     // canonical per-channel list: this channel's escapes in earlier k tiles come first
-    const int64_t cbase = (n < a.N) ? static_cast<int64_t>(a.chan_off[n]) +
-                                          a.ct[static_cast<size_t>(n) * a.k_tiles + kt] +
-                                          (half ? partner : 0)
-                                    : 0;
-    // escapes are rare (about one per record): their patterns are read again (from L2) rather
-    // than keeping the 32 loaded patterns live across the block scan, which cost occupancy
+    const int64_t cbase = (n < a.N) ? static_cast<int64_t>(chan_off_n) + ct_nk + (half ? partner : 0) : 0;
+    // Escapes are rare (about one per record): their patterns are read again (from L2) rather
+    // than kept live across the block scan. Each one's record bytes, written above with the
+    // in-window codes, get their placeholders here: the view byte (above the window E = 15,
+    // m_hi = 7; below it zero; the sign stays), and the plane-B byte it shares with weight j ^ 2
+    // (B = 15 above the window, 0 below, the weight's own low bits inside).
+    const uint16_t *wrow = a.w + static_cast<size_t>(n) * a.K + k0;
+    auto low_code = [&](uint32_t b) -> uint32_t {
+        const int e = static_cast<int>((b >> 7) & 0xFFu);
+        return (e > En) ? 0xFu : ((e < En - 15) ? 0u : (b & 0xFu));
+    };
     uint32_t seen = 0;
     for (uint32_t m = mask; m != 0; m &= m - 1) {
         const int j = __ffs(m) - 1;
-        const uint32_t bits = __ldg(a.w + static_cast<size_t>(n) * a.K + k0 + j);
+        const uint32_t bits = __ldg(wrow + j);
+        const uint32_t bits2 = __ldg(wrow + (j ^ 2));
+        const bool above = static_cast<int>((bits >> 7) & 0xFFu) > En;
+        rec[2048 * (2 * half + (j >> 4)) + 16 * nl + (j & 15)] = static_cast<uint8_t>((above ? 0xFEu : 0u) | (bits >> 15));
+        const int i8 = j & 7, nib = (i8 >> 1) + 4 * (i8 & 1);
+        const uint32_t lj = low_code(bits), lp = low_code(bits2);
+        rec[kViewBytes + 2048 * half + 16 * nl + 4 * (j >> 3) + (nib >> 1)] =
+            static_cast<uint8_t>((nib & 1) ? (lp | (lj << 4)) : (lj | (lp << 4)));
         const int64_t ri = rbase + seen, ci = cbase + seen;
         if (ri < a.rec_cap)
             a.rec_esc[ri] = static_cast<uint32_t>(nl * kTileK + 32 * half + j) | (bits << 16);
@@ -239,27 +305,6 @@ __global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
     }
 }
 
-// one warp per channel: exclusive prefix of its per-k-tile counts, in place, and the total
-__global__ void __launch_bounds__(256) rowscan_kernel(uint32_t *ct, int n_pad, int k_tiles, uint32_t *chan_cnt) {
-    const int n = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-    if (n >= n_pad) return;
-    uint32_t *row = ct + static_cast<size_t>(n) * k_tiles;
-    uint32_t run = 0;
-    for (int k0 = 0; k0 < k_tiles; k0 += 32) {
-        const int kt = k0 + lane;
-        const uint32_t c = (kt < k_tiles) ? row[kt] : 0u;
-        uint32_t incl = c;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-            if (lane >= off) incl += o;
-        }
-        if (kt < k_tiles) row[kt] = run + incl - c;
-        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
-    }
-    if (lane == 0) chan_cnt[n] = run;
-}
-
 // words of a record's index segment with c escapes: none, or a 4-word header + c entries
 // rounded up to a multiple of 4
 __device__ __forceinline__ uint32_t segment_words(uint32_t c) { return c ? 4u + ((c + 3u) & ~3u) : 0u; }
@@ -272,42 +317,70 @@ struct ScanJob {
     int seg;
 };
 
-// block b runs job b (the channel scan and the record scan share one launch)
+// Block b runs job b (the channel scan and the record scan share one launch). The input goes
+// through shared memory a tile of kScanThreads * kScanPer values at a time: read and written
+// back with coalesced accesses, each thread summing and then prefixing its own kScanPer
+// consecutive values there, with a block scan of the thread sums in between and the running
+// total carried from tile to tile.
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(ScanJob j0, ScanJob j1) {
     const ScanJob &job = blockIdx.x == 0 ? j0 : j1;
     const uint32_t *in = job.in;
     const int64_t count = job.count;
     uint32_t *out = job.out;
     const int seg = job.seg;
+    extern __shared__ uint32_t tile[];  // kScanThreads * kScanPer (+ 1 per 32, against bank conflicts)
     __shared__ uint32_t warp_sums[kScanThreads / 32];
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const int64_t chunk = (count + kScanThreads - 1) / kScanThreads;
-    const int64_t lo = t * chunk, hi = (lo + chunk < count) ? lo + chunk : count;
-    uint32_t local = 0;
-    for (int64_t i = lo; i < hi; ++i) {
-        const uint32_t v = in[i];
-        local += seg ? segment_words(v) : v;
-    }
-    uint32_t incl = local;
+    auto at = [](int i) { return i + (i >> 5); };  // padded index: a thread's kScanPer values span banks
+    uint32_t carry = 0;
+    constexpr int kTile = kScanThreads * kScanPer;
+    for (int64_t base = 0; base < count; base += kTile) {
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += o;
+        for (int j = 0; j < kScanPer; ++j) {
+            const int i = j * kScanThreads + t;
+            const uint32_t v = (base + i < count) ? in[base + i] : 0u;
+            tile[at(i)] = seg ? segment_words(v) : v;
+        }
+        __syncthreads();
+        uint32_t local = 0;
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j) local += tile[at(t * kScanPer + j)];
+        uint32_t incl = local;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {  // inclusive scan of the 32 warp sums
+            uint32_t x = warp_sums[lane];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, x, off);
+                if (lane >= off) x += o;
+            }
+            warp_sums[lane] = x;
+        }
+        __syncthreads();
+        const uint32_t before = warp ? warp_sums[warp - 1] : 0u, all = warp_sums[kScanThreads / 32 - 1];
+        uint32_t run = carry + before + incl - local;
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j) {
+            const uint32_t v = tile[at(t * kScanPer + j)];
+            tile[at(t * kScanPer + j)] = run;
+            run += v;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < kScanPer; ++j) {
+            const int i = j * kScanThreads + t;
+            if (base + i < count) out[base + i] = tile[at(i)];
+        }
+        carry += all;
+        __syncthreads();  // the tile and warp_sums are reused
     }
-    if (lane == 31) warp_sums[warp] = incl;
-    __syncthreads();
-    uint32_t before = 0, all = 0;
-    for (int i = 0; i < kScanThreads / 32; ++i) {
-        if (i < warp) before += warp_sums[i];
-        all += warp_sums[i];
-    }
-    uint32_t run = before + incl - local;
-    for (int64_t i = lo; i < hi; ++i) {
-        const uint32_t v = in[i];
-        out[i] = run;
-        run += seg ? segment_words(v) : v;
-    }
-    if (t == 0) out[count] = all;
+    if (t == 0) out[count] = carry;
 }
 
 struct Scratch {
@@ -354,11 +427,13 @@ w12_status count_pass(const uint16_t *w, int N, int K, const Scratch &s, uint8_t
     const int n_pad = n_tiles * kTileN;
     const int R = n_tiles * k_tiles;
     W12_CUDA(cudaMemsetAsync(s.rec_cnt, 0, sizeof(uint32_t) * static_cast<size_t>(R), st));
-    window_kernel<<<n_pad / kWindowWarps, kWindowWarps * 32, 0, st>>>(w, N, K, k_tiles, base_exp, s.ct, s.rec_cnt);
+    window_kernel<<<n_pad / kWindowWarps, kWindowWarps * 32, 0, st>>>(w, N, K, k_tiles, base_exp, s.ct, s.rec_cnt,
+                                                                       s.chan_cnt);
     W12_CUDA(cudaGetLastError());
-    rowscan_kernel<<<static_cast<int>(ceil_div(n_pad, 8)), 256, 0, st>>>(s.ct, n_pad, k_tiles, s.chan_cnt);
-    W12_CUDA(cudaGetLastError());
-    scan_kernel<<<2, kScanThreads, 0, st>>>(ScanJob{s.chan_cnt, N, esc_off, 0}, ScanJob{s.rec_cnt, R, rec_off, 1});
+    static const cudaError_t scan_attr =
+        cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kScanSmem));
+    W12_CUDA(scan_attr);
+    scan_kernel<<<2, kScanThreads, kScanSmem, st>>>(ScanJob{s.chan_cnt, N, esc_off, 0}, ScanJob{s.rec_cnt, R, rec_off, 1});
     W12_CUDA(cudaGetLastError());
     return W12_OK;
 }

@@ -26,7 +26,7 @@ constexpr int kMulThreads = 256;
 //      (hi, lo) with error-free transformations (the exact square as p + e from an FMA; two-sum
 //      additions), across the block in a fixed order: about 2^-40 relative accuracy;
 //   3. the mean's reciprocal square root starts from the fp32 approximation and takes one Newton
-//      step in fp64 (about 2^-43), kept as an fp32 pair;
+//      step in fp32 pairs (about 2^-43), kept as an fp32 pair;
 //   4. each of the thread's four columns, scaled by 2^-e (exact), is multiplied by it and rounded
 //      once to bf16 (fp32 arithmetic; fp64 only for results near the bottom of the fp32 range).
 // The result is the bf16 rounding of h / rms(h) except where that quotient lies within about
@@ -35,7 +35,7 @@ constexpr int kMulThreads = 256;
 constexpr int kRmsChunk = 4 * kRmsThreads;  // columns per block
 constexpr int kRmsRound = 8;                // 16-byte loads in flight per thread
 
-__global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__restrict__ h, int K, double inv_k,
+__global__ void __launch_bounds__(kRmsThreads) rms_bf16_kernel(const float *__restrict__ h, int K, F2 inv_k,
                                                                uint16_t *__restrict__ x) {
     grid_launch_dependents();
     grid_dependency_wait();
@@ -176,7 +176,7 @@ extern "C" w12_status w12_rms_bf16(const float *h, int M, int K, uint16_t *x, un
     W12_TRY(launch_cfg(&cfg, attr, flags, stream));
     cfg.gridDim = dim3(static_cast<unsigned>((K + kRmsChunk - 1) / kRmsChunk), static_cast<unsigned>(M));
     cfg.blockDim = dim3(kRmsThreads);
-    W12_CUDA(cudaLaunchKernelEx(&cfg, rms_bf16_kernel, h, K, 1.0 / static_cast<double>(K), x));
+    W12_CUDA(cudaLaunchKernelEx(&cfg, rms_bf16_kernel, h, K, f2_of(1.0 / static_cast<double>(K)), x));
     return W12_OK;
 }
 

@@ -607,21 +607,12 @@ __device__ __forceinline__ float scale_pow2(float v, int s) {
     return ldexpf(v, s);
 }
 
-// bf16 bits of w * y, nearest even, for y = yh + yl (|yl| <= ulp(yh) / 2) and w fp32, without fp64
-// in the common case. p = fl(w yh) is within 1.5 fp32 ulps of w y (the product's rounding error
-// plus w yl), so unless p lies within one ulp of the midpoint between its two bf16 neighbours,
-// p rounds like w y. Near the midpoint m, the sign of (p - m) + (w yh - p) + w yl decides (p - m
-// is exact; the product error comes from an FMA). Results near or below the fp32 normal range,
-// and non-finite ones, take the fp64 route.
-__device__ __forceinline__ uint16_t bf16_mul_rne(float w, float yh, float yl) {
-    const float p = __fmul_rn(w, yh);
+// The two rare cases of bf16_mul_rne below, kept out of line so the common path stays short.
+static __device__ __noinline__ uint16_t bf16_mul_rne_f64(float w, float yh, float yl) {
+    return bf16_bits_rne(static_cast<double>(w) * (static_cast<double>(yh) + static_cast<double>(yl)));
+}
+static __device__ __noinline__ uint16_t bf16_mul_rne_mid(float w, float yh, float yl, float p) {
     const uint32_t bits = __float_as_uint(p);
-    const uint32_t mag = bits & 0x7FFFFFFFu;
-    if (mag < 0x04000000u || mag >= 0x7F000000u)  // |p| < 2^-119, or at least 2^127 (Inf, NaN)
-        return bf16_bits_rne(static_cast<double>(w) * (static_cast<double>(yh) + static_cast<double>(yl)));
-    const uint32_t lo16 = bits & 0xFFFFu;
-    if (lo16 - 0x7FFFu > 2u)  // not within one ulp of the midpoint
-        return static_cast<uint16_t>((bits + 0x7FFFu + ((bits >> 16) & 1u)) >> 16);
     const float m = __uint_as_float((bits & 0xFFFF0000u) | 0x8000u);
     const float t = __fadd_rn(__fmaf_rn(w, yh, -p), __fmul_rn(w, yl));
     float d = __fadd_rn(__fsub_rn(p, m), t);  // w y - m, its sign exact but for a cancellation below 2^-149
@@ -632,9 +623,29 @@ __device__ __forceinline__ uint16_t bf16_mul_rne(float w, float yh, float yl) {
     return static_cast<uint16_t>(down + (down & 1u));  // on the midpoint: the even neighbour
 }
 
+// bf16 bits of w * y, nearest even, for y = yh + yl (|yl| <= ulp(yh) / 2) and w fp32, without fp64
+// in the common case. p = fl(w yh) is within 1.5 fp32 ulps of w y (the product's rounding error
+// plus w yl), so unless p lies within one ulp of the midpoint between its two bf16 neighbours,
+// p rounds like w y. Near the midpoint m, the sign of (p - m) + (w yh - p) + w yl decides (p - m
+// is exact; the product error comes from an FMA). Results near or below the fp32 normal range,
+// and non-finite ones, take the fp64 route.
+__device__ __forceinline__ uint16_t bf16_mul_rne(float w, float yh, float yl) {
+    const float p = __fmul_rn(w, yh);
+    const uint32_t bits = __float_as_uint(p);
+    const uint32_t mag = bits & 0x7FFFFFFFu;
+    if (mag < 0x04000000u || mag >= 0x7F000000u) return bf16_mul_rne_f64(w, yh, yl);  // |p| < 2^-119, >= 2^127
+    if ((bits & 0xFFFFu) - 0x7FFFu <= 2u) return bf16_mul_rne_mid(w, yh, yl, p);     // within an ulp of the midpoint
+    return static_cast<uint16_t>((bits + 0x7FFFu + ((bits >> 16) & 1u)) >> 16);
+}
+
 struct F2 {  // an unevaluated sum hi + lo of two fp32 values
     float hi, lo;
 };
+// a double as an fp32 pair hi + lo (host or device)
+__host__ __device__ inline F2 f2_of(double v) {
+    const float hi = static_cast<float>(v);
+    return {hi, static_cast<float>(v - static_cast<double>(hi))};
+}
 // a + b, with the rounding error of the leading addition carried into lo (two-sum)
 __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
     const float s = __fadd_rn(a.hi, b.hi);
@@ -645,18 +656,33 @@ __device__ __forceinline__ F2 f2_add(F2 a, F2 b) {
     return {hi, __fsub_rn(lo, __fsub_rn(hi, s))};
 }
 
-// 1 / rms of a row from the sum of squares of its values scaled by 2^-e (t, in fp32 pairs) and 1 / K:
-// the fp32 reciprocal square root of the mean and one Newton step in fp64 (about 2^-43), split
-// into an fp32 pair (yh, yl). The row's x = bf16(h / rms(h)) is then bf16_mul_rne(h * 2^-e, yh, yl).
+// 1 / rms of a row from the sum t (fp32 pair) of the squares of its values scaled by 2^-e and 1/K as
+// an fp32 pair: the fp32 reciprocal square root y0 of the mean and one Newton step,
+// y1 = y0 + y0 (1 - mean y0^2) / 2, with the residual formed in fp32 pairs (the square of y0 and
+// the products exact through FMAs; 1 - q is exact since q is within a few ulps of 1), about 2^-43
+// relative; returned as an fp32 pair. The row's x = bf16(h / rms(h)) is then
+// bf16_mul_rne(h * 2^-e, yh, yl).
 struct RmsScale {
     float yh, yl;
 };
-__device__ __forceinline__ RmsScale rms_scale(F2 t, double inv_k) {
-    const double mean = (static_cast<double>(t.hi) + static_cast<double>(t.lo)) * inv_k;
-    const double y0 = static_cast<double>(rsqrtf(static_cast<float>(mean)));
-    const double y1 = y0 * fma(-0.5 * mean * y0, y0, 1.5);
-    const float yh = __double2float_rn(y1);
-    return {yh, __double2float_rn(y1 - static_cast<double>(yh))};
+__device__ __forceinline__ RmsScale rms_scale(F2 t, F2 inv_k) {
+    // mean = t * inv_k as a pair (mh, ml)
+    const float p = __fmul_rn(t.hi, inv_k.hi);
+    float pe = __fmaf_rn(t.hi, inv_k.hi, -p);
+    pe = __fadd_rn(pe, __fadd_rn(__fmul_rn(t.hi, inv_k.lo), __fmul_rn(t.lo, inv_k.hi)));
+    const float mh = __fadd_rn(p, pe);
+    const float ml = __fsub_rn(pe, __fsub_rn(mh, p));
+    const float y0 = rsqrtf(mh);
+    // mean * y0^2 = q + qe
+    const float s = __fmul_rn(y0, y0);
+    const float se = __fmaf_rn(y0, y0, -s);
+    const float q = __fmul_rn(mh, s);
+    float qe = __fmaf_rn(mh, s, -q);
+    qe = __fadd_rn(qe, __fadd_rn(__fmul_rn(mh, se), __fmul_rn(ml, s)));
+    const float r = __fsub_rn(__fsub_rn(1.f, q), qe);
+    const float corr = __fmul_rn(__fmul_rn(0.5f, y0), r);
+    const float yh = __fadd_rn(y0, corr);
+    return {yh, __fsub_rn(corr, __fsub_rn(yh, y0))};
 }
 
 __device__ __forceinline__ uint32_t base2_of(int En) {

@@ -81,7 +81,7 @@ struct SParams {
     STensor t[kMaxLayersS][kKinds];
     SKind kind[kKinds];
     int L, M, npad, stages, nacc, acc_cols, G, H, F, Nqkv, rms_chunks, sbytes;
-    double inv_h;  // 1 / H
+    F2 inv_h;  // 1 / H as an fp32 pair
     float *h;
     uint16_t *xa, *xm, *qkv, *pg, *x_out;
     float *partials;     // [2][G][2][M][128]
@@ -608,7 +608,9 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                         continue;
                     }
                     const int e = ilogbf(bmax) + 1;  // |h| * 2^-e < 1
-                    F2 acc = {0.f, 0.f};
+                    // four independent pair sums (one per 32-bit lane of the 16-byte words), so the
+                    // dependent chain is a quarter as long; then combined in a fixed order
+                    F2 a4[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll 1
                     for (int t = 0; t < kRowF4; ++t) {
                         const float q[4] = {scale_pow2(v[t].x, -e), scale_pow2(v[t].y, -e), scale_pow2(v[t].z, -e),
@@ -616,9 +618,10 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
 #pragma unroll
                         for (int j = 0; j < 4; ++j) {
                             const float pp = __fmul_rn(q[j], q[j]);
-                            acc = f2_add(acc, F2{pp, __fmaf_rn(q[j], q[j], -pp)});
+                            a4[j] = f2_add(a4[j], F2{pp, __fmaf_rn(q[j], q[j], -pp)});
                         }
                     }
+                    F2 acc = f2_add(f2_add(a4[0], a4[1]), f2_add(a4[2], a4[3]));
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1)
                         acc = f2_add(acc, F2{__shfl_xor_sync(kAllOnes, acc.hi, off), __shfl_xor_sync(kAllOnes, acc.lo, off)});
@@ -631,10 +634,13 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                     }
                     named_bar_sync(kEpiBarS, 128);
                     const float yh = ctrl->scale.yh, yl = ctrl->scale.yl;
+                    // this thread's words in the unit's chunk: t with i_lo <= et + 128 t < i_hi
+                    const int t_lo = (i_lo > et) ? (i_lo - et + 127) / 128 : 0;
 #pragma unroll 1
-                    for (int t = 0; t < kRowF4; ++t) {
+                    for (int t = t_lo; t < kRowF4; ++t) {
                         const int i = et + 128 * t;
-                        if (i >= i_lo && i < i_hi) {
+                        if (i >= i_hi) break;
+                        {
                             uint2 out;
                             out.x = static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[t].x, -e), yh, yl)) |
                                     (static_cast<uint32_t>(bf16_mul_rne(scale_pow2(v[t].y, -e), yh, yl)) << 16);
@@ -1170,7 +1176,7 @@ extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_laye
     p.F = P.F;
     p.Nqkv = P.Nqkv;
     p.rms_chunks = P.rms_chunks;
-    p.inv_h = 1.0 / static_cast<double>(P.H);
+    p.inv_h = f2_of(1.0 / static_cast<double>(P.H));
     p.sbytes = P.sbytes;
     p.h = h;
     p.xa = reinterpret_cast<uint16_t *>(ws + P.off_xa);
