@@ -1081,7 +1081,9 @@ w12_status plan_stream(const w12_stream_layer *layers, int n_layers, int M, int 
     P->smem = 1024 + stages * P->sbytes + ctrl;
     // row-normalisation units: (row, chunk of the row) spread over the blocks
     const int H4 = H / 4;
-    P->rms_chunks = std::max(1, std::min(std::max(1, sms / M), (H4 + 127) / 128));
+    // (every unit reads its whole row for the statistics and writes its chunk: spreading the
+    // writes over more blocks shortens the phase while blocks are left over)
+    P->rms_chunks = std::max(1, std::min(std::max(1, sms / M), (H4 + 7) / 8));
     P->max_tiles = 0;
     for (const SKind &k : P->kind) P->max_tiles = std::max(P->max_tiles, k.n_tiles);
     size_t off = 0;
