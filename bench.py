@@ -250,7 +250,7 @@ def main():
                          "finishes; weights are static); plain: ordinary stream-ordered launches")
     ap.add_argument("--profile-gemm", type=int, default=0, metavar="M",
                     help="only run `--steps` W12 GEMM launches at M rows on the projection (for ncu)")
-    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax", "certified", "q6", "stream"])
+    ap.add_argument("--profile-op", default="gemm", choices=["gemm", "qview", "argmax", "certified", "q6", "stream", "encode"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -447,6 +447,8 @@ def profile_gemm(args):
     M = args.profile_gemm
     if args.profile_op == "stream":
         return profile_stream(args, dev, M)
+    if args.profile_op == "encode":
+        return profile_encode(args, dev)
     head = args.profile_op in ("argmax", "certified")
     N = VOCAB if head else N_MLP
     rec = synth.HEAD if head else synth.PROJ
@@ -477,6 +479,26 @@ def profile_gemm(args):
     w12.check(t)
     print(json.dumps({"op": args.profile_op, "M": M, "N": N, "K": K_HID, "launch_us_median": statistics.median(ts),
                       "bytes": t.gemm_bytes(args.profile_op == "qview")}))
+
+
+def profile_encode(args, dev):
+    """Encodes of the projection through the public calls (sizes, allocation, encode); prints the
+    median time of one. Used as the command under ncu for the encoder's kernels."""
+    from lossless_bit_weight_gb300 import w12
+
+    w = synth.weights(N_MLP, K_HID, synth.PROJ, seed=synth.seed_for(1, 0), device=dev)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        t = w12.encode(w)
+        b.record()
+        b.synchronize()
+        if i >= args.warmup:
+            ts.append(a.elapsed_time(b) * 1e3)
+    assert w12.verify(t, w) == 0
+    print(json.dumps({"op": "encode", "N": N_MLP, "K": K_HID, "encode_us_median": statistics.median(ts),
+                      "algorithmic_bytes": 3.5 * N_MLP * K_HID}))
 
 
 def profile_stream(args, dev, M, n_layers=2):
