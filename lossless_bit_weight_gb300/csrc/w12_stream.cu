@@ -904,7 +904,7 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                         acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
                         const int g = g0 + 128 * q;
                         const int m = g / (kTileN / 4), n = tile * kTileN + 4 * (g % (kTileN / 4));
-                        hv[q] = (k != kKindQkv && g < g_hi)
+                        hv[q] = (k != kKindQkv && g < g_hi && n < K.N)
                                     ? __ldcg(reinterpret_cast<const float4 *>(p.h + static_cast<size_t>(m) * p.H + n))
                                     : make_float4(0.f, 0.f, 0.f, 0.f);
                     }

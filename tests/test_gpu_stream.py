@@ -9,6 +9,8 @@
 - the full 64-layer model (hidden 5120, q 6144, k|v 2 x 1024, ffn 17408) at M in {1, 16, 32}:
   the step against the chain of launches, the head's argmax of its output against the oracle,
   and the first and last layers' linears against the oracle on sampled outputs;
+- rows wider than one normalisation unit holds (the multi-pass normalisation, ragged last tiles)
+  against the chain and the oracle;
 - repeated steps on one workspace give identical rows (its counters are left zeroed);
 - shapes the kernel does not take are refused on the host.
 """
@@ -126,6 +128,38 @@ def test_stream_small_matches_chain_and_oracle(w12, M):
     yd, add = oracle.gemm(to_np_u16(buf["p"]), to_np_u16(w["down"]))
     assert gemm_violations(d.cpu().numpy(), yd, add) == 0
     assert torch.equal(hs.view(torch.int32), (h_mid + d).view(torch.int32))
+    check_rms(xs, hs)
+
+
+@pytest.mark.parametrize("M", [1, 7])
+def test_stream_wide_rows(w12, M):
+    """Rows longer than one normalisation unit holds at once (hidden 5184 > 1280 16-byte words of
+    128 threads x 10): the normalisation's multi-pass path and the o and down sums over a ragged
+    last tile. With 81 k tiles the interleaved gate|up tensor splits its tiles' k ranges at other
+    points than the chain's concatenated one, so the gate|up sums, p and h are checked against the
+    oracle here; x, q|k|v and x2 against the chain bit for bit."""
+    L, H, nq, nkv, F = 1, 5184, 192, 64, 512
+    chain, step_layers, bf = make_layers(w12, L, H, nq, nkv, F, seed=700 + M, keep=(0,))
+    h0 = synth.activations(M, H, seed=710 + M, device="cuda").float() * 3.0
+    step = w12.StreamStep(step_layers, M, nq)
+    hs = h0.clone()
+    xs = step(hs)
+    step.check()
+    b = {k: v.clone() for k, v in step.buffers().items()}
+    w = bf[0]
+    x = w12.rms_bf16(h0)
+    assert torch.equal(b["x"].view(torch.int16), x.view(torch.int16))
+    check_rms(b["x"], h0)
+    assert torch.equal(b["qkv"].view(torch.int16), w12.gemm(chain[0]["qkv"], x, out_dtype=torch.bfloat16).view(torch.int16))
+    a = b["qkv"][:, :nq].contiguous()
+    h_mid = h0 + w12.gemm(step_layers[0]["o"], a)
+    assert torch.equal(b["x2"].view(torch.int16), w12.rms_bf16(h_mid).view(torch.int16))
+    check_rms(b["x2"], h_mid)
+    check_gate_up_product(b["p"], b["x2"], w["gate"], w["up"])
+    d, ad = oracle.gemm(to_np_u16(b["p"]), to_np_u16(w["down"]))
+    h_ref = h_mid.double().cpu().numpy() + d
+    tol = REL * ad + ABS + np.abs(h_ref) * 2.0 ** -23
+    assert np.all(np.abs(hs.double().cpu().numpy() - h_ref) <= tol)
     check_rms(xs, hs)
 
 
