@@ -469,6 +469,21 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
     return v;
 }
 
+// A release increment of a counter (gpu scope): the writes that happen before it in this block
+// (the calling thread's, and the other threads' before a block barrier that the caller passed) are
+// visible to a thread that reads the incremented value with an acquire load.
+__device__ __forceinline__ void red_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// The same with the old value returned and acquire semantics as well: the caller (and, after a
+// block barrier, its block) sees every write released by the increments before this one.
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

@@ -16,15 +16,16 @@
 //
 // Design on GB300: one block per SM (cooperative launch, so all blocks are resident), the warp
 // roles of the W12 GEMM kernel (activation producer, two MMA issuers, a feeder of records and
-// escape words, four epilogue warps, three decode groups of four warps) and one ring of slots that
-// runs through every GEMM of the step. Weights are static, so the feeder keeps fetching the records
-// of the next GEMM into free slots and the decode groups keep decoding them into tensor memory
-// while the previous phase
-// is still finishing; only the activation copies of a GEMM wait, until every block has completed
-// the phase that writes them (a per-phase completion counter in global memory, polled with a
-// bounded wait). The epilogue warps write each GEMM's outputs (a tile split between blocks is
-// summed in increasing block order by the block that publishes its part last) and run the
-// row-normalisation phases. The gate and up rows are interleaved in blocks of 64 at load time, so
+// escape words, four epilogue warps, three decode groups of four warps) and a sequence of slots
+// (two records each) that runs through every GEMM of the step. Weights are static, so the feeder
+// keeps fetching the records of the next GEMM into free shared-memory slots and the decode groups
+// keep decoding them into free tensor-memory slots while the previous phase is still finishing;
+// only the activation copies of a GEMM wait, until every block has completed the phase that
+// writes them (a per-phase completion counter in global memory, polled with a bounded wait). The
+// two kinds of slot form rings of their own, so at a phase boundary both shared and tensor memory
+// hold the next phase's weights. The epilogue warps write each GEMM's outputs (a tile split
+// between blocks is summed in increasing block order, each of the tile's blocks summing a slice of
+// it; gate|up's by the block that publishes its part last) and run the row-normalisation phases. The gate and up rows are interleaved in blocks of 64 at load time, so
 // a 128-row tile holds 64 gate rows and the 64 matching up rows and its epilogue forms the
 // product. Every wait is bounded (about a second); a block that gives up records an error bit in
 // the workspace error word and stops.
@@ -44,9 +45,10 @@ namespace {
 constexpr int kDecGroupsS = 3;
 constexpr int kThreadsS = 32 * (8 + 4 * kDecGroupsS);
 constexpr int kWProducer = 0, kWMma = 1, kWEscape = 2, kWMma2 = 3, kWEpi0 = 4, kWDec0 = 8;
-constexpr int kEscCapS = 128;      // index words staged per slot; more -> read from global
+constexpr int kEscCapS = 112;      // index words staged per slot; more -> read from global
 constexpr int kAColsS = 32;        // tensor-memory columns of one decoded record
-constexpr int kMaxStagesS = 8;
+constexpr int kMaxStagesS = 8;     // slots of decoded records in tensor memory (and their activations)
+constexpr int kMaxRawS = 10;       // slots of copied records in shared memory
 constexpr int kRowF4 = 10;  // 16-byte words of a row one epilogue thread holds in a normalisation unit
 constexpr int kTmemColsS = 512;
 constexpr int kSmemLimitS = 232448;
@@ -80,7 +82,7 @@ struct SKind {  // shape and work split of one of the four linears (the same in 
 struct SParams {
     STensor t[kMaxLayersS][kKinds];
     SKind kind[kKinds];
-    int L, M, npad, stages, nacc, acc_cols, G, H, F, Nqkv, rms_chunks, sbytes;
+    int L, M, npad, stages, rstages, nacc, acc_cols, G, H, F, Nqkv, rms_chunks, sbytes;
     F2 inv_h;  // 1 / H as an fp32 pair
     float *h;
     uint16_t *xa, *xm, *qkv, *pg, *x_out;
@@ -93,13 +95,14 @@ struct SParams {
 };
 
 struct SCtrl {
-    uint64_t full[kMaxStagesS], afull[kMaxStagesS], empty[kMaxStagesS], xfull[kMaxStagesS];
+    uint64_t full[kMaxRawS], rfree[kMaxRawS];                        // copied-record slots
+    uint64_t afull[kMaxStagesS], empty[kMaxStagesS], xfull[kMaxStagesS];  // decoded slots
     uint64_t accfull[2], accempty[2];
     uint64_t drained[2];
-    uint2 esc_info[kMaxStagesS];
-    const uint32_t *esc_ptr[kMaxStagesS];  // the slot's index words in global memory (when not staged)
-    int slot_nr[kMaxStagesS];              // records in the slot (1 or 2)
-    int slot_en1[kMaxStagesS];             // offset of the second record's window bases (0: same tile)
+    uint2 esc_info[kMaxRawS];
+    const uint32_t *esc_ptr[kMaxRawS];  // the slot's index words in global memory (when not staged)
+    int slot_nr[kMaxRawS];              // records in the slot (1 or 2)
+    int slot_en1[kMaxRawS];             // offset of the second record's window bases (0: same tile)
     int nslots;                            // slots in the block's whole sequence
     uint32_t tmem_base;
     int abort;
@@ -111,6 +114,9 @@ struct SCtrl {
 constexpr size_t kSCtrlBytes = (sizeof(SCtrl) + 127) / 128 * 128;
 constexpr size_t kXchgBytes = 16 * 64 * 4;  // up-half values of 16 rows x 64 columns
 constexpr int kEnBytes = 2 * kTileN;        // a slot's window bases E_n: 128 rows per record
+// a copied-record slot: two records, the index words, the window bases
+constexpr int kRawBytes = 2 * kRecordBytes + kEscCapS * 4 + kEnBytes;
+static_assert(kRawBytes % 16 == 0, "bulk copies land on 16-byte boundaries");
 
 __device__ __forceinline__ int range_start_s(int c, int units, int G) {
     return static_cast<int>(static_cast<uint32_t>(c) * static_cast<uint32_t>(units) / static_cast<uint32_t>(G));
@@ -210,22 +216,31 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     grid_launch_dependents();  // the next kernel may start loading its weights as SMs free up
-    const int S = p.stages, M = p.M, G = p.G, L = p.L;
+    // Two rings. Copied records (with their index words and window bases) occupy a shared-memory
+    // slot (Sm of them) only until a decode group has moved them into tensor memory; the decoded
+    // records and the slot's activations then wait in one of St tensor-memory slots for the MMAs.
+    // So while the MMAs wait at a phase boundary, Sm + St slots of the next phase are in flight
+    // or ready.
+    const int S = p.stages, Sm = p.rstages, M = p.M, G = p.G, L = p.L;
     const int xbytes = p.npad * 128;
-    const int sbytes = p.sbytes;
-    SCtrl *ctrl = reinterpret_cast<SCtrl *>(smem + S * sbytes);
+    const int sbytes = p.sbytes;  // the two activation tiles of a tensor-memory slot
+    uint8_t *raw = smem + S * sbytes;
+    SCtrl *ctrl = reinterpret_cast<SCtrl *>(raw + Sm * kRawBytes);
     float *xchg = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ctrl) + kSCtrlBytes);
     auto stage_x = [&](int s, int q) { return smem + s * sbytes + q * xbytes; };
-    auto stage_rec = [&](int s, int q) { return smem + s * sbytes + 2 * xbytes + q * kRecordBytes; };
-    auto stage_esc = [&](int s) { return smem + s * sbytes + 2 * xbytes + 2 * kRecordBytes; };
-    auto stage_en = [&](int s) { return smem + s * sbytes + 2 * xbytes + 2 * kRecordBytes + kEscCapS * 4; };
+    auto stage_rec = [&](int m, int q) { return raw + m * kRawBytes + q * kRecordBytes; };
+    auto stage_esc = [&](int m) { return raw + m * kRawBytes + 2 * kRecordBytes; };
+    auto stage_en = [&](int m) { return raw + m * kRawBytes + 2 * kRecordBytes + kEscCapS * 4; };
     const int c = blockIdx.x;
     const uint32_t Gu = static_cast<uint32_t>(G);
 
     if (warp == kWProducer) {
         if (lane == 0) {
+            for (int m = 0; m < Sm; ++m) {
+                mbar_init(smem_u32(&ctrl->full[m]), 1);     // the escape feeder's copies
+                mbar_init(smem_u32(&ctrl->rfree[m]), 128);  // the decode group is done with them
+            }
             for (int s = 0; s < S; ++s) {
-                mbar_init(smem_u32(&ctrl->full[s]), 1);  // the escape feeder's copies
                 mbar_init(smem_u32(&ctrl->afull[s]), 128);
                 mbar_init(smem_u32(&ctrl->empty[s]), 2);  // one arrival per MMA issuer
                 mbar_init(smem_u32(&ctrl->xfull[s]), 1);
@@ -394,10 +409,10 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
         }
     } else if (warp == kWEscape) {
         // ------------------------------------------------- record and escape feeder (warp-wide)
-        // Per slot, as soon as its ring position is free: the summary of the slot's index words
-        // (how many, how many belong to its first record, where they start) for the decode groups,
-        // and the bulk copies of the slot's records, of its index words and of its window bases,
-        // all counted on the slot's full barrier. Lane l holds rec_esc_off[wbase + l] (cur) and [wbase + 32 + l] (nxt) of the
+        // Per slot, as soon as its shared-memory slot is free (rfree): the summary of the slot's
+        // index words (how many, how many belong to its first record, where they start) for the
+        // decode groups, and the bulk copies of the slot's records, of its index words and of its
+        // window bases, all counted on the slot's full barrier. Lane l holds rec_esc_off[wbase + l] (cur) and [wbase + 32 + l] (nxt) of the
         // current phase's tensor, so the offsets are loaded 32 at a time, ahead of use.
         SlotIt it = start;
         RingS st;
@@ -438,7 +453,7 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
             const int tile0 = ftile;
             const bool new_tile = it.nr == 2 && fkt + 1 == KT;  // the second record starts the next tile
             const int s = st.idx;
-            const bool ok = mbar_wait(smem_u32(&ctrl->empty[s]), st.phase ^ 1, abort, p.err, kErrEscape);
+            const bool ok = mbar_wait(smem_u32(&ctrl->rfree[s]), st.phase ^ 1, abort, p.err, kErrEscape);
             if (!__all_sync(kAllOnes, ok)) break;
             const uint32_t fb = smem_u32(&ctrl->full[s]);
             const uint32_t cnt = hi - lo;
@@ -466,15 +481,17 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                 ++ftile;
             }
             it.next(p, c);
-            st.advance(1, S);
+            st.advance(1, Sm);
             issued = it.js;
         }
     } else if (warp >= kWDec0) {
         // ---------------------------------------------------------------- decode groups
         // Group g decodes slots g, g + 3, g + 6, ... of the block's sequence: each thread its row
         // of each record (view bytes and plane B -> 32 bf16x2 words), stored to its tensor-memory
-        // lane, then the warp's escapes patched in tensor memory. Everything a slot needs besides
-        // its records (record count, window bases, escape words) was staged by the escape feeder.
+        // lane, then the warp's escapes patched in tensor memory; then the shared-memory slot is
+        // handed back to the feeder (rfree) and the tensor-memory slot to the MMAs (afull).
+        // Everything a slot needs besides its records (record count, window bases, escape words)
+        // was staged by the escape feeder.
         const int g = (warp - kWDec0) >> 2;
         const int qw = warp & 3;
         const int nl = 32 * qw + lane;
@@ -497,15 +514,16 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
             decode_chunk16<false, 0>(v2, b1, base2, w + 16, m3, m15);
             decode_chunk16<false, 1>(v3, b1, base2, w + 24, m3, m15);
         };
-        // the escapes of record q of slot s that fall in this warp's 32 rows: read the entry's
-        // column, let the owner lane overwrite its half, write the column back
-        auto patch_record = [&](int s, int q, uint2 ei) {
+        // the escapes of record q of shared-memory slot m (decoded into tensor-memory slot s) that
+        // fall in this warp's 32 rows: read the entry's column, let the owner lane overwrite its
+        // half, write the column back
+        auto patch_record = [&](int m, int s, int q, uint2 ei) {
             const uint32_t hdr = ei.x;
             const uint32_t total = hdr & 0x7FFFFFFFu;
             const uint32_t split = ei.y;
             const uint32_t sg0 = (q == 0) ? 0u : split, sg1 = (q == 0) ? split : total;
             if (sg1 <= sg0) return;
-            const uint32_t *seg = ((hdr >> 31) ? ctrl->esc_ptr[s] : reinterpret_cast<const uint32_t *>(stage_esc(s))) + sg0;
+            const uint32_t *seg = ((hdr >> 31) ? ctrl->esc_ptr[m] : reinterpret_cast<const uint32_t *>(stage_esc(m))) + sg0;
             const uint32_t i_hi = seg[qw];
             const uint32_t tbase = a_slot(s, q) + lanes;
             for (uint32_t i = (qw == 0) ? 0u : seg[qw - 1]; i < i_hi; ++i) {
@@ -519,33 +537,49 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                 tmem_wait_st();
             }
         };
-        const bool shared_slots = (S % kDecGroupsS) != 0;  // see the GEMM kernel's decode loop
+        // A slot's shared-memory position (m) and tensor-memory position (s) come from rings of
+        // different sizes. When a ring's size is not a multiple of the group count, consecutive
+        // uses of a position go to different groups: before waiting for a use of the position,
+        // wait until the previous group's use of it is complete (rfree, afull), so that a parity
+        // wait cannot be satisfied by a phase two uses old.
+        const bool shared_m = (Sm % kDecGroupsS) != 0, shared_s = (S % kDecGroupsS) != 0;
+        RingS rm;
+        rm.advance(g, Sm);
         for (int js = g; js < nslots; js += kDecGroupsS) {
-            const int s = st.idx;
-            if (shared_slots) {
+            const int s = st.idx, m = rm.idx;
+            if (shared_m) {
+                const bool ok_prev = mbar_wait(smem_u32(&ctrl->rfree[m]), rm.phase ^ 1, abort, p.err, kErrDecode);
+                if (!__all_sync(kAllOnes, ok_prev)) break;
+            }
+            const bool ok_full = mbar_wait(smem_u32(&ctrl->full[m]), rm.phase, abort, p.err, kErrDecode);
+            if (!__all_sync(kAllOnes, ok_full)) break;
+            const int nr = ctrl->slot_nr[m];
+            const uint8_t *en = stage_en(m);
+            decode_record(m, 0, base2_of(en[nl]), wa);
+            // the tensor-memory slot is free once the MMAs of its previous use have completed
+            if (shared_s) {
                 const bool ok_prev = mbar_wait(smem_u32(&ctrl->afull[s]), st.phase ^ 1, abort, p.err, kErrDecode);
                 if (!__all_sync(kAllOnes, ok_prev)) break;
             }
-            const bool ok_full = mbar_wait(smem_u32(&ctrl->full[s]), st.phase, abort, p.err, kErrDecode);
-            if (!__all_sync(kAllOnes, ok_full)) break;
-            const int nr = ctrl->slot_nr[s];
-            const uint8_t *en = stage_en(s);
-            decode_record(s, 0, base2_of(en[nl]), wa);
+            const bool ok_empty = mbar_wait(smem_u32(&ctrl->empty[s]), st.phase ^ 1, abort, p.err, kErrDecode);
+            if (!__all_sync(kAllOnes, ok_empty)) break;
             tc_fence_after();
             tmem_st_32x32b_x32(a_slot(s, 0) + lanes, wa);
             if (nr == 2) {
-                decode_record(s, 1, base2_of(en[ctrl->slot_en1[s] + nl]), wb);
+                decode_record(m, 1, base2_of(en[ctrl->slot_en1[m] + nl]), wb);
                 tmem_st_32x32b_x32(a_slot(s, 1) + lanes, wb);
             }
             tmem_wait_st();
-            const uint2 ei = ctrl->esc_info[s];
+            const uint2 ei = ctrl->esc_info[m];
             if (ei.x != 0) {
-                patch_record(s, 0, ei);
-                if (nr == 2) patch_record(s, 1, ei);
+                patch_record(m, s, 0, ei);
+                if (nr == 2) patch_record(m, s, 1, ei);
             }
             tc_fence_before();
             mbar_arrive(smem_u32(&ctrl->afull[s]));
+            mbar_arrive(smem_u32(&ctrl->rfree[m]));
             st.advance(kDecGroupsS, S);
+            rm.advance(kDecGroupsS, Sm);
         }
     } else {
         // ---------------------------------------------------------------- epilogue + glue (4 warps)
@@ -560,13 +594,15 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
             if (et == 0 && !dead) ok = wait_count(p.done + ph, Gu, abort, p.err, kErrEpilogue);
             dead = named_bar_or(kEpiBarS, 128, !ok) || dead;
         };
-        // the epilogue's stores of a phase are complete; count this block for the phase
+        // the epilogue's stores of a phase are complete; count this block for the phase (a release
+        // increment after the block barrier: the four warps' stores are visible to whoever
+        // acquires the count)
         auto signal_phase = [&](int ph) {
             named_bar_sync(kEpiBarS, 128);
             if (et == 0) {
-                __threadfence();
-                const uint32_t old = atomicAdd(p.done + ph, 1u);
-                if (ph == kPhasesPerLayer * L && old == Gu - 1) {
+                if (ph < kPhasesPerLayer * L) {
+                    red_release_gpu(p.done + ph, 1u);
+                } else if (atom_add_acq_rel_gpu(p.done + ph, 1u) == Gu - 1) {
                     // every block has passed every wait of this launch: leave the counters zeroed
                     for (int i = 0; i <= kPhasesPerLayer * L; ++i) p.done[i] = 0;
                     for (int i = 0; i < kKinds * p.max_tiles; ++i) p.tile_cnt[i] = 0;
@@ -835,9 +871,8 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                 mbar_arrive(smem_u32(&ctrl->accempty[b]));
                 if (!full && !dead && k != kKindGu) {
                     // publish the part; the tile's sum is formed after the block's last segment
-                    __threadfence();
                     named_bar_sync(kEpiBarS, 128);
-                    if (et == 0) atomicAdd(p.tile_cnt + k * p.max_tiles + tile, 1u);
+                    if (et == 0) red_release_gpu(p.tile_cnt + k * p.max_tiles + tile, 1u);
                     split_tile[nsplit] = tile;
                     split_lo[nsplit] = c_lo;
                     split_hi[nsplit] = c_hi;
@@ -845,15 +880,13 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                 } else if (!full && !dead) {
                     // gate|up split tile: whichever block publishes its part last sums all parts in
                     // block order (the product needs both halves of every row of the tile)
-                    __threadfence();
                     named_bar_sync(kEpiBarS, 128);
                     if (et == 0) {
-                        const uint32_t old = atomicAdd(p.tile_cnt + k * p.max_tiles + tile, 1u);
+                        const uint32_t old = atom_add_acq_rel_gpu(p.tile_cnt + k * p.max_tiles + tile, 1u);
                         ctrl->last = (old == static_cast<uint32_t>(c_hi - c_lo)) ? 1 : 0;
                     }
                     named_bar_sync(kEpiBarS, 128);
                     if (ctrl->last) {
-                        __threadfence();
 #pragma unroll 1
                         for (int m0 = 0; m0 < M; m0 += 16) {
                             float f[16];
@@ -886,11 +919,9 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
                 const int tile = split_tile[sidx], c_lo = split_lo[sidx], c_hi = split_hi[sidx];
                 const int np = c_hi - c_lo + 1;
                 bool okc = true;
-                if (et == 0) {
+                if (et == 0)  // an acquire load of the count; the barrier below passes it to the block
                     okc = wait_count(p.tile_cnt + k * p.max_tiles + tile, layer1 * static_cast<uint32_t>(np), abort, p.err,
                                      kErrEpilogue);
-                    __threadfence();
-                }
                 dead = named_bar_or(kEpiBarS, 128, !okc) || dead;
                 if (dead) break;
                 const int G4 = M * (kTileN / 4);
@@ -982,8 +1013,8 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
     __syncthreads();
     // after an abort, let copies still in flight land before the block's shared memory is released
     if (warp == kWEscape && lane == 0 && ctrl->abort) {
-        for (int js = (issued > S ? issued - S : 0); js < issued; ++js)
-            if (!mbar_wait_drain(smem_u32(&ctrl->full[js % S]), (js / S) & 1)) atomicOr(p.err, kErrDrain);
+        for (int js = (issued > Sm ? issued - Sm : 0); js < issued; ++js)
+            if (!mbar_wait_drain(smem_u32(&ctrl->full[js % Sm]), (js / Sm) & 1)) atomicOr(p.err, kErrDrain);
     }
     if (warp == kWProducer && lane == 0 && ctrl->abort) {
         for (int js = (xissued > S ? xissued - S : 0); js < xissued; ++js)
@@ -1011,7 +1042,7 @@ constexpr int64_t kMinRecs = 8;
 
 struct StreamPlan {
     SKind kind[kKinds];
-    int H, F, Nqkv, nq, npad, stages, nacc, acc_cols, G, sbytes, smem, rms_chunks, max_tiles;
+    int H, F, Nqkv, nq, npad, stages, rstages, nacc, acc_cols, G, sbytes, smem, rms_chunks, max_tiles;
     size_t off_err, off_done, off_tile, off_part, off_xa, off_xm, off_qkv, off_p, ws_bytes;
 };
 
@@ -1068,17 +1099,19 @@ w12_status plan_stream(const w12_stream_layer *layers, int n_layers, int M, int 
     P->nq = n_q;
     P->G = sms;
     P->npad = (M + 15) / 16 * 16;
-    // slots 1024 bytes apart: every activation tile starts on a 128-byte-swizzle atom
-    P->sbytes = static_cast<int>(align_up(2 * P->npad * 128 + 2 * kRecordBytes + kEscCapS * 4 + kEnBytes, 1024));
+    // tensor-memory slots: what the accumulators leave of the 512 columns; each with its two
+    // activation tiles (npad x 128 bytes, so every tile starts on a 128-byte-swizzle atom); then as
+    // many shared-memory slots of copied records as the rest of shared memory holds
+    P->sbytes = 2 * P->npad * 128;
     const int ctrl = static_cast<int>(align_up(kSCtrlBytes + kXchgBytes, 1024));
-    int stages = (kSmemLimitS - 1024 - ctrl) / P->sbytes;
-    stages = std::min(stages, kMaxStagesS);
     P->nacc = 2;
     P->acc_cols = 2 * P->nacc * P->npad;
-    stages = std::min(stages, (kTmemColsS - P->acc_cols) / (2 * kAColsS));
-    if (stages < kDecGroupsS) return W12_ERR_UNSUPPORTED_SHAPE;
+    const int stages = std::min(kMaxStagesS, (kTmemColsS - P->acc_cols) / (2 * kAColsS));
+    const int rstages = std::min(kMaxRawS, (kSmemLimitS - 1024 - ctrl - stages * P->sbytes) / kRawBytes);
+    if (stages < kDecGroupsS || rstages < kDecGroupsS) return W12_ERR_UNSUPPORTED_SHAPE;
     P->stages = stages;
-    P->smem = 1024 + stages * P->sbytes + ctrl;
+    P->rstages = rstages;
+    P->smem = 1024 + stages * P->sbytes + rstages * kRawBytes + ctrl;
     // row-normalisation units: (row, chunk of the row) spread over the blocks
     const int H4 = H / 4;
     // (every unit reads its whole row for the statistics and writes its chunk: spreading the
@@ -1171,6 +1204,7 @@ extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_laye
     p.M = M;
     p.npad = P.npad;
     p.stages = P.stages;
+    p.rstages = P.rstages;
     p.nacc = P.nacc;
     p.acc_cols = P.acc_cols;
     p.G = P.G;
@@ -1254,3 +1288,4 @@ extern "C" w12_status w12_stream_interleave(const uint16_t *gate, const uint16_t
         return W12_ERR_CUDA;
     return W12_OK;
 }
+
