@@ -287,6 +287,15 @@ w12_status w12_stream_buffers(const w12_stream_layer *layers, int n_layers, int 
 w12_status w12_stream_step(const w12_stream_layer *layers, int n_layers, int M, int n_q, float *h, uint16_t *x_out,
                            void *workspace, size_t workspace_bytes, w12_stream_t stream);
 
+/* w12_stream_step with launch flags: 0, or W12_LAUNCH_TEST_STALL, a test hook for the failure
+ * path: each block's activation producer issues the copies of its first slot only, so the
+ * block's bounded waits run out after about a second. Every block then stops, h and x_out are
+ * invalid, w12_check reports W12_ERR_TIMEOUT, and the workspace must be zero-filled again.
+ * Nothing else in the library sets it. Other flags: W12_ERR_INVALID_ARG. */
+w12_status w12_stream_step_ex(const w12_stream_layer *layers, int n_layers, int M, int n_q, float *h,
+                              uint16_t *x_out, void *workspace, size_t workspace_bytes, unsigned flags,
+                              w12_stream_t stream);
+
 /* The gate|up layout w12_stream_step reads, from gate and up (device bf16 [ffn, hidden] each,
  * row-major; ffn % 64 == 0): gate_up (device bf16 [2 * ffn, hidden]) gets gate rows 64 i .. 64 i
  * + 63 at rows 128 i .., and up rows 64 i .. at rows 128 i + 64 ... Two strided device copies on

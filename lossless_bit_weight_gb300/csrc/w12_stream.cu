@@ -92,6 +92,7 @@ struct SParams {
     uint32_t *done;      // [6 L + 1] blocks that completed each phase
     int *err;
     uint32_t m3, m15;
+    int test_stall;  // W12_LAUNCH_TEST_STALL: the producer issues its first slot's copies only
 };
 
 struct SCtrl {
@@ -335,6 +336,7 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
             xi.next(p, c);
             xr.advance(1, S);
             xissued = xi.js;
+            if (p.test_stall) break;  // the test hook: the MMAs' wait on the next slot runs out
         }
     } else if (warp == kWMma || warp == kWMma2) {
         // ---------------------------------------------------------------- MMA issuers (warp-wide)
@@ -1188,9 +1190,11 @@ extern "C" w12_status w12_stream_buffers(const w12_stream_layer *layers, int n_l
     return W12_OK;
 }
 
-extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_layers, int M, int n_q, float *h,
-                                      uint16_t *x_out, void *workspace, size_t workspace_bytes, w12_stream_t stream) {
+extern "C" w12_status w12_stream_step_ex(const w12_stream_layer *layers, int n_layers, int M, int n_q, float *h,
+                                         uint16_t *x_out, void *workspace, size_t workspace_bytes, unsigned flags,
+                                         w12_stream_t stream) {
     if (!h || !x_out || !workspace) return W12_ERR_INVALID_ARG;
+    if (flags & ~static_cast<unsigned>(W12_LAUNCH_TEST_STALL)) return W12_ERR_INVALID_ARG;
     if (!aligned16(h) || (reinterpret_cast<uintptr_t>(x_out) & 7u) || (reinterpret_cast<uintptr_t>(workspace) & 255u))
         return W12_ERR_INVALID_ARG;
     StreamPlan P{};
@@ -1227,6 +1231,7 @@ extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_laye
     p.err = reinterpret_cast<int *>(ws + P.off_err);
     p.m3 = 8u;
     p.m15 = 32768u;
+    p.test_stall = (flags & W12_LAUNCH_TEST_STALL) ? 1 : 0;
     for (int k = 0; k < kKinds; ++k) p.kind[k] = P.kind[k];
     for (int l = 0; l < n_layers; ++l) {
         const w12_tensor *ts[kKinds] = {&layers[l].qkv, &layers[l].o, &layers[l].gate_up, &layers[l].down};
@@ -1271,6 +1276,11 @@ extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_laye
     }
     delete sp;
     return st;
+}
+
+extern "C" w12_status w12_stream_step(const w12_stream_layer *layers, int n_layers, int M, int n_q, float *h,
+                                      uint16_t *x_out, void *workspace, size_t workspace_bytes, w12_stream_t stream) {
+    return w12_stream_step_ex(layers, n_layers, M, n_q, h, x_out, workspace, workspace_bytes, 0u, stream);
 }
 
 extern "C" w12_status w12_stream_interleave(const uint16_t *gate, const uint16_t *up, int ffn, int hidden,

@@ -116,6 +116,7 @@ def lib() -> ctypes.CDLL:
             "w12_stream_workspace_size": ([ctypes.POINTER(CStreamLayer), i32, i32, i32, ctypes.POINTER(sz)], i32),
             "w12_stream_buffers": ([ctypes.POINTER(CStreamLayer), i32, i32, i32, ctypes.POINTER(sz)], i32),
             "w12_stream_step": ([ctypes.POINTER(CStreamLayer), i32, i32, i32, P, P, P, sz, P], i32),
+            "w12_stream_step_ex": ([ctypes.POINTER(CStreamLayer), i32, i32, i32, P, P, P, sz, ctypes.c_uint, P], i32),
             "w12_stream_interleave": ([P, P, i32, i32, P, P], i32),
         }
         for name, (args, res) in sig.items():
@@ -581,15 +582,19 @@ class StreamStep:
         self.n_qkv = layers[0]["qkv"].N
         self.ffn = layers[0]["down"].K
 
-    def __call__(self, h: torch.Tensor, x_out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-        """Runs the step on fp32 h [M, hidden] (updated in place); returns x_out = rms_bf16(final h)."""
+    def __call__(self, h: torch.Tensor, x_out: torch.Tensor | None = None, stream=None,
+                 test_stall: bool = False) -> torch.Tensor:
+        """Runs the step on fp32 h [M, hidden] (updated in place); returns x_out = rms_bf16(final h).
+        ``test_stall`` sets the ``W12_LAUNCH_TEST_STALL`` test hook (the failure path: the step's
+        bounded waits run out; ``check`` then raises and the workspace must be zeroed again)."""
         if h.dtype != torch.float32 or not h.is_contiguous() or tuple(h.shape) != (self.M, self.hidden):
             raise ValueError(f"h must be a contiguous fp32 tensor of shape ({self.M}, {self.hidden})")
         if x_out is None:
             x_out = torch.empty((self.M, self.hidden), dtype=torch.bfloat16, device=h.device)
         _check_out(x_out, self.M, self.hidden, (torch.bfloat16,))
-        _check(lib().w12_stream_step(self.arr, self.n, self.M, self.n_q, _ptr(h), _ptr(x_out), _ptr(self.ws),
-                                     self.ws_bytes, _stream(stream)), "w12_stream_step")
+        _check(lib().w12_stream_step_ex(self.arr, self.n, self.M, self.n_q, _ptr(h), _ptr(x_out), _ptr(self.ws),
+                                        self.ws_bytes, LAUNCH_TEST_STALL if test_stall else 0, _stream(stream)),
+               "w12_stream_step")
         return x_out
 
     def buffers(self) -> dict:

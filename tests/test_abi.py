@@ -176,5 +176,7 @@ def test_stream_argument_checks(w12):
     assert L.w12_stream_buffers(arr, 1, 8, 192, offs) == w12.ERR_INVALID_ARG
     assert L.w12_stream_step(arr, 1, 8, 192, None, one, one, 1 << 20, None) == w12.ERR_INVALID_ARG
     assert L.w12_stream_step(arr, 1, 8, 192, one, one, P(258), 1 << 20, None) == w12.ERR_INVALID_ARG  # misaligned
+    assert L.w12_stream_step_ex(arr, 1, 8, 192, None, one, one, 1 << 20, 0, None) == w12.ERR_INVALID_ARG
+    assert L.w12_stream_step_ex(arr, 1, 8, 192, one, one, one, 1 << 20, 8, None) == w12.ERR_INVALID_ARG  # flag
     assert L.w12_stream_interleave(None, one, 128, 64, one, None) == w12.ERR_INVALID_ARG
     assert L.w12_stream_interleave(one, one, 100, 64, one, None) == w12.ERR_UNSUPPORTED_SHAPE

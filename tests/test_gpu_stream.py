@@ -12,6 +12,8 @@
 - rows wider than one normalisation unit holds (the multi-pass normalisation, ragged last tiles)
   against the chain and the oracle;
 - repeated steps on one workspace give identical rows (its counters are left zeroed);
+- the failure path: under the test-stall hook the bounded waits run out and are reported, and a
+  step on the re-zeroed workspace is right;
 - shapes the kernel does not take are refused on the host.
 """
 import ctypes
@@ -180,6 +182,34 @@ def test_stream_repeat_and_counters(w12):
         assert torch.equal(x.view(torch.int16), outs[0][1].view(torch.int16))
     ws = step.ws.cpu().numpy()
     assert not ws[:4].any()  # the error word
+
+
+def test_stream_timeout_is_reported(w12):
+    """The failure path of the persistent kernel, without a GPU fault: under the
+    W12_LAUNCH_TEST_STALL hook each block's activation producer issues its first slot's copies
+    only, the MMAs' wait on the next slot gives up after about a second, every block stops (the
+    other blocks' waits on the phase counters run out too), and w12_check reports W12_ERR_TIMEOUT.
+    The context stays usable: once the workspace is zero-filled again, a step gives the rows of
+    the chain of separate launches."""
+    chain, step_layers, _ = make_layers(w12, 2, 256, 192, 64, 512, seed=91)
+    step = w12.StreamStep(step_layers, 8, 192)
+    h0 = synth.activations(8, 256, seed=92, device="cuda").float()
+    h = h0.clone()
+    step(h, test_stall=True)
+    with pytest.raises(w12.W12Error) as e:
+        step.check()
+    assert e.value.status == w12.ERR_TIMEOUT
+    step.ws.zero_()
+    h = h0.clone()
+    x = step(h)
+    step.check()
+    hc = h0.clone()
+    xc = chain_step(w12, chain, hc, 192, 512)
+    assert torch.equal(h.view(torch.int32), hc.view(torch.int32))
+    assert torch.equal(x.view(torch.int16), xc.view(torch.int16))
+    L = w12.lib()
+    assert L.w12_stream_step_ex(step.arr, step.n, step.M, step.n_q, w12._ptr(h), w12._ptr(x), w12._ptr(step.ws),
+                                step.ws_bytes, 8, None) == w12.ERR_INVALID_ARG  # an unknown flag
 
 
 def test_stream_refuses_shapes(w12):
