@@ -724,10 +724,15 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
             del wa, ta
     out["qpass_top1_agreement_M64"] = agree
     out["model_stream"] = model_stream(dev, th, wh, hbm_peak)
+    # the carried step again on the light recipe (no exact zeros: about one escape per record,
+    # the escape fraction the pages report for real models), labelled as such
+    light = model_stream(dev, th, wh, hbm_peak, layouts=("carried",), recipe=synth.LIGHT)
+    out["model_stream"]["by_layout"]["carried_light_recipe"] = light["by_layout"]["carried"]
     return out
 
 
-def model_stream(dev, th, wh, hbm_peak, Ms=(1, 16, 32), steps=5, layouts=("separate", "fused", "carried")):
+def model_stream(dev, th, wh, hbm_peak, Ms=(1, 16, 32), steps=5, layouts=("separate", "fused", "carried"),
+                 recipe=None):
     """One decoding step of the synthetic 64-layer model, captured once in a CUDA graph and
     replayed; the same sequence with bf16 cuBLAS on the unencoded weights beside it. Three
     layouts. Two stream the weights on fixed activations (no glue between the GEMMs): the seven
@@ -737,16 +742,18 @@ def model_stream(dev, th, wh, hbm_peak, Ms=(1, 16, 32), steps=5, layouts=("separ
     [Wq; Wk; Wv] holds the three tensors' records one after another. The third ("carried") is
     the step itself: M rows carried from layer to layer through the library's glue (row
     normalisation, residual adds fused into the GEMMs, the gate-up product): 257 GEMMs and 193
-    glue kernels; its cuBLAS counterpart runs the same chain with torch glue."""
+    glue kernels; its cuBLAS counterpart runs the same chain with torch glue. The layers' weights
+    follow `recipe` (default: the projection's, as stated)."""
     from lossless_bit_weight_gb300 import w12
 
+    recipe = synth.PROJ if recipe is None else recipe
     res = {"layers": 64, "by_layout": {}}
     stream = torch.cuda.Stream(device=dev)
     for layout in layouts:
         lin = []
         stream_layers = []
         for layer in range(64):
-            ws = {name: synth.weights(n_out, k_in, synth.PROJ, seed=synth.seed_for(3, 100 * layer + li), device=dev)
+            ws = {name: synth.weights(n_out, k_in, recipe, seed=synth.seed_for(3, 100 * layer + li), device=dev)
                   for li, (name, k_in, n_out) in enumerate(synth.LAYER_LINEARS)}
             groups = {"separate": [["q"], ["k"], ["v"], ["o"], ["gate"], ["up"], ["down"]],
                       "fused": [["q", "k", "v"], ["o"], ["gate", "up"], ["down"]],
