@@ -291,11 +291,12 @@ w12_stream_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant_
 
     if (warp == kWProducer) {
         // ---------------------------------------------------------------- producer (warp-wide)
-        // Activation tiles of each slot, in slot order: once the slot's ring position is free and
-        // the phase that writes the GEMM's input has completed on every block. The records of the
-        // slots go out from the escape feeder, which runs up to a ring's depth ahead of the
-        // activations, across GEMM boundaries. This loop stays short: the warp shares its
-        // scheduler with three decode warps, and every instruction here delays the next copy.
+        // Activation tiles of each slot, in slot order: once the slot's tensor-memory position is
+        // free (its tiles sit beside it) and the phase that writes the GEMM's input has completed
+        // on every block. The records of the slots go out from the escape feeder, which runs up to
+        // both rings' depth ahead of the activations, across GEMM boundaries. This loop stays
+        // short: the warp shares its scheduler with three decode warps, and every instruction here
+        // delays the next copy.
         SlotIt xi = start;
         RingS xr;
         int known = 0;  // phases [0, known) are known to be complete on every block
