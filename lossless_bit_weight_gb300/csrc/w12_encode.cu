@@ -67,14 +67,34 @@ window_kernel(const uint16_t *__restrict__ w, int N, int K, int k_tiles, uint8_t
         }
     }
     __syncwarp();
-    // best window: largest coverage, then smallest base
+    // best window: largest coverage, then smallest base. Lane l holds bins 8l .. 8l + 7 as the
+    // histogram's inclusive prefix P; the window [E - 15, E] covers P[E] - P[E - 16] weights,
+    // P[E - 16] being the same slot of lane l - 2
+    uint32_t P[8];
+    {
+        const uint4 h0 = reinterpret_cast<const uint4 *>(h)[2 * lane];
+        const uint4 h1 = reinterpret_cast<const uint4 *>(h)[2 * lane + 1];
+        P[0] = h0.x; P[1] = h0.y; P[2] = h0.z; P[3] = h0.w;
+        P[4] = h1.x; P[5] = h1.y; P[6] = h1.z; P[7] = h1.w;
+    }
+#pragma unroll
+    for (int j = 1; j < 8; ++j) P[j] += P[j - 1];
+    uint32_t incl = P[7];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    const uint32_t lane_before = incl - P[7];
     uint32_t best_c = 0;
     int best_E = 1 << 30;
-    for (int E = 16 + lane; E <= 254; E += 32) {
-        uint32_t c = 0;
 #pragma unroll
-        for (int d = 0; d < 16; ++d) c += h[E - d];
-        if (c > best_c || (c == best_c && E < best_E)) {
+    for (int j = 0; j < 8; ++j) {
+        P[j] += lane_before;
+        const uint32_t lo = __shfl_up_sync(0xFFFFFFFFu, P[j], 2);
+        const int E = 8 * lane + j;
+        const uint32_t c = P[j] - lo;
+        if (E >= 16 && E <= 254 && (c > best_c || (c == best_c && E < best_E))) {
             best_c = c;
             best_E = E;
         }
@@ -184,8 +204,8 @@ __device__ __forceinline__ uint32_t block_excl_scan256(uint32_t v, uint32_t *tot
 }
 
 // one block per record: planes of its 128 x 64 weights, the record bytes, its index segment and
-// its share of the per-channel lists
-__global__ void __launch_bounds__(256) pack_kernel(PackArgs a) {
+// its share of the per-channel lists; at most 40 registers, so that six blocks share an SM
+__global__ void __launch_bounds__(256, 6) pack_kernel(PackArgs a) {
     const int r = blockIdx.x;
     const int nt = r / a.k_tiles, kt = r % a.k_tiles;
     const int nl = threadIdx.x >> 1, half = threadIdx.x & 1;
