@@ -22,7 +22,7 @@
 namespace w12 {
 namespace {
 
-constexpr int kWindowWarps = 8;
+constexpr int kWindowWarps = 4;  // channels (warps) per window block (4: 56.6 us for the projection, 8: 57.9)
 constexpr int kScanThreads = 1024;
 constexpr int kScanPer = 8;     // values per scan thread per tile (8: 12.0 us for the projection, 16: 14.1, 32: 13.6)
 constexpr int kWinBatch = 4;    // 16-byte loads in flight per lane in the window pass
