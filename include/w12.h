@@ -220,7 +220,7 @@ w12_status w12_gemm_noalloc(const w12_tensor *t, const uint16_t *x, int M, void 
                             w12_stream_t stream);
 
 /* ---- glue of the synthetic layer stream (the pages give no layer dataflow) ---------------
- * The synthetic 64-layer stream carries M rows from layer to layer (the build's reading): h fp32
+ * The synthetic 64-layer stream carries M rows from layer to layer (the reading taken here): h fp32
  * [M, K]; x = bf16(h / rms(h)); a = bf16(x Wq^T); h += a Wo^T (W12_LAUNCH_ACCUMULATE);
  * x2 = bf16(h / rms(h)); p = bf16((x2 Wg^T) * (x2 Wu^T)); h += p Wd^T. These two calls are its
  * steps between the GEMMs. flags: 0 or W12_LAUNCH_OVERLAP (the kernel may start while the
@@ -242,7 +242,7 @@ w12_status w12_mul_bf16(const float *g, const float *u, int M, int N, int ld, ui
                         w12_stream_t stream);
 
 /* ---- f3: the persistent cross-GEMM kernel of the layer stream (SpecPilot App. F and Table
- *      A7, "persistent cross-GEMM W12": one kernel over a sequence of W12 GEMMs) ---------------
+ *      A7: one persistent kernel over a sequence of W12 GEMMs) -----------------------------------
  * One cooperative launch runs a whole decoding step of the synthetic layer stream above, every
  * GEMM and every glue step of n_layers layers, then the final row normalisation:
  *   per layer  x = rms_bf16(h); qkv = bf16(x Wqkv^T); h += qkv[:, :n_q] Wo^T;

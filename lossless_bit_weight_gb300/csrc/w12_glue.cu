@@ -1,5 +1,5 @@
 // Glue of the synthetic layer stream: the steps between the GEMMs when M rows are carried from
-// layer to layer (the pages give no layer dataflow; the build's reading is h fp32,
+// layer to layer (the pages give no layer dataflow; the reading taken here is h fp32,
 // x = bf16(h / rms(h)), a = bf16(x Wq^T), h += a Wo^T, x2 = bf16(h / rms(h)),
 // p = bf16((x2 Wg^T) * (x2 Wu^T)), h += p Wd^T). The residual adds are the GEMM's accumulate
 // mode; the row normalisation and the gate-up product are the two kernels here. Both are tiny

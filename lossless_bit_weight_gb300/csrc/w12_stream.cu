@@ -1,9 +1,9 @@
-// f3 — the persistent cross-GEMM W12 kernel (SpecPilot App. F and Table A7, "persistent
-// cross-GEMM W12": one kernel that runs a sequence of W12 GEMMs instead of a launch per GEMM; the
-// pages measured it on H100 and closed it there).
+// f3 — the persistent cross-GEMM W12 kernel (SpecPilot App. F and Table A7: one kernel that
+// runs a sequence of W12 GEMMs instead of a launch per GEMM; the pages measured it on H100 and
+// closed it there).
 //
 // One cooperative launch runs a whole decoding step of the synthetic layer stream (the pages give
-// no layer dataflow; the build's reading carries M rows h fp32 from layer to layer):
+// no layer dataflow; the reading taken here carries M rows h fp32 from layer to layer):
 //   per layer   x  = bf16(h / rms(h))                       row-normalisation phase
 //               qkv = bf16(x Wqkv^T)                        GEMM (k and v are computed and dropped)
 //               h += qkv[:, :n_q] Wo^T                      GEMM, added into h

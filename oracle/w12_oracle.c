@@ -23,10 +23,10 @@
  *   - INT6 Q-pass copy (per-row scale, 6-bit codes, its GEMM): [SP] §5.3 "Generality Through
  *     Memory"; App. C.
  *   - glue of the synthetic layer stream (residual add, row normalisation, gate-up product):
- *     no page gives a layer dataflow; these follow the build's written reading of one.
+ *     no page gives a layer dataflow; these follow the library's written reading of one.
  *
  * Physical details the pages leave open (window tie rule, placeholders, byte and nibble order,
- * per-record escape index) follow the build's written W12 specification; every function states
+ * per-record escape index) follow the library's written W12 specification; every function states
  * the rule it implements. Parity status: every function here is pinned by a CPU test
  * (round trip over all 65,536 bf16 patterns, brute-force window search, exact rational GEMM,
  * brute-force argmax, hand-derived byte fixtures, the lossless case of the INT6 copy, rounding
@@ -100,7 +100,7 @@ static void planes_of(uint16_t u, int En, int *E, int *mhi, int *b, int *s) {
     }
 }
 
-/* ---- record byte placement (the build's specification of the 12 KB record) --------------- */
+/* ---- record byte placement (the library's specification of the 12 KB record) --------------- */
 
 static size_t view_offset(int nl, int kl) { return (size_t)2048 * (kl >> 4) + 16 * nl + (kl & 15); }
 static size_t b_word_offset(int nl, int kl) {
@@ -366,7 +366,7 @@ void w12o_set_threads(int n) { (void)n; }
  * [SP] §4.1 "Certified LM head": an INT8 copy of the head whose per-row Cauchy-Schwarz error
  * bound discards every token that provably cannot be the argmax; the survivors are rescored
  * exactly, and the full head runs when too many survive. The pages give no formulas; this is
- * the plainest reading, in the build's written specification:
+ * the plainest reading, in the library's written specification:
  *   scale   s_n = fp32(max_k |w[n,k]| / 127)   (0 for an all-zero row)
  *   code    q[n,k] = round-half-even(w[n,k] / s_n), clamped to [-127, 127]
  *   residual c_n = || w[n,:] - s_n q[n,:] ||_2          (+inf if the row holds Inf or NaN)
@@ -474,7 +474,7 @@ void w12o_certified_argmax(const uint16_t *x, int M, const uint16_t *w, int N, i
 /* ---- INT6 Q-pass copy -------------------------------------------------------------------
  * [SP] §5.3 ("DSpark also added the INT6 copy for the Q pass"; "an INT6/INT8 Q-pass copy") and
  * App. C (the Q pass reads the nested 8-bit view or a separate low-precision copy). The pages
- * give no formulas; the plainest reading, fixed in the build's written specification, is the
+ * give no formulas; the plainest reading, fixed in the library's written specification, is the
  * INT8 copy's per-row symmetric quantisation with 6-bit codes:
  *   scale   s_n = fp32(max_k |w[n,k]| / 31)  (0 for an all-zero row and for a row holding Inf
  *                                             or NaN, whose codes are then all 0)
@@ -509,7 +509,7 @@ void w12o_copy_q6(const uint16_t *w, int N, int K, float *scale, int8_t *q) {
     }
 }
 
-/* The INT6 copy's records, from row-major codes c [N,K] (build's specification). One record
+/* The INT6 copy's records, from row-major codes c [N,K] (the library's specification). One record
  * per 128 x 64 tile, record r = n_tile * k_tiles + k_tile, 6144 bytes, holding u = c + 32
  * (1..63; padding rows and columns hold code 0, u = 32) as two planes of 32-bit little-endian
  * words. For local row n_l, k_l = 16 g + 2 j + h (group g 0..3, pair j 0..7, half h 0..1):
@@ -571,7 +571,7 @@ void w12o_gemm_q6(const uint16_t *x, int M, const int8_t *q, const float *scale,
 
 /* ---- glue of the synthetic layer stream --------------------------------------------------
  * The pages give no layer dataflow; the synthetic 64-layer stream that carries M rows from layer
- * to layer (the build's reading) needs three steps besides the GEMMs: the residual add (y += x W^T,
+ * to layer (the reading taken here) needs three steps besides the GEMMs: the residual add (y += x W^T,
  * one fp32 addition per output), the row normalisation and the gate-up product below. */
 
 /* bf16 bits of a double, rounded to nearest even (normal, subnormal, overflow to Inf, NaN). */

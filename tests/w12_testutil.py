@@ -1,6 +1,6 @@
 """Shared checks for the GPU parity tests: the GEMM error bound and the argmax near-tie rule.
 
-Tolerances (fixed by the build's task statement for this path):
+Tolerances (the GEMM's stated accuracy bound for this path):
   fp32 y:  |y - y_ref| <= 2e-3 * sum_k |x_k w_k| + 1e-6 per element (y_ref in fp64)
   bf16 y:  within one bf16 ulp of the fp64 reference, plus the fp32 bound above
   argmax:  top-1 must equal the fp64 oracle's wherever the oracle's top-1/top-2 gap exceeds
