@@ -699,9 +699,9 @@ def extras(w, t0, copies, xs, dev, hbm_peak, tc_peak, l2):
                      "overlap_weight_gbs": round(th.gemm_bytes() / (ao_us * 1e-6) / 1e9, 1),
                      "qview_overlap_us": round(q_us, 1),
                      "cublas_linear_argmax_us": round(c_us, 1)}
-    # Q-pass top-1 agreement with the exact argmax on the 151936-wide head at M = 64 (reported,
-    # not pinned): the nested view (escapes clamped to the window, low mantissa bits := 1000b),
-    # the INT8 and the INT6 copies; on the head recipe and on the same recipe without the planted
+    # how often the Q pass picks the same top-1 token as the exact argmax, on the 151936-wide
+    # head at M = 64 (reported, not pinned): the nested view (escapes clamped to the window,
+    # low mantissa bits := 1000b), the INT8 and the INT6 copies; on the head recipe and on the same recipe without the planted
     # 2^12 outliers (which the view clamps and which dominate these logits)
     x64 = synth.activations(64, K_HID, seed=synth.seed_for(4, 64), device=dev)
     agree = {}

@@ -3,11 +3,11 @@
  *
  * W12 is the lossless 12-bit weight format of "SpecPilot: Autonomous Algorithm Discovery and
  * Systems Optimization for Speculative Decoding" (arXiv 2611.02501), §4.1 "W12: A Lossless
- * 12-bit Weight Format" and Fig. 5: each BF16 weight of an output channel is stored as three
- * 4-bit planes (A: sign and top three mantissa bits; E: exponent offset inside the channel's
- * 16-binade window [E_n-15, E_n]; B: low four mantissa bits); weights outside the window, zeros
- * and denormals go to an exact escape list; 12 KB records cover 128x64 weight tiles with the
- * 8-bit A+E view first and plane B last.
+ * 12-bit Weight Format" and Fig. 5: a BF16 weight is kept as three nibbles (A: its sign and
+ * three highest mantissa bits; E: its exponent relative to the channel's 16-binade window
+ * [E_n-15, E_n]; B: its four lowest mantissa bits); a weight the nibbles cannot hold (exponent
+ * out of the window, zero, subnormal, Inf, NaN) is kept bit for bit in an escape list; 12 KB
+ * records hold 128x64 weight tiles, the 8-bit A+E view first and plane B last.
  *
  * Conventions for every call
  *   - Memory: every data pointer is a DEVICE pointer owned by the caller. The library never
@@ -117,8 +117,8 @@ w12_status w12_encode_sizes(const uint16_t *w, int N, int K, void *scratch, size
 w12_status w12_encode(const uint16_t *w, int N, int K, void *scratch, size_t scratch_bytes,
                       const w12_tensor *t, w12_stream_t stream);
 
-/* ---- a2: load-time check (SpecPilot §4.1: "checks every decoded tensor against the
- *          checkpoint bit for bit"; Table A2 caption) ----------------------------------------- */
+/* ---- a2: load-time check (SpecPilot §4.1; Table A2 caption: the decoded weights are compared
+ *          bit for bit with the checkpoint when the model loads) ------------------------------ */
 
 /* Decodes the whole tensor into w_out (device bf16 [N, K]) from records, base_exp and the
  * per-record escape index. Asynchronous. */
@@ -143,8 +143,8 @@ w12_status w12_workspace_size(const w12_tensor *t, int M, int op, size_t *bytes)
 
 /* a3 (SpecPilot §4.1 and Fig. 5b; §6.3): y[m, n] = sum_k x[m, k] * w[n, k] with every weight
  * decoded exactly in registers and fp32 accumulation; y is fp32 or bf16 (round to nearest even)
- * [M, N] by y_dtype. x: device bf16 [M, K], 16-byte aligned. Deterministic split of the
- * reduction over thread blocks in a fixed order. Asynchronous. */
+ * [M, N] by y_dtype. x: device bf16 [M, K], 16-byte aligned. When the k range is split
+ * between blocks, their parts are added in one fixed order (run-to-run identical). Asynchronous. */
 w12_status w12_gemm(const w12_tensor *t, const uint16_t *x, int M, void *y, int y_dtype,
                     void *workspace, size_t workspace_bytes, w12_stream_t stream);
 
@@ -314,9 +314,10 @@ w12_status w12_gemm_config(const w12_tensor *t, int M, int op, int *grid, int *s
                            int *smem_bytes);
 
 /* ---- certified LM head (SpecPilot §4.1 "Certified LM head") ------------------------------
- * An INT8 copy of the head whose per-row Cauchy-Schwarz bound discards every token that
- * provably cannot be the argmax; the survivors are rescored exactly from the W12 head, and when
- * a row has too many survivors the full W12 argmax runs instead. The argmax and the top-1/top-2
+ * The head is also kept as INT8 codes with a bound per row (Cauchy-Schwarz on the quantisation
+ * residual); a token whose upper bound falls below another token's lower bound cannot win and is
+ * dropped, the tokens left are scored again from the W12 head, and a row that keeps too many
+ * falls back to the full W12 argmax. The argmax and the top-1/top-2
  * gap are those of the whole head.
  *
  * The copy, per output row n of the bf16 head W [N, K] (the readings the pages leave open):

@@ -1,7 +1,8 @@
-// Certified LM head (SpecPilot §4.1 "Certified LM head"): an INT8 copy of the head with a
-// per-row Cauchy-Schwarz error bound. Tokens that provably cannot be the argmax are discarded;
-// the survivors are rescored from the exact weights of the W12 head, with fp32 accumulation;
-// with too many survivors the full W12 argmax runs instead. The argmax is that of the whole
+// Certified LM head (SpecPilot §4.1 "Certified LM head"): the head also kept as INT8 codes with
+// a bound per row (Cauchy-Schwarz on the quantisation residual). A token whose upper bound lies
+// below another token's lower bound cannot win and is dropped; the tokens left are scored again
+// from the exact weights of the W12 head, with fp32 accumulation; a row that keeps too many
+// falls back to the full W12 argmax. The argmax is that of the whole
 // head, under the same near-tie rule as the fused argmax: a rescored logit carries fp32
 // summation error, so rows whose top-1/top-2 gap is within that error may rank either way.
 //

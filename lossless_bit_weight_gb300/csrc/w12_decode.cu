@@ -1,7 +1,7 @@
 // a2 — W12 decode and the load-time bit-for-bit check.
 //
-// SpecPilot §4.1: "At load time, the server checks every decoded tensor against the checkpoint
-// bit for bit" (also the caption of Table A2). One block per 128x64 record: 256 threads, each
+// SpecPilot §4.1 and the caption of Table A2: when the model loads, each decoded tensor is
+// compared bit for bit with the checkpoint. One block per 128x64 record: 256 threads, each
 // decodes 32 weights of one channel row (two view chunks, one plane-B chunk) with the same
 // in-register decode the GEMM uses, then the record's escapes are restored from the per-record
 // index. HBM-bound: 1.5 B/weight read (+2 B/weight written or compared).

@@ -1,10 +1,10 @@
 // a1 — W12 encoder on the GPU.
 //
-// SpecPilot §4.1 "W12: A Lossless 12-bit Weight Format" and Fig. 5a: per output channel choose
-// the 16-binade window [E_n-15, E_n] covering the most weights; store in-window weights as a
-// sign/top-mantissa nibble, an exponent-offset nibble and a low-mantissa nibble; send weights
-// outside the window, zeros and denormals to an exact escape list. Ties of the window choice
-// go to the smallest E_n; placeholders, byte/nibble order and the per-record escape index follow
+// SpecPilot §4.1 "W12: A Lossless 12-bit Weight Format" and Fig. 5a: each output channel gets
+// the 16-binade window [E_n-15, E_n] that holds the largest number of its weights; a weight
+// whose exponent falls in it is written as three nibbles (sign and high mantissa bits, exponent
+// offset, low mantissa bits), every other weight (exponent out of the window, zero, subnormal)
+// is kept bit for bit in an escape list. Ties of the window choice go to the smallest E_n; placeholders, byte/nibble order and the per-record escape index follow
 // the library's written format specification.
 //
 // Passes (all HBM-streaming, integer only):

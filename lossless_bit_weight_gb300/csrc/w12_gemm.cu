@@ -1,9 +1,10 @@
 // a3/a4/a5 — the skinny W12 GEMM on 5th-generation tensor cores (tcgen05, sm_103a).
 //
-// SpecPilot §4.1 and Fig. 5b: the GEMM decodes W12 records in registers so that the memory
-// stream hides the decode, and splits the reduction over thread blocks in a fixed order so the
-// result is deterministic; §6.3 and App. E: it is bound by weight bytes at 1-32 rows; §4.3: the
-// Q pass reads only the nested 8-bit view; §2.1: greedy verification takes the row argmax.
+// SpecPilot §4.1 and Fig. 5b: the weights are expanded from W12 on chip, inside the GEMM, where
+// the expansion overlaps the weight stream from memory; the k range is shared out between
+// blocks whose parts are added in an order that never changes, so results repeat bit for bit;
+// §6.3 and App. E: it is bound by weight bytes at 1-32 rows; §4.3: the Q pass reads only the
+// nested 8-bit view; §2.1: greedy verification takes the row argmax.
 //
 // Design on GB300 (one persistent block per SM, 8 + 4*G warps with G = W12_DECODE_GROUPS decode
 // groups, 20 warps by default). Work moves through a ring of

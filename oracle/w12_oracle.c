@@ -58,8 +58,8 @@ double w12o_bf16_to_double(uint16_t u) {
     return (double)f;
 }
 
-/* ---- window choice: [SP] §4.1 ("for each channel n, W12 selects the 16-binade window
- *      [E_n-15, E_n] that covers the most weights"); ties -> smallest E_n ---------------- */
+/* ---- window choice: [SP] §4.1 (per channel n, the 16-binade window [E_n-15, E_n] holding
+ *      the largest number of the channel's weights); ties -> smallest E_n ------------------ */
 
 int w12o_window(const uint16_t *row, int K) {
     long hist[256];
@@ -362,10 +362,11 @@ int w12o_threads(void) { return 1; }
 void w12o_set_threads(int n) { (void)n; }
 #endif
 
-/* ---- certified LM head: an INT8 copy with a per-row error bound -----------------------------
- * [SP] §4.1 "Certified LM head": an INT8 copy of the head whose per-row Cauchy-Schwarz error
- * bound discards every token that provably cannot be the argmax; the survivors are rescored
- * exactly, and the full head runs when too many survive. The pages give no formulas; this is
+/* ---- certified LM head: INT8 codes of the head and a bound per row ---------------------------
+ * [SP] §4.1 "Certified LM head": INT8 codes of the head with a Cauchy-Schwarz bound per row;
+ * a token whose upper bound lies below another's lower bound cannot win and is dropped, the
+ * rest are scored again exactly, and a row keeping too many falls back to the whole head. The
+ * pages give no formulas; this is
  * the plainest reading, in the library's written specification:
  *   scale   s_n = fp32(max_k |w[n,k]| / 127)   (0 for an all-zero row)
  *   code    q[n,k] = round-half-even(w[n,k] / s_n), clamped to [-127, 127]
@@ -472,8 +473,8 @@ void w12o_certified_argmax(const uint16_t *x, int M, const uint16_t *w, int N, i
 }
 
 /* ---- INT6 Q-pass copy -------------------------------------------------------------------
- * [SP] §5.3 ("DSpark also added the INT6 copy for the Q pass"; "an INT6/INT8 Q-pass copy") and
- * App. C (the Q pass reads the nested 8-bit view or a separate low-precision copy). The pages
+ * [SP] §5.3 (a later drafter brought an INT6 copy for the Q pass; INT6 and INT8 Q-pass copies
+ * are both named) and App. C (the Q pass reads the nested 8-bit view or a separate low-precision copy). The pages
  * give no formulas; the plainest reading, fixed in the library's written specification, is the
  * INT8 copy's per-row symmetric quantisation with 6-bit codes:
  *   scale   s_n = fp32(max_k |w[n,k]| / 31)  (0 for an all-zero row and for a row holding Inf

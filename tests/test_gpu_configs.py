@@ -217,5 +217,5 @@ def test_qview_argmax_and_agreement_on_lm_head(w12):
             assert wrong == 0, det
             assert checked >= 14
         del w, t
-    print("Q-pass top-1 agreement with the exact pass on the LM head at M=64: "
+    print("share of rows where the Q pass picks the exact top-1 token, LM head, M=64: "
           + ", ".join(f"{k} {v:.3f}" for k, v in rates.items()))
