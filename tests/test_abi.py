@@ -180,3 +180,96 @@ def test_stream_argument_checks(w12):
     assert L.w12_stream_step_ex(arr, 1, 8, 192, one, one, one, 1 << 20, 8, None) == w12.ERR_INVALID_ARG  # flag
     assert L.w12_stream_interleave(None, one, 128, 64, one, None) == w12.ERR_INVALID_ARG
     assert L.w12_stream_interleave(one, one, 100, 64, one, None) == w12.ERR_UNSUPPORTED_SHAPE
+
+
+def _fake_tensor(w12, N, K):
+    """A descriptor with the right shape and aligned buffer addresses that no call below reads:
+    each fails its argument check before any device work."""
+    t = w12.CTensor()
+    assert w12.lib().w12_tensor_shape(N, K, ctypes.byref(t), None, None) == w12.OK
+    t.records, t.base_exp, t.esc_off, t.rec_esc_off = 0x10000, 0x20000, 0x30000, 0x40000
+    return t
+
+
+def _fake_q8(w12, N, K):
+    h = w12.CQ8Head()
+    assert w12.lib().w12_q8_shape(N, K, ctypes.byref(h), None, None) == w12.OK
+    h.codes, h.scale, h.bound = 0x50000, 0x60000, 0x70000
+    return h
+
+
+@pytest.mark.parametrize("N,K", [(151936, 5120), (130, 72)])
+def test_int8_head_shape_and_argument_checks(w12, N, K):
+    """The certified head's INT8 copy: its sizes (8192-byte records, one fp32 scale and bound per
+    padded row), and its calls' argument checks, all on the host."""
+    L = w12.lib()
+    P = ctypes.c_void_p
+    one = P(0x80000)
+    h = w12.CQ8Head()
+    cb, rb, nb = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    assert L.w12_q8_shape(N, K, ctypes.byref(h), ctypes.byref(cb), ctypes.byref(rb)) == w12.OK
+    nt, kt = -(-N // 128), -(-K // 64)
+    assert (h.N, h.K, h.n_tiles, h.k_tiles) == (N, K, nt, kt)
+    assert cb.value == nt * kt * 8192 and rb.value == 4 * nt * 128
+    assert L.w12_q8_shape(N, 12, ctypes.byref(h), None, None) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_q8_shape(N, K, None, None, None) == w12.ERR_INVALID_ARG
+    # no buffers in h yet
+    assert L.w12_q8_build(one, ctypes.byref(h), None) == w12.ERR_INVALID_ARG
+    assert L.w12_q8_argmax_workspace_size(ctypes.byref(h), 1, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    hq = _fake_q8(w12, N, K)
+    assert L.w12_q8_build(None, ctypes.byref(hq), None) == w12.ERR_INVALID_ARG
+    assert L.w12_q8_argmax_workspace_size(ctypes.byref(hq), 1, None) == w12.ERR_INVALID_ARG
+    # the Q pass over the copy takes W12_LAUNCH_OVERLAP only
+    assert L.w12_q8_argmax(ctypes.byref(hq), one, 1, one, one, one, w12.LAUNCH_TEST_STALL, one, 1 << 20,
+                           None) == w12.ERR_INVALID_ARG
+    hq.n_tiles += 1  # a descriptor whose tile counts do not match its shape
+    assert L.w12_q8_build(one, ctypes.byref(hq), None) == w12.ERR_INVALID_ARG
+
+
+def test_certified_head_argument_checks(w12):
+    """w12_certified_workspace_size and w12_lmhead_certified reject a W12 head and an INT8 copy of
+    different shapes, and row counts outside [1, W12_MAX_M], before any device work."""
+    L = w12.lib()
+    P = ctypes.c_void_p
+    one = P(0x80000)
+    nb = ctypes.c_size_t()
+    t = _fake_tensor(w12, 1024, 512)
+    h = _fake_q8(w12, 1024, 512)
+    other = _fake_q8(w12, 1152, 512)
+    assert L.w12_certified_workspace_size(ctypes.byref(t), ctypes.byref(h), 1, None) == w12.ERR_INVALID_ARG
+    assert L.w12_certified_workspace_size(None, ctypes.byref(h), 1, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    assert L.w12_certified_workspace_size(ctypes.byref(t), ctypes.byref(other), 1,
+                                          ctypes.byref(nb)) == w12.ERR_INVALID_ARG
+    assert L.w12_certified_workspace_size(ctypes.byref(t), ctypes.byref(h), 0,
+                                          ctypes.byref(nb)) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_certified_workspace_size(ctypes.byref(t), ctypes.byref(h), w12.MAX_M + 1,
+                                          ctypes.byref(nb)) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_lmhead_certified(ctypes.byref(t), ctypes.byref(other), None, one, 1, one, one, one, None, one,
+                                  1 << 20, None) == w12.ERR_INVALID_ARG
+
+
+def test_gemm_launch_options_and_config_checks(w12):
+    """w12_gemm_ex: unknown ops, an argmax op given y, and a GEMM op given argmax outputs are
+    rejected; w12_gemm_config rejects row counts and ops it does not take; w12_check rejects a
+    missing or too small workspace. All before any device work."""
+    L = w12.lib()
+    P = ctypes.c_void_p
+    one = P(0x80000)
+    t = _fake_tensor(w12, 17408, 5120)
+    g, s, m = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    for op in (-1, 4, 99):
+        assert L.w12_gemm_ex(ctypes.byref(t), one, 1, op, one, 0, None, None, None, 0, one, 1 << 20,
+                             None) == w12.ERR_INVALID_ARG
+    assert L.w12_gemm_ex(ctypes.byref(t), one, 1, w12.OP_ARGMAX, one, 0, one, one, one, 0, one, 1 << 20,
+                         None) == w12.ERR_INVALID_ARG
+    assert L.w12_gemm_ex(ctypes.byref(t), one, 1, w12.OP_GEMM, one, 0, one, None, None, 0, one, 1 << 20,
+                         None) == w12.ERR_INVALID_ARG
+    assert L.w12_gemm_config(None, 1, w12.OP_GEMM, ctypes.byref(g), ctypes.byref(s),
+                             ctypes.byref(m)) == w12.ERR_INVALID_ARG
+    for M in (0, w12.MAX_M + 1):
+        assert L.w12_gemm_config(ctypes.byref(t), M, w12.OP_GEMM, ctypes.byref(g), ctypes.byref(s),
+                                 ctypes.byref(m)) == w12.ERR_UNSUPPORTED_SHAPE
+    assert L.w12_gemm_config(ctypes.byref(t), 1, 99, ctypes.byref(g), ctypes.byref(s),
+                             ctypes.byref(m)) == w12.ERR_INVALID_ARG
+    assert L.w12_check(None, 16, None) == w12.ERR_INVALID_ARG
+    assert L.w12_check(one, 8, None) == w12.ERR_INVALID_ARG
