@@ -1365,7 +1365,7 @@ w12_status lmhead_argmax_if(const w12_tensor *t, const uint16_t *x, int M, int32
 extern "C" w12_status w12_workspace_size(const w12_tensor *t, int M, int op, size_t *bytes) {
     using namespace w12;
     W12_TRY(check_tensor(t));
-    if (!bytes) return W12_ERR_INVALID_ARG;
+    if (!bytes || op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) return W12_ERR_INVALID_ARG;
     Layout L{};
     W12_TRY(plan(t, M, op, &L));
     *bytes = L.ws_bytes;
@@ -1376,6 +1376,7 @@ extern "C" w12_status w12_gemm_config(const w12_tensor *t, int M, int op, int *g
                                       int *smem_bytes) {
     using namespace w12;
     W12_TRY(check_tensor(t));
+    if (op < W12_OP_GEMM || op > W12_OP_QVIEW_ARGMAX) return W12_ERR_INVALID_ARG;
     Layout L{};
     W12_TRY(plan(t, M, op, &L));
     if (grid) *grid = L.grid;

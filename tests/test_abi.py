@@ -250,8 +250,8 @@ def test_certified_head_argument_checks(w12):
 
 def test_gemm_launch_options_and_config_checks(w12):
     """w12_gemm_ex: unknown ops, an argmax op given y, and a GEMM op given argmax outputs are
-    rejected; w12_gemm_config rejects row counts and ops it does not take; w12_check rejects a
-    missing or too small workspace. All before any device work."""
+    rejected; w12_gemm_config and w12_workspace_size reject row counts and ops they do not take;
+    w12_check rejects a missing or too small workspace. All before any device work."""
     L = w12.lib()
     P = ctypes.c_void_p
     one = P(0x80000)
@@ -269,7 +269,10 @@ def test_gemm_launch_options_and_config_checks(w12):
     for M in (0, w12.MAX_M + 1):
         assert L.w12_gemm_config(ctypes.byref(t), M, w12.OP_GEMM, ctypes.byref(g), ctypes.byref(s),
                                  ctypes.byref(m)) == w12.ERR_UNSUPPORTED_SHAPE
-    assert L.w12_gemm_config(ctypes.byref(t), 1, 99, ctypes.byref(g), ctypes.byref(s),
-                             ctypes.byref(m)) == w12.ERR_INVALID_ARG
+    nb = ctypes.c_size_t()
+    for op in (-1, 4, 99, 100, 103):  # only the four W12_OP_* codes
+        assert L.w12_gemm_config(ctypes.byref(t), 1, op, ctypes.byref(g), ctypes.byref(s),
+                                 ctypes.byref(m)) == w12.ERR_INVALID_ARG
+        assert L.w12_workspace_size(ctypes.byref(t), 1, op, ctypes.byref(nb)) == w12.ERR_INVALID_ARG
     assert L.w12_check(None, 16, None) == w12.ERR_INVALID_ARG
     assert L.w12_check(one, 8, None) == w12.ERR_INVALID_ARG
